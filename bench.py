@@ -1,0 +1,342 @@
+#!/usr/bin/env python3
+"""MoE-layer throughput on one GB300 per rank.
+
+Workload (default): the decode verify window -- one MoE layer, 4 tokens,
+hidden 2048, 512 experts top-10, expert intermediate 512, a shared expert
+(intermediate 512, sigmoid gate), 4-bit block-scaled weights, Zipf(1.1)
+router bias, 50% of the experts resident in cache slots and the rest in
+device staging slots.  One step = one pass of the hot path over a fresh
+4-token window: router, top-k, expert groups, residency lookup, gate/up,
+down, combine with the gated shared expert, and the heat-counter update.
+The L2 is flushed (a 256 MB write) before every timed step; the flush is
+outside the step's CUDA-event pair.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the same workload instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+DEFAULT_WORKLOAD = "decode_t4_h2048_e512_k10"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget for cpu_baseline")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", self.gpu_id], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(self.rows),
+                "power_w_max": max((float(r[3]) for r in self.rows if r[3].replace(".", "").isdigit()), default=None)}
+
+
+def gpu_id_for(dev) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------- oracle leg
+def oracle_sample(w, seconds: float, tokens_per_call=None):
+    """Time the CPU oracle on windows of the workload until ~`seconds` elapse.
+    Returns (tokens/s, tokens, calls, wall seconds)."""
+    from oracle import layer as olayer
+    from serving_router_top_gb300 import inputs as I
+    s = w.shape
+    li = I.layer_inputs(w)
+    experts = {}
+
+    def get(e):
+        if e not in experts:
+            experts[e] = I.expert_weights(w.seed, 0, e, s.H, s.I)
+        return experts[e]
+
+    for e in range(s.E):       # generation is input preparation, not oracle work
+        get(e)
+    mask = I.resident_mask(w.seed, 0, s.E, w.resident_frac)
+    resid = np.where(mask, np.cumsum(mask) - 1, -1).astype(np.int32)
+    stage = np.where(~mask, np.cumsum(~mask) - 1, -1).astype(np.int32)
+    T = w.T if tokens_per_call is None else tokens_per_call
+    tokens = calls = 0
+    t0 = time.perf_counter()
+    while True:
+        x = I.activations(w.seed, 1000 + calls, T, s.H)
+        olayer.moe_layer(x, li.w_router, li.bias, s.k, get, s.H, s.I, resid=resid, stage=stage, shared=li.shared,
+                         I_shared=s.I_shared, w_shared_gate_bits=li.w_shared_gate)
+        tokens += T
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return tokens / el, tokens, calls, el
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    s = w.shape
+    cores = os.cpu_count()
+    # size each step so warmup + steps finish in about two and a half minutes
+    t_call = oracle_sample(w, 0.0)[3]
+    budget = 150.0
+    per_step = budget / max(1, args.steps + args.warmup)
+    T = w.T if t_call <= per_step else 1
+    for _ in range(args.warmup):
+        oracle_sample(w, 0.0, T)
+    t0 = time.perf_counter()
+    tokens = 0
+    for _ in range(args.steps):
+        tokens += oracle_sample(w, 0.0, T)[1]
+    el = time.perf_counter() - t0
+    value = tokens / el
+    sample = (f"{args.steps} oracle layer calls of {T} token(s) each (fp64 numpy, seeded windows of "
+              f"{w.name}); expert weights pre-generated")
+    out = {"impl": "reference", "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": w.name, "tokens_per_window": w.T, "hidden": s.H, "experts": s.E, "top_k": s.k,
+                      "intermediate": s.I, "shared_intermediate": s.I_shared},
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ ours
+def algorithmic_bytes(st, G: int, T: int) -> dict:
+    """Bytes each kernel must move at minimum for one window with G routed groups."""
+    H, I_, E, k, Is = st.H, st.I, st.E, st.k, st.I_shared
+    gu = G * 2 * I_ * (H // 2 + H // 16) + (2 * Is * (H // 2 + H // 16) if Is else 0)
+    gu += T * H * 2 + (T * k + (T if Is else 0)) * I_ * 4           # activations in, h out
+    dn = G * H * (I_ // 2 + I_ // 16) + (H * (Is // 2 + Is // 16) if Is else 0)
+    dn += (T * k + (T if Is else 0)) * (I_ * 4 + H * 4)               # h in, o out
+    router = E * H * 2 + T * H * 2 + T * E * 4
+    return {"gateup_decode": gu, "down_decode": dn, "router": router}
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    from serving_router_top_gb300 import build, inputs as I, moe
+    from serving_router_top_gb300.model import ModelState
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    s = w.shape
+    T = w.T
+    st = ModelState(w)
+    P = 64
+    xs_host = [torch.from_numpy(I.activations(w.seed, 10_000 * rank + i, T, s.H).view(np.int16)).pin_memory()
+               for i in range(P)]
+    xs = [x.cuda() for x in xs_host]
+    y = torch.zeros((T, s.H), dtype=torch.int16, device="cuda")       # bf16 output bits
+    y_host = torch.zeros((T, s.H), dtype=torch.int16).pin_memory()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    ids_ptr = st.ws.view.topk_ids
+    ngroups = moe.device_view(st.ws.view.num_groups, (1,), "int32", st.ws)
+    stream = torch.cuda.current_stream()
+
+    def step(x):
+        st.forward(0, x, y, T, y_is_fp32=False)
+        moe.cache_heat_update(st.cache, ids_ptr, T, s.k, 0)
+
+    st.ws.set_profiling(True)
+    for i in range(args.warmup):
+        flush.zero_()
+        step(xs[i % P])
+    torch.cuda.synchronize()
+    rc = moe.moe_sync_status(st.ws)
+    if rc != moe.MOE_OK:
+        raise RuntimeError(f"device error during warm-up: {moe.strerror(rc)}")
+
+    sampler = ClockSampler(gpu_id_for(local))
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kern_ms = {}
+    kern_bytes = {}
+    launches = 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        a, b = ev[i]
+        a.record(stream)
+        step(xs[i % P])
+        b.record(stream)
+        times = st.ws.kernel_times()          # synchronises on the step's last kernel
+        G = int(ngroups.item())
+        by = algorithmic_bytes(st, G, T)
+        for name, ms in times:
+            kern_ms[name] = kern_ms.get(name, 0.0) + ms
+            kern_bytes[name] = kern_bytes.get(name, 0) + by.get(name, 0)
+        launches += len(times) + 1            # + the heat update
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = sum(a.elapsed_time(b) for a, b in ev)
+    time.sleep(0.2)
+    sampler.stop()
+    rc = moe.moe_sync_status(st.ws)
+    if rc != moe.MOE_OK:
+        raise RuntimeError(f"device error in timed region: {moe.strerror(rc)}")
+
+    # end to end through the C ABI with host buffers: H2D of the window, the step, D2H of the output
+    st.ws.set_profiling(False)
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    xd = torch.empty_like(xs[0])
+    for i in range(args.steps):
+        flush.zero_()
+        a, b = ev2[i]
+        a.record(stream)
+        xd.copy_(xs_host[i % P], non_blocking=True)
+        step(xd)
+        y_host.copy_(y, non_blocking=True)
+        b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in ev2)
+
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+    tokens = T * args.steps * world
+    value = tokens / (total_ms / 1e3)
+    e2e_value = tokens / (e2e_ms / 1e3)
+    if rank != 0:
+        return
+    peaks, src = measured_peaks()
+    dom = max(kern_ms, key=lambda n: kern_ms[n] if n in kern_bytes and kern_bytes[n] else -1)
+    avg_ms = kern_ms[dom] / args.steps
+    avg_bytes = kern_bytes[dom] / args.steps
+    achieved = avg_bytes / (avg_ms / 1e3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    clocks = sampler.summary()
+    out = {
+        "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp4-e2m1 weights, f16/f32 math",
+        "data": "synthetic",
+        "config": {"workload": w.name, "tokens_per_window": T, "hidden": s.H, "experts": s.E, "top_k": s.k,
+                   "intermediate": s.I, "shared_intermediate": s.I_shared, "zipf_s": w.zipf_s,
+                   "resident_frac": w.resident_frac, "l2": "flushed (256 MB write) before every timed step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "peak_source": f"{src} hbm_gbs",
+                     "algorithmic_bytes_per_launch": avg_bytes, "avg_launch_us": avg_ms * 1e3},
+        "kernels_us_per_step": {n: 1e3 * v / args.steps for n, v in kern_ms.items()},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * s.H * 2,
+                "d2h_bytes_per_step": T * s.H * 2},
+        "gpu_launches": launches,
+    }
+    if not args.no_cpu_baseline:
+        v, tok, calls, el = oracle_sample(w, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                               "sample": f"{calls} oracle layer calls x {w.T} tokens ({tok} tokens, {el:.1f} s), "
+                                         f"fp64 numpy, same workload, seeded windows"}
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    from serving_router_top_gb300 import inputs as I
+    w = I.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

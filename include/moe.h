@@ -1,0 +1,278 @@
+/*
+ * moe.h -- C ABI of libmoe: the MoE layer forward over a slot-addressed expert
+ * cache, and the adaptive cache policy beside it, for one NVIDIA GB300
+ * (sm_103a).
+ *
+ * Everything here follows the problem statement of the Strata expert-paths
+ * page (hanayo.cn, "显存里缓存的是什么？", "路由以后，专家怎样分工？",
+ * "哪些专家能长期留在显存？") and the FreeToken reading notes
+ * (zhongzhuzhou.org, sections 3.3 and 4): experts are identified by
+ * (layer, expert); a residency table maps that identity to a cache slot or to
+ * a "not resident" sentinel; tokens that chose the same expert form one group
+ * with input and output positions; the expert computes gate/up, SiLU(gate)*up
+ * and the down projection on 4-bit block-scaled weights; outputs are merged
+ * with the routing weights plus a gated shared expert; heat counters with
+ * decay drive same-layer hot-in/cold-out swaps, and a swapped slot is
+ * published only after its copy has landed.
+ *
+ * Conventions for every call
+ *   - Pointers named *_dev / tensors are DEVICE memory owned by the caller,
+ *     unless the argument says "host".  bf16 tensors are passed as raw 16-bit
+ *     patterns (uint16_t).  All arrays are dense row-major.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     compute call is asynchronous on that stream; it allocates nothing and
+ *     does not synchronise.  The caller keeps the arguments alive until the
+ *     stream has passed the call.
+ *   - The return value reports errors the host can see at call time:
+ *     MOE_OK, MOE_EINVAL (bad shape, k > E, NULL pointer, size limits),
+ *     MOE_ENOMEM, MOE_ECUDA (a CUDA call or kernel launch failed).
+ *     Conditions only the device can see (an expert neither resident nor
+ *     staged, an index out of range, a NaN logit, a bounded wait that
+ *     expired) are recorded in the workspace's device error word; the
+ *     kernels never trap.  moe_sync_status() synchronises the stream, returns
+ *     the first recorded device error and clears it.
+ *   - Handles (moe_cache, moe_ws) are owned by the library and hold device
+ *     memory allocated at creation.  They are not thread-safe; one stream
+ *     should drive a workspace at a time.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* == cudaStream_t */
+
+enum {
+  MOE_OK = 0,
+  MOE_EINVAL = 1,
+  MOE_ENOMEM = 2,
+  MOE_ECUDA = 3,
+  MOE_EMISSING = 4, /* device: a routed expert is neither resident nor staged */
+  MOE_ERANGE = 5,   /* device: an index (slot, expert id) is out of range     */
+  MOE_ENAN = 6,     /* device: a router logit is NaN                          */
+  MOE_ETIMEOUT = 7  /* device: a bounded wait gave up                          */
+};
+
+/* Source of a group's weights, as resolved by the residency lookup. */
+enum { MOE_SRC_MISSING = -1, MOE_SRC_RESIDENT = 0, MOE_SRC_STAGED = 1 };
+
+/* Forward modes. */
+enum { MOE_MODE_AUTO = 0, MOE_MODE_DECODE = 1, MOE_MODE_PREFILL = 2 };
+
+typedef struct moe_cache moe_cache; /* residency + staging tables, slot pools, heats, backing store */
+typedef struct moe_ws moe_ws;       /* per-call scratch: logits, ids, groups, h, o, error word */
+
+/* ------------------------------------------------------------------ shapes */
+
+/* One MoE layer.  H hidden, I routed intermediate, E experts, k per token,
+ * I_shared shared-expert intermediate (0 = no shared expert).
+ * Limits: H, I, I_shared powers of two in [32, 4096]; I_shared == 0 or the
+ * same number of 32-column chunks per lane as I (both <= 1024, or equal);
+ * 1 <= k <= min(E, 32); 1 <= E <= 1024. */
+typedef struct {
+  int H, I, E, k, I_shared;
+} moe_layer_shape;
+
+/* Per-layer weights that live outside the expert cache. */
+typedef struct {
+  const uint16_t* w_router;      /* bf16 [E, H]; NULL -> logits are an input (see moe_route) */
+  const float* bias;             /* fp32 [E] added to the logits, or NULL                    */
+  const uint16_t* w_shared_gate; /* bf16 [H] shared-expert gate vector, or NULL               */
+  const void* shared_blob;       /* device blob of the shared expert (moe_pack_expert), or NULL */
+  int layer;                     /* layer index in the cache's (layer, expert) space          */
+  moe_layer_shape s;
+} moe_layer_desc;
+
+/* ------------------------------------------------------------- weight blobs
+ * Canonical matrix format (the NVFP4 row layout of the Qwen3.8-Flash-Next
+ * DGX Spark deployment notes, "一个 160 维向量在 packed 文件中占 90 字节" and
+ * "NVFP4 code 和 scale 如何反量化"): rows x cols values, each row cols/2 code
+ * bytes (two E2M1 codes per byte, low nibble = even column) followed by
+ * cols/16 FP8-E4M3 block scales (one per 16 columns); one FP32 global scale
+ * per matrix.  value = E2M1(code) * E4M3(scale) * global.
+ *
+ * An expert blob is the library's slot layout of one expert's three matrices
+ * gate [I x H], up [I x H], down [H x I]: a 256-byte header, then code and
+ * scale regions per matrix, each 256-byte aligned.  moe_blob_bytes() gives
+ * its size; all slots of a cache have that stride. */
+size_t moe_blob_bytes(int H, int I);
+
+/* Repack one expert from canonical packed rows (HOST pointers: gate and up
+ * [I][9H/16] bytes, down [H][9I/16] bytes) into a HOST blob buffer of
+ * moe_blob_bytes(H, I) bytes.  Synchronous, host only. */
+int moe_pack_expert(const uint8_t* gate_rows, const uint8_t* up_rows, const uint8_t* down_rows, int H, int I,
+                    float gscale_gate, float gscale_up, float gscale_down, void* blob_out_host);
+
+/* -------------------------------------------------------------- the cache */
+
+/* Create a cache for L layers x E experts of shape (H, I): `nslots` cache
+ * slots and `nstaging` staging slots in device memory, the residency and
+ * staging tables (all -1), fp32 heat counters (0) and statistics.
+ * `backing` holds the blobs of all L*E experts, expert (l, e) at offset
+ * (l*E + e) * moe_blob_bytes(H, I); it is device memory when
+ * backing_on_device != 0, else page-locked host memory (cudaHostAlloc'd or
+ * cudaHostRegister'ed) that the device reads directly.  The caller owns it
+ * and keeps it alive and unchanged while the cache exists (it is the source
+ * of truth; evicted experts need no copy back).  Synchronous. */
+int moe_cache_create(moe_cache** out, int L, int E, int H, int I, int nslots, int nstaging, const void* backing,
+                     int backing_on_device);
+int moe_cache_destroy(moe_cache* c);
+
+/* Admit one expert into a free slot (the Strata page's admit(): only while a
+ * free slot exists; otherwise *slot_out = -1 and the expert stays
+ * non-resident).  Copies its blob from the backing store.  Synchronous. */
+int moe_cache_admit(moe_cache* c, int layer, int expert, int32_t* slot_out);
+
+/* Bulk set-up: make exactly the experts with mask_host[l*E+e] != 0 resident
+ * (admitted in (layer, expert) order), or staged when `staging` != 0.
+ * Synchronous.  Fails with MOE_ENOMEM when the pool is too small. */
+int moe_cache_fill(moe_cache* c, const uint8_t* mask_host, int staging);
+
+/* Device pointers to the cache's tables (valid for the cache's lifetime):
+ * resid / stage int32 [L*E] (slot or -1), heat fp32 [L*E], slot_owner int32
+ * [nslots] (l*E+e or -1), slot and staging pool bases. */
+typedef struct {
+  int32_t* resid;
+  int32_t* stage;
+  float* heat;
+  int32_t* slot_owner;
+  void* slots;
+  void* staging;
+  size_t blob_bytes;
+  int L, E, nslots, nstaging;
+} moe_cache_view;
+int moe_cache_get_view(const moe_cache* c, moe_cache_view* out);
+
+/* Per-layer counters accumulated on the device: out_host receives
+ * int64 [L][4] = {lookups, resident hits, staged, missing}.  Synchronous. */
+int moe_get_stats(const moe_cache* c, int64_t* out_host);
+
+/* ---------------------------------------------------------- the workspace */
+
+/* Scratch for layer calls of up to maxT tokens of shape s (device memory,
+ * sized at creation).  Holds logits, top-k ids/weights, the expert groups,
+ * the intermediate h, per-position expert outputs and the error word. */
+int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s);
+int moe_ws_destroy(moe_ws* ws);
+
+/* Device pointers to the groups written by the last moe_group /
+ * moe_layer_forward on this workspace (capacities maxT*k):
+ *   num_groups int32[1]; grp_expert int32[G] ascending; grp_off int32[G+1];
+ *   grp_slot int32[G] (slot or staging index, -1 missing);
+ *   grp_src int32[G] (MOE_SRC_*); ent_tok int32[T*k]; ent_pos int32[T*k]
+ *   (t*k + r), entries of group g at [grp_off[g], grp_off[g+1]) by token. */
+typedef struct {
+  int32_t* num_groups;
+  int32_t* grp_expert;
+  int32_t* grp_off;
+  int32_t* grp_slot;
+  int32_t* grp_src;
+  int32_t* ent_tok;
+  int32_t* ent_pos;
+  float* logits;    /* fp32 [maxT, E] */
+  int32_t* topk_ids; /* int32 [maxT, k] */
+  float* topk_w;    /* fp32 [maxT, k] */
+  int32_t* error;   /* int32[1] device error word (first error wins) */
+} moe_ws_view;
+int moe_ws_get_view(const moe_ws* ws, moe_ws_view* out);
+
+/* Optional per-kernel timing.  When enabled, every hot-path call on this
+ * workspace records a CUDA event pair around each kernel it launches, on the
+ * call's stream.  moe_ws_kernel_times() synchronises on the last event and
+ * writes, for the kernels of the most recent call in launch order, their
+ * elapsed milliseconds (ms_out[i]) and static names (names_out[i], may be
+ * NULL); *n_out receives the count (at most `max`).  Off by default. */
+int moe_ws_set_profiling(moe_ws* ws, int enable);
+int moe_ws_kernel_times(moe_ws* ws, int max, float* ms_out, const char** names_out, int* n_out);
+
+/* Synchronise `stream`, return the device error word (MOE_OK if none) and
+ * reset it to MOE_OK. */
+int moe_sync_status(moe_ws* ws, moe_stream_t stream);
+const char* moe_strerror(int code);
+
+/* ------------------------------------------------------- the hot path calls */
+
+/* Router logits and top-k with renormalised weights (Strata page, "显存里缓存
+ * 的是什么？": the router picks each token's experts and their merge weights).
+ *   x: bf16 [T, H]; w_router: bf16 [E, H] or NULL; bias: fp32 [E] or NULL;
+ *   logits_io: fp32 [T, E] -- output l = x.W_r^T + bias (fp32 accumulate)
+ *   when w_router != NULL, else an INPUT (same-logits mode);
+ *   topk_ids: int32 [T, k] -- the k largest logits, weight descending, ties
+ *   to the lower expert id; topk_w: fp32 [T, k] -- exp(l - l_max) / sum over
+ *   the k chosen (= softmax over E renormalised over the k).
+ * A NaN logit records MOE_ENAN in err_dev (int32[1], may be NULL). */
+int moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, float* logits_io, int T, int H, int E,
+              int k, int32_t* topk_ids, float* topk_w, int32_t* err_dev, moe_stream_t stream);
+
+/* Dedupe one layer's selections into expert groups and look each group up
+ * (Strata page, "路由以后，专家怎样分工？": repeated experts of a layer and
+ * window form one group recording input and output positions; "哪些专家能长期
+ * 留在显存？": (layer, expert) -> slot or sentinel).  topk_ids int32 [T, k]
+ * (each row distinct ids in [0, E)).  Writes the workspace's group arrays
+ * (moe_ws_view): groups by ascending expert id, entries by ascending token,
+ * position t*k + r; slot from the residency table, else the staging table,
+ * else MOE_SRC_MISSING (also recorded as MOE_EMISSING).  Updates the cache's
+ * lookup counters.  Out-of-range ids record MOE_ERANGE. */
+int moe_group(const int32_t* topk_ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws,
+              moe_stream_t stream);
+
+/* The whole layer: router -> top-k -> groups -> lookup -> SwiGLU experts on
+ * the slot blobs -> routing-weighted combine + sigmoid-gated shared expert:
+ *   y[t] = sigmoid(x_t . w_sg) * S(x_t) + sum_r w[t,r] * E_{ids[t,r]}(x_t)
+ * (Strata page, "路由以后，专家怎样分工？"; FreeToken notes section 3.2: the
+ * merge is exact, no expert dropped).  x: bf16 [T, H]; y: bf16 [T, H], or
+ * fp32 [T, H] when y_is_fp32.  T <= the workspace's maxT.  mode selects the
+ * decode (GEMV) or prefill (grouped GEMM) expert kernels; AUTO picks by T. */
+int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T, moe_cache* c,
+                      moe_ws* ws, int mode, moe_stream_t stream);
+
+/* Heat update (Strata page, "哪些专家能长期留在显存？": accumulate how often
+ * each expert is routed to): heat[layer*E+e] = fl32(heat + (float)count_e)
+ * with count_e the number of (token, rank) selections of e in topk_ids
+ * int32 [T, k].  Out-of-range ids record MOE_ERANGE in err_dev (may be NULL). */
+int cache_heat_update(moe_cache* c, const int32_t* topk_ids, int T, int k, int layer, int32_t* err_dev,
+                      moe_stream_t stream);
+
+typedef struct {
+  int layer, hot_expert, cold_expert, slot;
+  float diff;
+} moe_swap;
+
+typedef struct {
+  float threshold; /* 1.5f  */
+  int max_swaps;   /* 96    */
+  float decay;     /* 0.7f  */
+} moe_policy_cfg;
+
+/* One planning round (same section: pair hot non-resident with cold resident
+ * experts of the same layer when the heat difference reaches the threshold,
+ * sort by difference, cap per round, then decay all heats):
+ *   per layer, non-resident experts by heat desc (id asc) are paired i-th with
+ *   resident experts by heat asc (id asc) while fl32(h_hot - h_cold) >=
+ *   threshold; candidates of all layers ordered by (diff desc, layer asc,
+ *   hot id asc); the first max_swaps written to plan_dev (moe_swap[max_swaps],
+ *   device) and their number to n_dev (int32[1], device); then every heat
+ *   becomes fl32(heat * decay).  Requires L*E <= 32768 and max_swaps <= 4096. */
+int cache_plan_swaps(moe_cache* c, const moe_policy_cfg* p, moe_swap* plan_dev, int32_t* n_dev, moe_stream_t stream);
+
+/* Execute a plan (same section: new weights are visible only after the copy
+ * completes; a slot is reused only after earlier reads finished):
+ *   on `compute`: unmap each cold expert (resid = -1), record event
+ *   "unmapped";  on `copy`: wait "unmapped", copy each hot blob from the
+ *   backing store into the slot, record "copied";  on `compute`: wait
+ *   "copied", publish (resid[hot] = slot).  Kernels queued on `compute`
+ *   before this call finish reading the old slots before the copy starts;
+ *   kernels queued after it see either the old mapping (never) or the new one.
+ *   No host synchronisation; n_dev is read on the device. */
+int moe_cache_apply_swaps(moe_cache* c, const moe_swap* plan_dev, const int32_t* n_dev, moe_stream_t compute,
+                          moe_stream_t copy);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

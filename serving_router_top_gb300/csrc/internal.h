@@ -1,0 +1,27 @@
+// Kernel launchers shared between libmoe translation units (not part of the ABI).
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+int launch_router(const uint16_t* x, const uint16_t* w_router, const float* bias, const uint16_t* w_gate,
+                  float* logits, float* gate_logit, int T, int H, int E, cudaStream_t s);
+int launch_prep_act(const uint16_t* x, __half* x16, float* scale, int T, int H, cudaStream_t s);
+int launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* err, cudaStream_t s);
+
+int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws, cudaStream_t s);
+
+// Decode expert path (CUDA-core GEMVs over the slot blobs).
+int launch_gateup_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s);
+int launch_down_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s);
+int launch_combine(const moe_layer_desc* d, void* y, int y_is_fp32, int T, moe_ws* ws, cudaStream_t s);
+
+// Policy.
+int launch_heat_update(moe_cache* c, const int32_t* ids, int T, int k, int layer, int32_t* err, cudaStream_t s);
+int launch_plan_swaps(moe_cache* c, const moe_policy_cfg* p, moe_swap* plan, int32_t* n, cudaStream_t s);
+int launch_apply_swaps(moe_cache* c, const moe_swap* plan, const int32_t* n, int max_swaps, cudaStream_t compute,
+                       cudaStream_t copy);
+int launch_blob_copy(moe_cache* c, const int32_t* src_index, const int32_t* dst_index, int n, int to_staging,
+                     cudaStream_t s);
+
+}  // namespace moe

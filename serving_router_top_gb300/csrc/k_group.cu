@@ -1,0 +1,179 @@
+// Dedupe of one layer's selections into expert groups, with the residency lookup.
+//
+// Strata expert paths, "路由以后，专家怎样分工？": repeated experts of one layer
+// and window form one group that records its input and output positions;
+// "哪些专家能长期留在显存？": the residency table maps (layer, expert) to a slot
+// or a "not resident" value.  FreeToken notes, section 4: the dedupe, the
+// classification against the residency table and the id -> slot rewrite stay
+// on the device (no host round trip), so the step can be captured in a graph.
+//
+// Canonical output: groups by ascending expert id; within a group, entries by
+// ascending token; an entry's output position is t*k + r.
+//
+// One CTA (1024 threads): a shared-memory histogram, a block scan over the E
+// experts, then placement in token chunks -- within a chunk each expert keeps
+// a bitmap of the tokens that chose it, and an entry's rank in its group is
+// the experts' running count plus the popcount of the bits below its token.
+#include "internal.h"
+
+namespace moe {
+
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_sums[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  total = warp_sums[nw - 1];
+  int before = warp ? warp_sums[warp - 1] : 0;
+  __syncthreads();
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(1024) k_group(const int32_t* __restrict__ ids, int T, int k, int E, int layer,
+                                                const int32_t* __restrict__ resid, const int32_t* __restrict__ stage,
+                                                const uint8_t* slots, const uint8_t* staging, size_t blob_bytes,
+                                                int nslots, int nstaging, int32_t* __restrict__ num_groups,
+                                                int32_t* __restrict__ grp_expert, int32_t* __restrict__ grp_off,
+                                                int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
+                                                const uint8_t** __restrict__ grp_blob, int32_t* __restrict__ ent_tok,
+                                                int32_t* __restrict__ ent_pos, unsigned long long* stats, int32_t* err,
+                                                int W) {
+  extern __shared__ int sm[];
+  int* cnt = sm;                                       // [E]
+  int* off = cnt + E;                                  // [E]
+  int* base = off + E;                                 // [E]
+  uint32_t* bits = reinterpret_cast<uint32_t*>(base + E);  // [E][W]
+  __shared__ int warp_sums[32];
+  __shared__ int s_hit, s_stg, s_miss;
+  const int n = T * k;
+  const int chunk = W * 32;
+
+  for (int e = threadIdx.x; e < E; e += blockDim.x) { cnt[e] = 0; base[e] = 0; }
+  if (threadIdx.x == 0) { s_hit = 0; s_stg = 0; s_miss = 0; }
+  __syncthreads();
+  bool bad = false;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    int e = ids[i];
+    if (e < 0 || e >= E) { bad = true; continue; }
+    atomicAdd(&cnt[e], 1);
+  }
+  if (bad) set_error(err, MOE_ERANGE);
+  __syncthreads();
+
+  // scan counts and presence (E <= blockDim.x)
+  const int e = threadIdx.x;
+  const int c = e < E ? cnt[e] : 0;
+  int total_entries, total_groups;
+  const int ex_c = block_excl_scan(c, warp_sums, total_entries);
+  const int ex_g = block_excl_scan(c > 0 ? 1 : 0, warp_sums, total_groups);
+  if (e < E) off[e] = ex_c;
+  if (e < E && c > 0) {
+    const int g = ex_g;
+    grp_expert[g] = e;
+    grp_off[g] = ex_c;
+    const int flat = layer * E + e;
+    int slot = resid[flat];
+    int src = MOE_SRC_MISSING;
+    const uint8_t* blob = nullptr;
+    if (slot >= 0) {
+      if (slot < nslots) { src = MOE_SRC_RESIDENT; blob = slots + size_t(slot) * blob_bytes; }
+      else { set_error(err, MOE_ERANGE); slot = -1; }
+    }
+    if (src == MOE_SRC_MISSING) {
+      int st = stage ? stage[flat] : -1;
+      if (st >= 0 && st < nstaging) { slot = st; src = MOE_SRC_STAGED; blob = staging + size_t(st) * blob_bytes; }
+      else if (st >= nstaging) set_error(err, MOE_ERANGE);
+    }
+    if (src == MOE_SRC_MISSING) { slot = -1; set_error(err, MOE_EMISSING); }
+    grp_slot[g] = slot;
+    grp_src[g] = src;
+    grp_blob[g] = blob;
+    atomicAdd(src == MOE_SRC_RESIDENT ? &s_hit : src == MOE_SRC_STAGED ? &s_stg : &s_miss, 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    *num_groups = total_groups;
+    grp_off[total_groups] = total_entries;
+    if (stats) {
+      unsigned long long* st = stats + size_t(layer) * 4;
+      atomicAdd(st + 0, (unsigned long long)total_groups);
+      atomicAdd(st + 1, (unsigned long long)s_hit);
+      atomicAdd(st + 2, (unsigned long long)s_stg);
+      atomicAdd(st + 3, (unsigned long long)s_miss);
+    }
+  }
+
+  // stable placement, one token chunk at a time
+  for (int t0 = 0; t0 < T; t0 += chunk) {
+    const int t1 = min(T, t0 + chunk);
+    for (int i = threadIdx.x; i < E * W; i += blockDim.x) bits[i] = 0u;
+    __syncthreads();
+    for (int i = t0 * k + threadIdx.x; i < t1 * k; i += blockDim.x) {
+      const int ex = ids[i];
+      if (ex < 0 || ex >= E) continue;
+      const int lt = i / k - t0;
+      uint32_t old = atomicOr(&bits[ex * W + (lt >> 5)], 1u << (lt & 31));
+      if (old & (1u << (lt & 31))) set_error(err, MOE_ERANGE);  // an expert chosen twice by one token
+    }
+    __syncthreads();
+    for (int i = t0 * k + threadIdx.x; i < t1 * k; i += blockDim.x) {
+      const int ex = ids[i];
+      if (ex < 0 || ex >= E) continue;
+      const int t = i / k, lt = t - t0, wd = lt >> 5;
+      const uint32_t* row = bits + ex * W;
+      int rank = base[ex] + __popc(row[wd] & ((1u << (lt & 31)) - 1u));
+      for (int w = 0; w < wd; ++w) rank += __popc(row[w]);
+      const int pos = off[ex] + rank;
+      ent_tok[pos] = t;
+      ent_pos[pos] = i;
+    }
+    __syncthreads();
+    for (int ex = threadIdx.x; ex < E; ex += blockDim.x) {
+      int s = 0;
+      for (int w = 0; w < W; ++w) s += __popc(bits[ex * W + w]);
+      base[ex] += s;
+    }
+    __syncthreads();
+  }
+}
+
+int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws, cudaStream_t s) {
+  if (E > 1024 || E <= 0) return MOE_EINVAL;
+  // bitmap words per expert: as many as fit 64 KB, at most 32 (1024 tokens per chunk)
+  int W = 16384 / E;
+  if (W > 32) W = 32;
+  if (W < 1) W = 1;
+  const int needW = (T + 31) / 32;
+  if (W > needW) W = needW > 0 ? needW : 1;
+  size_t smem = size_t(3 * E) * 4 + size_t(E) * W * 4;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(k_group, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024) != cudaSuccess)
+      return MOE_ECUDA;
+    attr_set = true;
+  }
+  k_group<<<1, 1024, smem, s>>>(ids, T, k, E, layer, c ? c->resid : nullptr, c ? c->stage : nullptr,
+                                c ? c->slots : nullptr, c ? c->staging : nullptr, c ? c->blob_bytes : 0,
+                                c ? c->nslots : 0, c ? c->nstaging : 0, ws->num_groups, ws->grp_expert, ws->grp_off,
+                                ws->grp_slot, ws->grp_src, ws->grp_blob, ws->ent_tok, ws->ent_pos,
+                                c ? c->stats : nullptr, ws->error, W);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+}  // namespace moe

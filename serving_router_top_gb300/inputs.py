@@ -64,6 +64,12 @@ def packed_row_bytes(cols: int) -> int:
     return cols // 2 + cols // 16
 
 
+def random_bytes(g: np.random.Generator, n: int) -> np.ndarray:
+    """n uniform bytes: the little-endian bytes of raw 64-bit PCG64 outputs."""
+    words = g.bit_generator.random_raw((n + 7) // 8).astype("<u8", copy=False)
+    return words.view(np.uint8)[:n]
+
+
 def packed_matrix(g: np.random.Generator, rows: int, cols: int) -> np.ndarray:
     """One matrix in the canonical packed-row format, uint8 ``[rows, 9*cols/16]``.
 
@@ -71,8 +77,8 @@ def packed_matrix(g: np.random.Generator, rows: int, cols: int) -> np.ndarray:
     the exponent field e in 3..6, three the mantissa field m in 0..7.
     """
     assert cols % 16 == 0, cols
-    codes = np.frombuffer(g.bytes(rows * cols // 2), dtype=np.uint8).reshape(rows, cols // 2)
-    r = np.frombuffer(g.bytes(rows * cols // 16), dtype=np.uint8).reshape(rows, cols // 16)
+    codes = random_bytes(g, rows * cols // 2).reshape(rows, cols // 2)
+    r = random_bytes(g, rows * cols // 16).reshape(rows, cols // 16)
     scales = (((r & 3) + 3) << 3) | ((r >> 2) & 7)
     return np.concatenate([codes, scales], axis=1)
 

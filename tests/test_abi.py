@@ -1,0 +1,85 @@
+"""The C-ABI library builds, loads without a GPU and exports every symbol include/moe.h declares;
+host-only entry points (blob sizing and packing, error strings) checked on the CPU."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import formats
+from serving_router_top_gb300 import build, inputs, moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return moe.load()
+
+
+def test_header_declares_the_five_path_calls():
+    names = header_functions()
+    for n in ("moe_route", "moe_group", "moe_layer_forward", "cache_heat_update", "cache_plan_swaps"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert set(names) == set(moe.EXPORTED), set(names) ^ set(moe.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror(lib):
+    assert moe.strerror(moe.MOE_OK) == "ok"
+    assert "resident" in moe.strerror(moe.MOE_EMISSING)
+
+
+@pytest.mark.parametrize("H,I", [(256, 128), (2048, 512), (128, 64), (4096, 2048)])
+def test_blob_pack_layout(lib, H, I):
+    ex = inputs.expert_weights(0, 0, 7, H, I)
+    ex.gscale = (0.5, 2.0, 1.25)
+    blob = moe.moe_pack_expert(ex.gate, ex.up, ex.down, H, I, ex.gscale)
+    assert blob.size == moe.moe_blob_bytes(H, I)
+    hdr = blob[:32].view(np.uint32)
+    assert hdr[0] == 0x42454F4D and hdr[2] == H and hdr[3] == I
+    assert blob[16:28].view(np.float32).tolist() == [0.5, 2.0, 1.25]
+    # every region holds the canonical codes / scales, 256-byte aligned, in gate, up, down order
+    off = 256
+    regions = []
+    for rows, cols in ((I, H), (I, H), (H, I)):
+        regions.append((off, rows, cols))
+        off += -(-rows * cols // 2 // 256) * 256
+    for (coff, rows, cols), m in zip(regions, (ex.gate, ex.up, ex.down)):
+        assert np.array_equal(blob[coff:coff + rows * cols // 2].reshape(rows, cols // 2), m[:, :cols // 2])
+    for (_, rows, cols), m in zip(regions, (ex.gate, ex.up, ex.down)):
+        assert np.array_equal(blob[off:off + rows * cols // 16].reshape(rows, cols // 16), m[:, cols // 2:])
+        off += -(-rows * cols // 16 // 256) * 256
+    assert off == blob.size
+
+
+def test_pack_rejects_bad_shapes(lib):
+    with pytest.raises(moe.MoeError):
+        moe.moe_pack_expert(np.zeros((4, 9), np.uint8), np.zeros((4, 9), np.uint8), np.zeros((16, 2), np.uint8),
+                            16, 4)
+    assert moe.moe_blob_bytes(100, 64) == 0
+
+
+def test_blob_roundtrip_dequantises_like_canonical(lib):
+    """Reading a blob region back as canonical rows gives the same oracle values."""
+    H, I = 128, 64
+    ex = inputs.expert_weights(3, 1, 2, H, I)
+    blob = moe.moe_pack_expert(ex.gate, ex.up, ex.down, H, I)
+    codes = blob[256:256 + I * H // 2].reshape(I, H // 2)
+    sc_off = 256 + 2 * (I * H // 2) + (H * I // 2)
+    scales = blob[sc_off:sc_off + I * H // 16].reshape(I, H // 16)
+    rows = np.concatenate([codes, scales], axis=1)
+    assert np.array_equal(formats.dequantize(rows, H), formats.dequantize(ex.gate, H))

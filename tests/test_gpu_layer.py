@@ -1,0 +1,140 @@
+"""GPU parity of the whole layer (router -> top-k -> groups -> lookup -> experts -> combine)
+against the oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import layer as olayer
+from serving_router_top_gb300 import inputs as I
+from serving_router_top_gb300 import moe
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    U.require_gpu()
+
+
+def run_layer(st, x_bits, T, bf16_out=False, layer=0):
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda()
+    if bf16_out:
+        y = torch.zeros((T, st.H), dtype=torch.int16, device="cuda")
+    else:
+        y = torch.zeros((T, st.H), dtype=torch.float32, device="cuda")
+    st.forward(layer, x, y, T, y_is_fp32=not bf16_out)
+    rc = moe.moe_sync_status(st.ws)
+    assert rc == moe.MOE_OK, moe.strerror(rc)
+    return U.y_to_numpy(y, bf16_out)
+
+
+def check_layer(st, T, bf16_out=False, step=0, layer=0):
+    x_bits = I.activations(st.w.seed, step, T, st.H)
+    y = run_layer(st, x_bits, T, bf16_out, layer)
+    logits_t, ids_t, w_t = st.ws.routing(T)
+    logits = logits_t.cpu().numpy()
+    ids = ids_t.cpu().numpy()
+    w = w_t.cpu().numpy()
+    li = st.layers[layer].host
+    # router logits: within the fp32-accumulation bound of the oracle's
+    ref_logits = olayer.router_logits(x_bits, li.w_router, li.bias)
+    bound = U.logits_bound(x_bits, li.w_router, li.bias)
+    assert np.all(np.abs(logits.astype(np.float64) - ref_logits) <= bound)
+    # top-k on the same fp32 logits: bit-exact ids, weights to fp32 rounding
+    ref_ids, ref_w = olayer.top_k(logits, st.k)
+    assert np.array_equal(ids, ref_ids)
+    assert np.allclose(w, ref_w, rtol=1e-5, atol=1e-7)
+    # top-k on the oracle's own logits differs only at near-ties
+    o_ids, _ = olayer.top_k(ref_logits, st.k)
+    for t in np.flatnonzero((o_ids != ids).any(axis=1)):
+        srt = np.sort(ref_logits[t].astype(np.float64))[::-1]
+        gaps = np.abs(np.diff(srt[: st.k + 1]))
+        assert gaps.min() <= 2 * bound[t].max(), t
+    # the rest of the layer on identical routing
+    ref = U.oracle_layer_from_state(st, layer, x_bits, logits)
+    exp_, off, slot, src, ent_tok, ent_pos = st.ws.groups(T)
+    assert np.array_equal(exp_, ref.groups.experts)
+    assert np.array_equal(off, ref.groups.off)
+    assert np.array_equal(ent_tok, ref.groups.ent_tok)
+    assert np.array_equal(ent_pos, ref.groups.ent_pos)
+    assert np.array_equal(slot, ref.slot)
+    assert np.array_equal(src, ref.src)
+    return U.assert_close_layer(y, ref.y, bf16_out), ref
+
+
+def test_layer_t8_h256_e16_k2():
+    st_ = I.WORKLOADS["layer_t8_h256_e16_k2"]
+    from serving_router_top_gb300.model import ModelState
+    st = ModelState(st_)
+    for step in range(3):
+        check_layer(st, st_.T, step=step)
+    check_layer(st, st_.T, bf16_out=True, step=5)
+
+
+@pytest.mark.parametrize("T,H,I_,E,k,Is,frac", [
+    (1, 128, 64, 12, 3, 64, 1.0),
+    (5, 128, 64, 12, 3, 64, 0.5),      # ragged token count, half staged
+    (7, 256, 128, 40, 7, 32, 0.25),    # shared intermediate narrower than routed
+    (33, 64, 32, 9, 9, 0, 1.0),        # k == E, no shared expert
+    (64, 1024, 256, 64, 6, 256, 0.5),
+    (3, 4096, 2048, 16, 2, 2048, 1.0),  # the large-expert row widths
+])
+def test_layer_small_shapes(T, H, I_, E, k, Is, frac):
+    from serving_router_top_gb300.model import ModelState
+    w = I.small_workload(T=T, H=H, I=I_, E=E, k=k, I_shared=Is, zipf_s=0.8, resident_frac=frac, seed=T + E)
+    st = ModelState(w)
+    check_layer(st, T)
+    check_layer(st, max(1, T // 2), step=1)   # fewer tokens than the workspace was sized for
+
+
+def test_layer_decode_t4_h2048_e512_k10():
+    from serving_router_top_gb300.model import ModelState
+    w = I.WORKLOADS["decode_t4_h2048_e512_k10"]
+    st = ModelState(w)
+    rel, ref = check_layer(st, w.T)
+    assert (ref.src == moe.MOE_SRC_STAGED).any() and (ref.src == moe.MOE_SRC_RESIDENT).any()
+    check_layer(st, w.T, bf16_out=True, step=1)
+    stats = st.cache.stats()
+    assert stats[0, 0] == stats[0, 1] + stats[0, 2] and stats[0, 3] == 0
+
+
+def test_missing_expert_is_reported():
+    from serving_router_top_gb300.model import ModelState
+    w = I.small_workload(T=6, H=128, I=64, E=12, k=3, I_shared=0, resident_frac=0.25, seed=3)
+    st = ModelState(w, stage_rest=False)
+    x = torch.from_numpy(I.activations(w.seed, 0, 6, 128).view(np.int16)).cuda()
+    y = torch.zeros((6, 128), dtype=torch.float32, device="cuda")
+    st.forward(0, x, y, 6)
+    assert moe.moe_sync_status(st.ws) == moe.MOE_EMISSING
+    assert moe.moe_sync_status(st.ws) == moe.MOE_OK  # cleared
+
+
+def test_route_same_logits_mode_ties_and_nan():
+    U.require_gpu()
+    T, E, k = 9, 37, 5
+    g = np.random.default_rng(0)
+    logits = g.integers(-2, 3, size=(T, E)).astype(np.float32)  # many exact ties
+    lt = torch.from_numpy(logits).cuda()
+    ids = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_route(None, None, None, lt, T, 0, E, k, ids, w, err)
+    torch.cuda.synchronize()
+    ref_ids, ref_w = olayer.top_k(logits, k)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    assert np.allclose(w.cpu().numpy(), ref_w, rtol=1e-6)
+    assert int(err.item()) == 0
+    logits[2, 4] = np.nan
+    moe.moe_route(None, None, None, torch.from_numpy(logits).cuda(), T, 0, E, k, ids, w, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == moe.MOE_ENAN
+
+
+def test_group_rejects_out_of_range_ids():
+    from serving_router_top_gb300.model import ModelState
+    w = I.small_workload(T=4, H=64, I=32, E=8, k=2, I_shared=0)
+    st = ModelState(w)
+    ids = torch.tensor([[0, 1], [2, 9], [3, 4], [5, 6]], dtype=torch.int32, device="cuda")
+    moe.moe_group(ids, 4, 2, 8, 0, st.cache, st.ws)
+    assert moe.moe_sync_status(st.ws) == moe.MOE_ERANGE

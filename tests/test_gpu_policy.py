@@ -1,0 +1,139 @@
+"""GPU parity of the cache policy (heat update, swap planning with decay, swap execution)
+against the fp32 oracle: plans and heats bit-exact, residency equal to the plan applied."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import policy as opol
+from serving_router_top_gb300 import moe
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+F32 = np.float32
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    U.require_gpu()
+
+
+def make_cache(L, E, resident, H=64, I=32, seed=0):
+    """A cache whose backing blobs are distinct random bytes, with `resident` [L,E] admitted."""
+    nb = moe.moe_blob_bytes(H, I)
+    g = np.random.default_rng(seed)
+    backing = torch.from_numpy(g.integers(0, 256, size=L * E * nb, dtype=np.uint8)).cuda()
+    c = moe.Cache(L, E, H, I, int(resident.sum()), 0, backing, True)
+    c.fill(resident.astype(np.uint8))
+    return c, backing, nb
+
+
+def set_heat(c, heat):
+    _, _, h = c.tables()
+    h.copy_(torch.from_numpy(heat))
+
+
+def run_plan(c, thr=1.5, cap=96, decay=0.7):
+    plan = torch.zeros(max(cap, 1) * 5, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.cache_plan_swaps(c, thr, cap, decay, plan, n)
+    torch.cuda.synchronize()
+    cnt = int(n.item())
+    arr = plan.cpu().numpy().view(moe.SWAP_DTYPE)[:cnt]
+    return arr, plan, n
+
+
+def plans_equal(got, ref):
+    assert len(got) == len(ref), (len(got), len(ref))
+    for a, b in zip(got, ref):
+        assert (int(a["layer"]), int(a["hot_expert"]), int(a["cold_expert"]), int(a["slot"])) == \
+               (b.layer, b.hot_expert, b.cold_expert, b.slot)
+        assert F32(a["diff"]) == F32(b.diff)
+
+
+def test_heat_update_bit_exact():
+    L, E, k, T = 3, 40, 5, 17
+    resident = np.zeros((L, E), dtype=bool)
+    c, _, _ = make_cache(L, E, resident)
+    g = np.random.default_rng(1)
+    heat = (g.random(L * E) * 50).astype(F32)
+    set_heat(c, heat)
+    ref = heat.copy()
+    for step in range(20):
+        layer = step % L
+        ids = np.stack([g.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        moe.cache_heat_update(c, torch.from_numpy(ids).cuda(), T, k, layer)
+        opol.heat_update(ref, ids, layer, E)
+    torch.cuda.synchronize()
+    assert np.array_equal(c.tables()[2].cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("L,E,seed", [(1, 4, 0), (3, 37, 1), (8, 256, 2), (48, 512, 3)])
+def test_plan_swaps_bit_exact(L, E, seed):
+    g = np.random.default_rng(seed)
+    resident = g.random((L, E)) < 0.3
+    c, _, _ = make_cache(L, E, resident)
+    # integer-valued heats with many ties and exact-threshold differences, then decayed values
+    heat = (g.integers(0, 12, size=L * E) * F32(0.5)).astype(F32)
+    heat[g.random(L * E) < 0.1] *= F32(0.7)
+    set_heat(c, heat)
+    resid = c.tables()[0].cpu().numpy()
+    ref_heat = heat.copy()
+    ref = opol.plan_round(ref_heat, resid, L, E)
+    got, _, _ = run_plan(c)
+    plans_equal(got, ref)
+    assert np.array_equal(c.tables()[2].cpu().numpy(), ref_heat)
+
+
+def test_plan_worked_example_and_cap():
+    E = 4
+    resident = np.array([[False, True, False, False]])
+    c, _, _ = make_cache(1, E, resident)
+    set_heat(c, np.array([10, 8, 0, 0], dtype=F32))
+    got, _, _ = run_plan(c)
+    assert len(got) == 1 and int(got[0]["hot_expert"]) == 0 and int(got[0]["cold_expert"]) == 1
+    assert F32(got[0]["diff"]) == F32(2.0)
+    assert c.tables()[2].cpu().numpy().tolist() == [F32(7.0), F32(5.6), 0, 0]
+    # decay-only round: nothing left to pair
+    set_heat(c, np.array([1, 0, 0, 0], dtype=F32))
+    got, _, _ = run_plan(c)
+    assert len(got) == 0 and c.tables()[2].cpu().numpy()[0] == F32(0.7)
+    # cap: 100 candidates -> 96
+    L, E = 4, 64
+    res = np.zeros((L, E), dtype=bool)
+    res[:, 32:57] = True
+    c2, _, _ = make_cache(L, E, res)
+    heat = np.zeros(L * E, dtype=F32)
+    g = np.random.default_rng(5)
+    for l in range(L):
+        heat[l * E:l * E + 25] = (2 + g.integers(0, 1000, 25)).astype(F32)
+    set_heat(c2, heat)
+    resid = c2.tables()[0].cpu().numpy()
+    ref = opol.plan_swaps(heat.copy(), resid, L, E)
+    got, _, _ = run_plan(c2)
+    assert len(ref) == 96
+    plans_equal(got, ref)
+
+
+def test_apply_swaps_publishes_after_copy():
+    L, E = 2, 24
+    g = np.random.default_rng(7)
+    resident = g.random((L, E)) < 0.4
+    c, backing, nb = make_cache(L, E, resident)
+    heat = g.integers(0, 20, size=L * E).astype(F32)
+    set_heat(c, heat)
+    resid_before = c.tables()[0].cpu().numpy()
+    ref_plan = opol.plan_swaps(heat.copy(), resid_before, L, E)
+    got, plan, n = run_plan(c)
+    plans_equal(got, ref_plan)
+    copy = torch.cuda.Stream()
+    moe.moe_cache_apply_swaps(c, plan, n, torch.cuda.current_stream(), copy)
+    torch.cuda.synchronize()
+    ref_resid = resid_before.copy()
+    opol.apply_swaps(ref_resid, ref_plan, E)
+    resid = c.tables()[0].cpu().numpy()
+    assert np.array_equal(resid, ref_resid)
+    # every resident slot holds exactly its expert's backing blob
+    pool = moe.device_view(c.view.slots, (c.nslots * nb,), "uint8", c)
+    for f in np.flatnonzero(resid >= 0):
+        s = int(resid[f])
+        assert torch.equal(pool[s * nb:(s + 1) * nb], backing[f * nb:(f + 1) * nb]), f
