@@ -116,38 +116,47 @@ def measured_peaks():
 
 
 # ------------------------------------------------------------- oracle leg
-def oracle_sample(w, seconds: float, tokens_per_call=None):
-    """Time the CPU oracle on windows of the workload until ~`seconds` elapse.
-    Returns (tokens/s, tokens, calls, wall seconds)."""
-    from oracle import layer as olayer
-    from serving_router_top_gb300 import inputs as I
-    s = w.shape
-    li = I.layer_inputs(w)
-    experts = {}
+class OracleRunner:
+    """The CPU oracle on windows of the workload, with the expert weights generated
+    up front (input preparation, outside any timing)."""
 
-    def get(e):
-        if e not in experts:
-            experts[e] = I.expert_weights(w.seed, 0, e, s.H, s.I)
-        return experts[e]
+    def __init__(self, w):
+        from serving_router_top_gb300 import inputs as I
+        self.w, self.I = w, I
+        s = w.shape
+        self.li = I.layer_inputs(w)
+        self.experts = [I.expert_weights(w.seed, 0, e, s.H, s.I) for e in range(s.E)]
+        mask = I.resident_mask(w.seed, 0, s.E, w.resident_frac)
+        self.resid = np.where(mask, np.cumsum(mask) - 1, -1).astype(np.int32)
+        self.stage = np.where(~mask, np.cumsum(~mask) - 1, -1).astype(np.int32)
+        self.calls = 0
 
-    for e in range(s.E):       # generation is input preparation, not oracle work
-        get(e)
-    mask = I.resident_mask(w.seed, 0, s.E, w.resident_frac)
-    resid = np.where(mask, np.cumsum(mask) - 1, -1).astype(np.int32)
-    stage = np.where(~mask, np.cumsum(~mask) - 1, -1).astype(np.int32)
-    T = w.T if tokens_per_call is None else tokens_per_call
-    tokens = calls = 0
-    t0 = time.perf_counter()
-    while True:
-        x = I.activations(w.seed, 1000 + calls, T, s.H)
-        olayer.moe_layer(x, li.w_router, li.bias, s.k, get, s.H, s.I, resid=resid, stage=stage, shared=li.shared,
-                         I_shared=s.I_shared, w_shared_gate_bits=li.w_shared_gate)
-        tokens += T
-        calls += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return tokens / el, tokens, calls, el
+    def call(self, T: int) -> int:
+        """One oracle layer call on a fresh window of T tokens; returns T."""
+        from oracle import layer as olayer
+        s, li = self.w.shape, self.li
+        x = self.I.activations(self.w.seed, 1000 + self.calls, T, s.H)
+        olayer.moe_layer(x, li.w_router, li.bias, s.k, self.experts.__getitem__, s.H, s.I, resid=self.resid,
+                         stage=self.stage, shared=li.shared, I_shared=s.I_shared,
+                         w_shared_gate_bits=li.w_shared_gate)
+        self.calls += 1
+        return T
+
+    def sample(self, seconds: float, T=None):
+        """Calls until ~`seconds` elapse: (tokens/s, tokens, calls, wall seconds)."""
+        T = self.w.T if T is None else T
+        tokens = calls = 0
+        t0 = time.perf_counter()
+        while True:
+            tokens += self.call(T)
+            calls += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return tokens / el, tokens, calls, el
+
+
+def oracle_sample(w, seconds: float):
+    return OracleRunner(w).sample(seconds)
 
 
 def run_reference(args, w):
@@ -156,17 +165,17 @@ def run_reference(args, w):
         return
     s = w.shape
     cores = os.cpu_count()
-    # size each step so warmup + steps finish in about two and a half minutes
-    t_call = oracle_sample(w, 0.0)[3]
-    budget = 150.0
-    per_step = budget / max(1, args.steps + args.warmup)
+    runner = OracleRunner(w)
+    # size each step so warm-up + steps finish in about two and a half minutes
+    t_call = runner.sample(0.0)[3]
+    per_step = 150.0 / max(1, args.steps + args.warmup)
     T = w.T if t_call <= per_step else 1
     for _ in range(args.warmup):
-        oracle_sample(w, 0.0, T)
+        runner.call(T)
     t0 = time.perf_counter()
     tokens = 0
     for _ in range(args.steps):
-        tokens += oracle_sample(w, 0.0, T)[1]
+        tokens += runner.call(T)
     el = time.perf_counter() - t0
     value = tokens / el
     sample = (f"{args.steps} oracle layer calls of {T} token(s) each (fp64 numpy, seeded windows of "
@@ -227,10 +236,20 @@ def run_ours(args, w):
         st.forward(0, x, y, T, y_is_fp32=False)
         moe.cache_heat_update(st.cache, ids_ptr, T, s.k, 0)
 
+    # The whole step is captured once in a CUDA graph (the C-ABI calls allocate
+    # nothing and never synchronise, so they are capture-safe) and replayed.
+    x_in = torch.empty_like(xs[0])
+    x_in.copy_(xs[0])
     st.ws.set_profiling(True)
+    step(x_in)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(x_in)
     for i in range(args.warmup):
+        x_in.copy_(xs[i % P])
         flush.zero_()
-        step(xs[i % P])
+        graph.replay()
     torch.cuda.synchronize()
     rc = moe.moe_sync_status(st.ws)
     if rc != moe.MOE_OK:
@@ -247,10 +266,11 @@ def run_ours(args, w):
         dist.barrier()
     torch.cuda.synchronize()
     for i in range(args.steps):
+        x_in.copy_(xs[i % P])
         flush.zero_()
         a, b = ev[i]
         a.record(stream)
-        step(xs[i % P])
+        graph.replay()
         b.record(stream)
         times = st.ws.kernel_times()          # synchronises on the step's last kernel
         G = int(ngroups.item())
@@ -269,18 +289,26 @@ def run_ours(args, w):
     if rc != moe.MOE_OK:
         raise RuntimeError(f"device error in timed region: {moe.strerror(rc)}")
 
-    # end to end through the C ABI with host buffers: H2D of the window, the step, D2H of the output
+    # End to end through the C ABI with host buffers: the graph holds the H2D
+    # copy of the window from pinned memory, the step and the D2H copy of the
+    # output; the host writes the next window into the pinned buffer first.
     st.ws.set_profiling(False)
+    x_pin = torch.empty_like(xs_host[0]).pin_memory()
+    g2 = torch.cuda.CUDAGraph()
+    x_pin.copy_(xs_host[0])
+    with torch.cuda.graph(g2):
+        x_in.copy_(x_pin, non_blocking=True)
+        step(x_in)
+        y_host.copy_(y, non_blocking=True)
     ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    xd = torch.empty_like(xs[0])
     for i in range(args.steps):
+        x_pin.copy_(xs_host[i % P])
         flush.zero_()
         a, b = ev2[i]
         a.record(stream)
-        xd.copy_(xs_host[i % P], non_blocking=True)
-        step(xd)
-        y_host.copy_(y, non_blocking=True)
+        g2.replay()
         b.record(stream)
+        b.synchronize()
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in ev2)
 

@@ -13,8 +13,8 @@ using namespace moe;
 namespace {
 
 bool shape_ok(const moe_layer_shape& s) {
-  // row widths: powers of two from 32 to 4096 (lanes per row and chunks per lane are powers of two)
-  auto cols_ok = [](int c) { return c >= 32 && c <= 4096 && (c & (c - 1)) == 0; };
+  // row widths: powers of two from 64 to 4096 (lanes per row and chunks per lane are powers of two)
+  auto cols_ok = [](int c) { return c >= 64 && c <= 4096 && (c & (c - 1)) == 0; };
   if (!cols_ok(s.H) || !cols_ok(s.I)) return false;
   if (s.I_shared != 0 && !cols_ok(s.I_shared)) return false;
   if (s.E < 1 || s.E > kMaxE || s.k < 1 || s.k > kMaxK || s.k > s.E) return false;
@@ -259,6 +259,16 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   const size_t o_x16 = cv.take<__half>(size_t(maxT) * s.H);
   const size_t o_xs = cv.take<float>(maxT);
   const size_t o_h = cv.take<float>((Tk + maxT) * Imax);
+  const size_t o_hmax = cv.take<float>(Tk + maxT);
+  // split-K scratch: slicing is chosen only while row blocks <= 2 per warp of the
+  // decode grid (2 CTAs of 8 warps per SM)
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 160;
+  const size_t split_blocks = size_t(sms) * 16 * 2 + 1;
+  const size_t o_part = cv.take<float>(split_blocks * 8 * 32 * 8);
+  const size_t o_cnt = cv.take<int>(split_blocks);
   const size_t o_o = cv.take<float>((Tk + maxT) * s.H);
   const size_t o_err = cv.take<int32_t>(1);
   uint8_t* base = nullptr;
@@ -282,6 +292,10 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   w->x16 = reinterpret_cast<__half*>(base + o_x16);
   w->xscale = reinterpret_cast<float*>(base + o_xs);
   w->h = reinterpret_cast<float*>(base + o_h);
+  w->hmax = reinterpret_cast<float*>(base + o_hmax);
+  w->part = reinterpret_cast<float*>(base + o_part);
+  w->cnt = reinterpret_cast<int*>(base + o_cnt);
+  w->split_blocks = split_blocks;
   w->o = reinterpret_cast<float*>(base + o_o);
   w->error = reinterpret_cast<int32_t*>(base + o_err);
   if (cudaMemset(base, 0, cv.off) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
@@ -388,13 +402,9 @@ int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y
   int rc;
   ws->prof_n = 0;
   {
-    ProfScope p(ws, "prep_act", st);
-    if ((rc = launch_prep_act(x, ws->x16, ws->xscale, T, s.H, st))) return rc;
-  }
-  {
     ProfScope p(ws, "router", st);
     if ((rc = launch_router(x, d->w_router, d->bias, s.I_shared > 0 ? d->w_shared_gate : nullptr, ws->logits,
-                            ws->gate_logit, T, s.H, s.E, st)))
+                            ws->gate_logit, T, s.H, s.E, st, ws->x16, ws->xscale)))
       return rc;
   }
   {

@@ -36,6 +36,7 @@ inline BlobLayout blob_layout(int H, int I) {
   L.scale_off[0] = o; o += align256(gu_sc);
   L.scale_off[1] = o; o += align256(gu_sc);
   L.scale_off[2] = o; o += align256(d_sc);
+  o += 256;  // tail guard: bulk copies of a last partial 16-byte block never leave the blob
   L.bytes = o;
   return L;
 }
@@ -166,9 +167,13 @@ struct moe_ws {
   int32_t* ent_tok;     // [maxT*k]
   int32_t* ent_pos;     // [maxT*k]
   // activations
-  __half* x16;          // [maxT, H] x * xscale in f16
-  float* xscale;        // [maxT]
+  __half* x16;          // [maxT, H] x times a per-token power of two, f16
+  float* xscale;        // [maxT] that power of two
   float* h;             // [maxT*k + maxT, max(I, I_shared)] routed entries then shared rows
+  float* hmax;          // [maxT*k + maxT] max|h| per row
+  float* part;          // split-K partial tiles: [split_blocks][8 slices][32 lanes][8]
+  int* cnt;             // [split_blocks] arrival counters, zero between calls
+  size_t split_blocks;
   float* o;             // [maxT*k + maxT, H] routed outputs by position, then shared outputs
   int32_t* error;       // [1]
   // optional per-kernel timing of the most recent call
@@ -183,15 +188,25 @@ struct ProfScope {
   moe_ws* ws;
   int idx;
   cudaStream_t s;
+  // Inside stream capture the records become external event nodes of the graph,
+  // so the times stay readable after each replay.
+  static void record(cudaEvent_t e, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(st, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+      cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+    else
+      cudaEventRecord(e, st);
+  }
   ProfScope(moe_ws* w, const char* name, cudaStream_t st) : ws(w), idx(-1), s(st) {
     if (ws && ws->prof_on && ws->prof_n < 16) {
       idx = ws->prof_n++;
       ws->prof_name[idx] = name;
-      cudaEventRecord(ws->prof_ev[2 * idx], s);
+      record(ws->prof_ev[2 * idx], s);
     }
   }
   ~ProfScope() {
-    if (idx >= 0) cudaEventRecord(ws->prof_ev[2 * idx + 1], s);
+    if (idx >= 0) record(ws->prof_ev[2 * idx + 1], s);
   }
 };
 }  // namespace moe

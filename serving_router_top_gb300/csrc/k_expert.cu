@@ -1,4 +1,4 @@
-// Decode expert path: memory-bound GEMVs over the slot blobs, and the combine.
+// Decode expert path: GEMVs over the slot blobs on the tensor cores, and the combine.
 //
 // Strata expert paths, "CPU 怎样把剩下的专家算完？": an expert computes gate and
 // up, the activation, then the down projection; "路由以后，专家怎样分工？": each
@@ -7,62 +7,60 @@
 // Spark notes, "NVFP4 code 和 scale 如何反量化": weight = E2M1 code x E4M3 block
 // scale (per 16) x FP32 global scale.
 //
-// Work unit: a warp owns a tile of rows of one group (or of the shared
-// expert).  LPR = min(32, cols/32) lanes share a row; lane q of a row reads
-// the row's 16-byte code chunks q, q+LPR, ... (32 codes each, two scale
-// blocks) with 128-bit streaming loads, so RPW = 32/LPR rows run side by side.
-// Codes become f16 pairs in registers (cvt e2m1x2); the activations of up to
-// TC tokens sit in registers as f16 pairs (pre-scaled by a power of two);
-// products accumulate in fp32 per 16-value block, are scaled by the block's
-// E4M3 scale and summed in fp32.
+// Arithmetic.  A group's tokens (at most 8 at a time) form the N side of
+// mma.sync m16n8k16 (f16 in, fp32 accumulate): A = code x block scale, which
+// is exact in f16 (at most 6 significant bits, magnitude 2^-10 .. 2688);
+// B = the activations in f16 after a power-of-two per-vector scale (the x
+// input is bf16 and lands in f16 exactly; the down input h is fp32 and is
+// rounded to f16, relative error <= 2^-11).  Within each 64-column segment a
+// lane's K slots map to 16 contiguous physical columns (the sum over K is
+// order-free when A and B use the same map), so a lane reads 8 contiguous code
+// bytes per row, all of one scale block.  On CUDA cores the same dequantised
+// dot product costs 2-5 instructions per weight, above the issue budget at
+// HBM speed; here it is about one.
 #include "internal.h"
 
 namespace moe {
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
+// ---------------------------------------------------------------- helpers
+// Two E2M1 codes (one byte, low nibble first) -> f16 pair (exact).
+__device__ __forceinline__ uint32_t cvt_e2m1x2(uint32_t byte) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(out) : "r"(byte));
+  return out;
+}
+// 16 bits = codes of K slots (2t, 2t+1) in the low byte and (2t+8, 2t+9) in the
+// high byte -> the two f16 pairs.
+__device__ __forceinline__ void e2m1_pair2(uint32_t two_bytes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(two_bytes));
+}
+__device__ __forceinline__ uint2 ldg_stream_u2(const void* p) {
+  uint2 v;
+  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
-
-__device__ __forceinline__ uint32_t ldg_u16(const void* p) {
+__device__ __forceinline__ uint32_t ldg_u8(const void* p) {
   unsigned short v;
-  asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  asm("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
   return v;
 }
-
-__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t word, uint32_t* o) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-      : "r"(word));
+constexpr int kMaxSlices = 8;
+// One E4M3 scale byte -> the f16 pair (s, s) (exact).
+__device__ __forceinline__ uint32_t scale_pair(uint32_t byte) { return e4m3x2_to_f16x2(byte | (byte << 8)); }
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
-
-// acc[j] += sum over the chunk's 32 columns of w * x_j, for TC tokens.
-template <int TC>
-__device__ __forceinline__ void chunk_dot(uint4 cw, uint32_t sc2, const uint32_t (&xv)[TC][16], float (&acc)[TC]) {
-  uint32_t w[16];
-  e2m1x8_to_f16x2x4(cw.x, w + 0);
-  e2m1x8_to_f16x2x4(cw.y, w + 4);
-  e2m1x8_to_f16x2x4(cw.z, w + 8);
-  e2m1x8_to_f16x2x4(cw.w, w + 12);
-  const float2 s = f16x2_to_f32x2(e4m3x2_to_f16x2(sc2));
-#pragma unroll
-  for (int j = 0; j < TC; ++j) {
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) a0 = fma2_f16_f32(w[b], xv[j][b], a0);
-#pragma unroll
-    for (int b = 8; b < 16; ++b) a1 = fma2_f16_f32(w[b], xv[j][b], a1);
-    acc[j] = fmaf(a0, s.x, acc[j]);
-    acc[j] = fmaf(a1, s.y, acc[j]);
-  }
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 struct DecodeArgs {
@@ -71,225 +69,245 @@ struct DecodeArgs {
   const uint8_t* const* grp_blob;
   const int32_t* ent_tok;
   const int32_t* ent_pos;
-  const __half* x16;   // [T, H]
-  const float* xscale; // [T]
-  float* h;            // [(maxTk + maxT) * Imax]
-  float* o;            // [(maxTk + maxT) * H]
+  const __half* x16;     // [T, H] f16, x * xscale
+  const float* xscale;   // [T]
+  float* h;              // [(maxTk + maxT) * Imax]
+  float* hmax;           // [maxTk + maxT] max|h| per row (float bits, atomicMax)
+  float* o;              // [(maxTk + maxT) * H]
   const uint8_t* shared_blob;
   int T, H, I, I_s, Imax, maxTk;
   DevBlobLayout lay_r, lay_s;
-  int rows_per_task;   // rows (or row pairs) per warp task
-  int tasks_r, tasks_s;  // tasks per routed group / for the shared expert
+  int nrb_r, nrb_s;      // 16-row blocks of a routed / the shared matrix
+  int ks_r, ks_s;        // K slices per row block
+  int ks_max, maxG;      // scratch geometry
+  float* part;           // split-K partial tiles
+  int* cnt;              // per row block arrival counters (zero between calls)
   int32_t* err;
 };
 
-// Which group a task belongs to, its token count, weights and rows.
-struct TaskInfo {
+// Work split.  A task is one 16-row block of one group's matrix (gate/up: the
+// gate rows and the matching up rows) over one K slice of C/KS columns; warps
+// take tasks independently (grid-stride).  Each lane loads its 8 code bytes
+// of rows g and g+8 per 64-column segment straight from the slot blob (64-bit
+// loads; the four lanes of a row read 32 contiguous bytes), four segments at
+// a time before any math.  With KS > 1 the slices' 16x8 partial tiles go to a
+// scratch buffer and the last warp to finish a row block (arrival counter)
+// adds them in slice order and writes the rows, so results do not depend on
+// scheduling.
+struct GemvTask {
   const uint8_t* blob;
-  int n, e0, shared, rows, r0, r1;
-  const DevBlobLayout* lay;
+  int shared, g, rb, ks, KS, C, n, e0;
 };
 
-__device__ __forceinline__ bool decode_task(const DecodeArgs& a, int task, int G, int rows_r, int rows_s, TaskInfo& ti) {
-  if (task < G * a.tasks_r) {
-    const int g = task / a.tasks_r, tile = task - g * a.tasks_r;
-    ti.e0 = a.grp_off[g];
-    ti.n = a.grp_off[g + 1] - ti.e0;
-    ti.blob = a.grp_blob[g];
-    ti.shared = 0;
-    ti.rows = rows_r;
-    ti.lay = &a.lay_r;
-    ti.r0 = tile * a.rows_per_task;
-  } else {
-    const int tile = task - G * a.tasks_r;
-    if (tile >= a.tasks_s) return false;
-    ti.e0 = 0;
-    ti.n = a.T;
-    ti.blob = a.shared_blob;
-    ti.shared = 1;
-    ti.rows = rows_s;
-    ti.lay = &a.lay_s;
-    ti.r0 = tile * a.rows_per_task;
+__device__ __forceinline__ bool gemv_task(const DecodeArgs& a, bool gateup, int task, int G, GemvTask& t) {
+  const int routed = G * a.nrb_r * a.ks_r;
+  if (task < routed) {
+    t.shared = 0;
+    t.ks = task % a.ks_r;
+    const int grb = task / a.ks_r;
+    t.g = grb / a.nrb_r;
+    t.rb = grb - t.g * a.nrb_r;
+    t.KS = a.ks_r;
+    t.blob = a.grp_blob[t.g];
+    t.C = gateup ? a.H : a.I;
+    t.e0 = a.grp_off[t.g];
+    t.n = a.grp_off[t.g + 1] - t.e0;
+    return true;
   }
-  ti.r1 = min(ti.rows, ti.r0 + a.rows_per_task);
+  const int st = task - routed;
+  if (st >= a.nrb_s * a.ks_s) return false;
+  t.shared = 1;
+  t.ks = st % a.ks_s;
+  t.rb = st / a.ks_s;
+  t.g = G;
+  t.KS = a.ks_s;
+  t.blob = a.shared_blob;
+  t.C = gateup ? a.H : a.I_s;
+  t.e0 = 0;
+  t.n = a.T;
   return true;
 }
 
-// ------------------------------------------------------------------ gate/up
-// h[row of entry][r] = SiLU(gs_g * <Wg[r], x>) * (gs_u * <Wu[r], x>)
-template <int CPL, int TC>
-__global__ void __launch_bounds__(256, 2) k_gateup(DecodeArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int H = a.H;
-  const int LPR = min(32, H / 32), RPW = 32 / LPR;
-  const int q = lane % LPR, sub = lane / LPR;
+constexpr int kSegUnroll = 4;
+
+// GATEUP: input x (f16 [T,H]) -> h[entry row][r] = SiLU(gs_g*<Wg_r,x>) * gs_u*<Wu_r,x>, and max|h| per row
+// !GATEUP: input h (fp32 rows, to f16 with a per-row power-of-two scale) -> o[position][r] = gs_d*<Wd_r,h>
+template <bool GATEUP>
+__global__ void __launch_bounds__(256, 2) k_expert_gemv(DecodeArgs a) {
+  constexpr int NM = GATEUP ? 2 : 1;
+  const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
   const int G = *a.num_groups;
-  const int total = G * a.tasks_r + a.tasks_s;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  const size_t code_row = H / 2, scale_row = H / 16;
-  for (int task = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < total; task += nw) {
-    TaskInfo ti;
-    if (!decode_task(a, task, G, a.I, a.I_s, ti)) break;
-    const uint8_t* gc = ti.blob ? ti.blob + ti.lay->code_off[0] : nullptr;
-    const uint8_t* uc = ti.blob ? ti.blob + ti.lay->code_off[1] : nullptr;
-    const uint8_t* gsc = ti.blob ? ti.blob + ti.lay->scale_off[0] : nullptr;
-    const uint8_t* usc = ti.blob ? ti.blob + ti.lay->scale_off[1] : nullptr;
-    float gs_g = 0.f, gs_u = 0.f;
-    if (ti.blob) {
-      const BlobHeader* hd = reinterpret_cast<const BlobHeader*>(ti.blob);
-      gs_g = hd->gscale[0];
-      gs_u = hd->gscale[1];
+  const int total = G * a.nrb_r * a.ks_r + a.nrb_s * a.ks_s;
+  for (int task = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < total; task += nwarps) {
+    GemvTask tk;
+    if (!gemv_task(a, GATEUP, task, G, tk)) break;
+    const DevBlobLayout& lay = tk.shared ? a.lay_s : a.lay_r;
+    const int code_row = tk.C / 2, scale_row = tk.C / 16;
+    const int segs = tk.C / (64 * tk.KS), seg0 = tk.ks * segs;
+    const int row0 = tk.rb * 16 + g8;  // this lane's rows: row0 and row0 + 8
+    const uint8_t* cp[NM];
+    const uint8_t* sp[NM];
+    float gsc[NM];
+#pragma unroll
+    for (int m = 0; m < NM; ++m) {
+      const int mi = GATEUP ? m : 2;
+      cp[m] = tk.blob ? tk.blob + lay.code_off[mi] + size_t(row0) * code_row + 8 * t4 : nullptr;
+      sp[m] = tk.blob ? tk.blob + lay.scale_off[mi] + size_t(row0) * scale_row + t4 : nullptr;
+      gsc[m] = tk.blob ? reinterpret_cast<const BlobHeader*>(tk.blob)->gscale[mi] : 0.f;
     }
-    for (int j0 = 0; j0 < ti.n; j0 += TC) {
-      uint32_t xv[CPL][TC][16];
-      float inv_xs[TC];
-      int hrow[TC];
-#pragma unroll
-      for (int j = 0; j < TC; ++j) {
-        const bool ok = j0 + j < ti.n;
-        const int tok = ok ? (ti.shared ? j0 + j : a.ent_tok[ti.e0 + j0 + j]) : 0;
-        hrow[j] = ok ? (ti.shared ? a.maxTk + j0 + j : ti.e0 + j0 + j) : -1;
-        inv_xs[j] = ok ? 1.0f / a.xscale[tok] : 0.f;
-        const uint4* xr = reinterpret_cast<const uint4*>(a.x16 + size_t(tok) * H);
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-          const int c = q + LPR * i;
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 t4 = ok ? xr[c * 4 + v] : make_uint4(0, 0, 0, 0);
-            xv[i][j][4 * v + 0] = t4.x;
-            xv[i][j][4 * v + 1] = t4.y;
-            xv[i][j][4 * v + 2] = t4.z;
-            xv[i][j][4 * v + 3] = t4.w;
-          }
+    const int nblocks = (tk.n + 7) >> 3;
+    for (int nb = 0; nb < nblocks; ++nb) {
+      const int nv = min(8, tk.n - nb * 8);
+      // the activation vector this lane feeds to B: vector nb*8 + g8 of the group
+      const bool bvalid = g8 < nv;
+      const void* brow = nullptr;
+      float bscale = 1.f;
+      if (bvalid) {
+        const int jj = nb * 8 + g8;
+        if (GATEUP) {
+          const int tok = tk.shared ? jj : a.ent_tok[tk.e0 + jj];
+          brow = a.x16 + size_t(tok) * a.H;
+        } else {
+          const int hr = tk.shared ? a.maxTk + jj : tk.e0 + jj;
+          brow = a.h + size_t(hr) * a.Imax;
+          bscale = pow2_scale_for(a.hmax[hr]);
         }
       }
-      for (int rs = ti.r0; rs < ti.r1; rs += RPW) {
-        const int r = rs + sub;
-        const bool rv = r < ti.r1 && ti.blob;
-        float ag[TC], au[TC];
+      float acc[NM][4];
 #pragma unroll
-        for (int j = 0; j < TC; ++j) { ag[j] = 0.f; au[j] = 0.f; }
-        if (rv) {
-          uint4 cg[CPL], cu[CPL];
-          uint32_t sg[CPL], su[CPL];
+      for (int m = 0; m < NM; ++m)
 #pragma unroll
-          for (int i = 0; i < CPL; ++i) {
-            const int c = q + LPR * i;
-            cg[i] = ldg_stream(gc + r * code_row + c * 16);
-            cu[i] = ldg_stream(uc + r * code_row + c * 16);
-            sg[i] = ldg_u16(gsc + r * scale_row + c * 2);
-            su[i] = ldg_u16(usc + r * scale_row + c * 2);
+        for (int q = 0; q < 4; ++q) acc[m][q] = 0.f;
+      if (tk.blob) {
+        for (int s0 = 0; s0 < segs; s0 += kSegUnroll) {
+          uint2 cw[kSegUnroll][NM][2];
+          uint32_t sw[kSegUnroll][NM][2];
+          uint32_t bx[kSegUnroll][8];
+#pragma unroll
+          for (int u = 0; u < kSegUnroll; ++u) {
+            const int seg = seg0 + s0 + u;
+            const bool ok = s0 + u < segs;
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+              cw[u][m][0] = ok ? ldg_stream_u2(cp[m] + seg * 32) : make_uint2(0, 0);
+              cw[u][m][1] = ok ? ldg_stream_u2(cp[m] + size_t(8) * code_row + seg * 32) : make_uint2(0, 0);
+              sw[u][m][0] = ok ? ldg_u8(sp[m] + seg * 4) : 0u;
+              sw[u][m][1] = ok ? ldg_u8(sp[m] + size_t(8) * scale_row + seg * 4) : 0u;
+            }
+            if (ok && bvalid) {
+              if (GATEUP) {
+                const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __half*>(brow) + seg * 64 + 16 * t4);
+                const uint4 v0 = p[0], v1 = p[1];
+                bx[u][0] = v0.x; bx[u][1] = v0.y; bx[u][2] = v0.z; bx[u][3] = v0.w;
+                bx[u][4] = v1.x; bx[u][5] = v1.y; bx[u][6] = v1.z; bx[u][7] = v1.w;
+              } else {
+                const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(brow) + seg * 64 + 16 * t4);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  const float4 f = p[v];
+                  __half2 h0 = __floats2half2_rn(f.x * bscale, f.y * bscale);
+                  __half2 h1 = __floats2half2_rn(f.z * bscale, f.w * bscale);
+                  bx[u][2 * v] = *reinterpret_cast<uint32_t*>(&h0);
+                  bx[u][2 * v + 1] = *reinterpret_cast<uint32_t*>(&h1);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int v = 0; v < 8; ++v) bx[u][v] = 0u;
+            }
           }
 #pragma unroll
-          for (int i = 0; i < CPL; ++i) {
-            chunk_dot<TC>(cg[i], sg[i], xv[i], ag);
-            chunk_dot<TC>(cu[i], su[i], xv[i], au);
-          }
-        }
+          for (int u = 0; u < kSegUnroll; ++u) {
+            if (s0 + u < segs) {
 #pragma unroll
-        for (int j = 0; j < TC; ++j) {
-          for (int o = LPR >> 1; o > 0; o >>= 1) {
-            ag[j] += __shfl_xor_sync(0xffffffffu, ag[j], o);
-            au[j] += __shfl_xor_sync(0xffffffffu, au[j], o);
-          }
-        }
-        if (q == 0 && r < ti.r1) {
+              for (int m = 0; m < NM; ++m) {
+                const uint32_t sc0 = scale_pair(sw[u][m][0]), sc1 = scale_pair(sw[u][m][1]);
+                const uint32_t w0[2] = {cw[u][m][0].x, cw[u][m][0].y}, w1[2] = {cw[u][m][1].x, cw[u][m][1].y};
 #pragma unroll
-          for (int j = 0; j < TC; ++j) {
-            if (hrow[j] >= 0) {
-              const float g = ag[j] * inv_xs[j] * gs_g;
-              const float u = au[j] * inv_xs[j] * gs_u;
-              a.h[size_t(hrow[j]) * a.Imax + r] = ti.blob ? silu_f32(g) * u : 0.f;
+                for (int kb = 0; kb < 4; ++kb) {
+                  uint32_t a0, a1, a2, a3;
+                  e2m1_pair2(w0[kb >> 1] >> (16 * (kb & 1)), a0, a2);  // row g: K slots 2t,2t+1 / 2t+8,2t+9
+                  e2m1_pair2(w1[kb >> 1] >> (16 * (kb & 1)), a1, a3);  // row g+8
+                  mma16816(acc[m], hmul2(a0, sc0), hmul2(a1, sc1), hmul2(a2, sc0), hmul2(a3, sc1), bx[u][2 * kb],
+                           bx[u][2 * kb + 1]);
+                }
+              }
             }
           }
         }
       }
-    }
-  }
-}
-
-// -------------------------------------------------------------------- down
-// o[pos][r] = gs_d * <Wd[r], h_entry>; h enters as f16 with a per-entry
-// power-of-two scale chosen from max|h_entry|.
-template <int CPL, int TC>
-__global__ void __launch_bounds__(256, 2) k_down(DecodeArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int H = a.H;
-  const int G = *a.num_groups;
-  const int total = G * a.tasks_r + a.tasks_s;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  for (int task = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < total; task += nw) {
-    TaskInfo ti;
-    if (!decode_task(a, task, G, H, H, ti)) break;
-    const int C = ti.shared ? a.I_s : a.I;  // contraction length
-    const int LPR = min(32, C / 32), RPW = 32 / LPR;
-    const int q = lane % LPR, sub = lane / LPR;
-    const size_t code_row = C / 2, scale_row = C / 16;
-    const uint8_t* dc = ti.blob ? ti.blob + ti.lay->code_off[2] : nullptr;
-    const uint8_t* dsc = ti.blob ? ti.blob + ti.lay->scale_off[2] : nullptr;
-    const float gs_d = ti.blob ? reinterpret_cast<const BlobHeader*>(ti.blob)->gscale[2] : 0.f;
-    for (int j0 = 0; j0 < ti.n; j0 += TC) {
-      uint32_t hv[CPL][TC][16];
-      float inv_hs[TC];
-      int orow[TC];
+      // ---- split-K: leave the partial, the last slice of the row block finishes it
+      bool finish = true;
+      if (tk.KS > 1) {
+        const int grb = tk.shared ? a.maxG * a.nrb_r + tk.rb : tk.g * a.nrb_r + tk.rb;
+        float* pp = a.part + ((size_t(grb) * a.ks_max + tk.ks) * 32 + lane) * 8;
 #pragma unroll
-      for (int j = 0; j < TC; ++j) {
-        const bool ok = j0 + j < ti.n;
-        const int hr = ok ? (ti.shared ? a.maxTk + j0 + j : ti.e0 + j0 + j) : 0;
-        orow[j] = ok ? (ti.shared ? a.maxTk + j0 + j : a.ent_pos[ti.e0 + j0 + j]) : -1;
-        const float4* hp = reinterpret_cast<const float4*>(a.h + size_t(hr) * a.Imax);
-        float m = 0.f;
+        for (int m = 0; m < NM; ++m)
+          reinterpret_cast<float4*>(pp)[m] = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+        __threadfence();
+        int old = 0;
+        if (lane == 0) old = atomicAdd(a.cnt + grb, 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        finish = old == tk.KS - 1;
+        if (finish) {
+          __threadfence();
 #pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-          const int c = q + LPR * i;
+          for (int m = 0; m < NM; ++m)
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            float4 f = ok ? hp[c * 8 + v] : make_float4(0.f, 0.f, 0.f, 0.f);
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+            for (int q = 0; q < 4; ++q) acc[m][q] = 0.f;
+          for (int s = 0; s < tk.KS; ++s) {
+            const float* qp = a.part + ((size_t(grb) * a.ks_max + s) * 32 + lane) * 8;
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+              const float4 f = __ldcg(reinterpret_cast<const float4*>(qp) + m);
+              acc[m][0] += f.x; acc[m][1] += f.y; acc[m][2] += f.z; acc[m][3] += f.w;
+            }
           }
+          if (lane == 0) a.cnt[grb] = 0;  // ready for the next call
         }
-        for (int o = LPR >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const float sc = pow2_scale_for(m);
-        inv_hs[j] = 1.0f / sc;
+      }
+      if (!finish) continue;
+      // ---- epilogue: lane holds rows row0, row0+8 x vectors nb*8 + 2*t4 + {0, 1}
+      float hm[2] = {0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-          const int c = q + LPR * i;
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            float4 f = ok ? hp[c * 8 + v] : make_float4(0.f, 0.f, 0.f, 0.f);
-            __half2 p0 = __floats2half2_rn(f.x * sc, f.y * sc);
-            __half2 p1 = __floats2half2_rn(f.z * sc, f.w * sc);
-            hv[i][j][2 * v + 0] = *reinterpret_cast<uint32_t*>(&p0);
-            hv[i][j][2 * v + 1] = *reinterpret_cast<uint32_t*>(&p1);
+      for (int q = 0; q < 4; ++q) {
+        const int jloc = 2 * t4 + (q & 1);
+        const int r = row0 + 8 * (q >> 1);
+        if (jloc < nv) {
+          const int jj = nb * 8 + jloc;
+          if (GATEUP) {
+            const int tok = tk.shared ? jj : a.ent_tok[tk.e0 + jj];
+            const float inv = 1.0f / a.xscale[tok];
+            const int hrow = tk.shared ? a.maxTk + jj : tk.e0 + jj;
+            const float hv = tk.blob ? silu_f32(acc[0][q] * inv * gsc[0]) * (acc[NM - 1][q] * inv * gsc[NM - 1]) : 0.f;
+            a.h[size_t(hrow) * a.Imax + r] = hv;
+            hm[q & 1] = fmaxf(hm[q & 1], fabsf(hv));
+          } else {
+            const int hr = tk.shared ? a.maxTk + jj : tk.e0 + jj;
+            const float inv = 1.0f / pow2_scale_for(a.hmax[hr]);
+            const int orow = tk.shared ? a.maxTk + jj : a.ent_pos[tk.e0 + jj];
+            a.o[size_t(orow) * a.H + r] = tk.blob ? acc[0][q] * inv * gsc[0] : 0.f;
           }
         }
       }
-      for (int rs = ti.r0; rs < ti.r1; rs += RPW) {
-        const int r = rs + sub;
-        const bool rv = r < ti.r1 && ti.blob;
-        float acc[TC];
+      if (GATEUP) {
+        // max|h| over the 16 rows of the block per vector, one atomic per vector
 #pragma unroll
-        for (int j = 0; j < TC; ++j) acc[j] = 0.f;
-        if (rv) {
-          uint4 cw[CPL];
-          uint32_t sw[CPL];
-#pragma unroll
-          for (int i = 0; i < CPL; ++i) {
-            const int c = q + LPR * i;
-            cw[i] = ldg_stream(dc + r * code_row + c * 16);
-            sw[i] = ldg_u16(dsc + r * scale_row + c * 2);
-          }
-#pragma unroll
-          for (int i = 0; i < CPL; ++i) chunk_dot<TC>(cw[i], sw[i], hv[i], acc);
+        for (int o = 4; o < 32; o <<= 1) {
+          hm[0] = fmaxf(hm[0], __shfl_xor_sync(0xffffffffu, hm[0], o));
+          hm[1] = fmaxf(hm[1], __shfl_xor_sync(0xffffffffu, hm[1], o));
         }
+        if (g8 == 0) {
 #pragma unroll
-        for (int j = 0; j < TC; ++j)
-          for (int o = LPR >> 1; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
-        if (q == 0 && r < ti.r1) {
-#pragma unroll
-          for (int j = 0; j < TC; ++j)
-            if (orow[j] >= 0) a.o[size_t(orow[j]) * H + r] = ti.blob ? acc[j] * inv_hs[j] * gs_d : 0.f;
+          for (int q = 0; q < 2; ++q) {
+            const int jloc = 2 * t4 + q;
+            if (jloc < nv) {
+              const int jj = nb * 8 + jloc;
+              const int hrow = tk.shared ? a.maxTk + jj : tk.e0 + jj;
+              atomicMax(reinterpret_cast<unsigned int*>(a.hmax) + hrow, __float_as_uint(hm[q]));
+            }
+          }
         }
       }
     }
@@ -335,29 +353,15 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ o, co
 }
 
 // ----------------------------------------------------------------- launchers
-static int g_num_sms = 0;
 static int num_sms() {
-  if (!g_num_sms) {
+  static int n = 0;
+  if (!n) {
     int dev = 0;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 148;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
   }
-  return g_num_sms;
-}
-
-template <int CPL, int TC>
-static void launch_gu(const DecodeArgs& a, int blocks, cudaStream_t s) {
-  k_gateup<CPL, TC><<<blocks, 256, 0, s>>>(a);
-}
-template <int CPL, int TC>
-static void launch_dn(const DecodeArgs& a, int blocks, cudaStream_t s) {
-  k_down<CPL, TC><<<blocks, 256, 0, s>>>(a);
-}
-
-static int cpl_of(int cols) {
-  const int chunks = cols / 32;
-  return chunks <= 32 ? 1 : chunks / 32;
+  return n;
 }
 
 static DecodeArgs decode_args(const moe_layer_desc* d, int T, moe_ws* ws) {
@@ -371,6 +375,7 @@ static DecodeArgs decode_args(const moe_layer_desc* d, int T, moe_ws* ws) {
   a.x16 = ws->x16;
   a.xscale = ws->xscale;
   a.h = ws->h;
+  a.hmax = ws->hmax;
   a.o = ws->o;
   const bool has_shared = sh.I_shared > 0 && d->shared_blob;
   a.shared_blob = has_shared ? reinterpret_cast<const uint8_t*>(d->shared_blob) : nullptr;
@@ -386,40 +391,53 @@ static DecodeArgs decode_args(const moe_layer_desc* d, int T, moe_ws* ws) {
   return a;
 }
 
-int launch_gateup_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s) {
+static int pow2_floor(int v) {
+  int p = 1;
+  while (p * 2 <= v) p *= 2;
+  return p;
+}
+
+// Slices per row block: enough tasks for about four per warp, each slice at
+// least 256 columns.
+static int pick_ks(int C, int row_blocks, int nwarps) {
+  int ks = pow2_floor((4 * nwarps) / (row_blocks > 0 ? row_blocks : 1));
+  const int cap = C / 256 > 0 ? C / 256 : 1;
+  if (ks > cap) ks = cap;
+  if (ks > kMaxSlices) ks = kMaxSlices;
+  return ks < 1 ? 1 : ks;
+}
+
+template <bool GATEUP>
+static int launch_gemv(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s) {
   DecodeArgs a = decode_args(d, T, ws);
+  const int rows_r = GATEUP ? a.I : a.H, rows_s = GATEUP ? a.I_s : a.H;
+  a.nrb_r = rows_r / 16;
+  a.nrb_s = a.shared_blob ? rows_s / 16 : 0;
+  a.maxG = T * d->s.k < d->s.E ? T * d->s.k : d->s.E;
   const int blocks = num_sms() * 2;
-  // tasks of 8 rows (each a gate row and an up row)
-  a.rows_per_task = 8;
-  a.tasks_r = (a.I + a.rows_per_task - 1) / a.rows_per_task;
-  a.tasks_s = a.I_s ? (a.I_s + a.rows_per_task - 1) / a.rows_per_task : 0;
-  switch (cpl_of(a.H)) {
-    case 1: launch_gu<1, 4>(a, blocks, s); break;
-    case 2: launch_gu<2, 2>(a, blocks, s); break;
-    case 4: launch_gu<4, 1>(a, blocks, s); break;
-    default: return MOE_EINVAL;
-  }
+  const int nwarps = blocks * 8;
+  const int C_r = GATEUP ? a.H : a.I, C_s = GATEUP ? a.H : (a.I_s ? a.I_s : a.I);
+  // K is split only when every group fits one block of 8 vectors (T <= 8): the
+  // partial scratch and counters are per row block, not per vector block
+  a.ks_r = T <= 8 ? pick_ks(C_r, a.maxG * a.nrb_r + a.nrb_s, nwarps) : 1;
+  a.ks_s = T <= 8 && a.shared_blob ? pick_ks(C_s, a.maxG * a.nrb_r + a.nrb_s, nwarps) : 1;
+  a.ks_max = kMaxSlices;
+  // slices only exist when row blocks are few (at most two per warp), so the
+  // scratch sized for that bound always holds them
+  if ((a.ks_r > 1 || a.ks_s > 1) && size_t(a.maxG * a.nrb_r + a.nrb_s) > ws->split_blocks) return MOE_EINVAL;
+  a.part = ws->part;
+  a.cnt = ws->cnt;
+  k_expert_gemv<GATEUP><<<blocks, 256, 0, s>>>(a);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
 
+int launch_gateup_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s) {
+  return launch_gemv<true>(d, T, ws, s);
+}
+
 int launch_down_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s) {
-  DecodeArgs a = decode_args(d, T, ws);
-  const int blocks = num_sms() * 2;
-  // tasks of 16 output rows; contraction over I (routed) / I_s (shared)
-  a.rows_per_task = 16;
-  a.tasks_r = (a.H + a.rows_per_task - 1) / a.rows_per_task;
-  a.tasks_s = a.I_s ? a.tasks_r : 0;
-  const int cpl_d = cpl_of(a.I);
-  if (a.I_s && cpl_of(a.I_s) != cpl_d) return MOE_EINVAL;
-  switch (cpl_d) {
-    case 1: launch_dn<1, 4>(a, blocks, s); break;
-    case 2: launch_dn<2, 2>(a, blocks, s); break;
-    case 4: launch_dn<4, 1>(a, blocks, s); break;
-    default: return MOE_EINVAL;
-  }
-  MOE_LAUNCH_CHECK();
-  return MOE_OK;
+  return launch_gemv<false>(d, T, ws, s);
 }
 
 int launch_combine(const moe_layer_desc* d, void* y, int y_is_fp32, int T, moe_ws* ws, cudaStream_t s) {

@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t* __restrict__ ids,
                                                 int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
                                                 const uint8_t** __restrict__ grp_blob, int32_t* __restrict__ ent_tok,
                                                 int32_t* __restrict__ ent_pos, unsigned long long* stats, int32_t* err,
-                                                int W) {
+                                                int W, float* __restrict__ hmax, int maxTk) {
   extern __shared__ int sm[];
   int* cnt = sm;                                       // [E]
   int* off = cnt + E;                                  // [E]
@@ -64,6 +64,11 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t* __restrict__ ids,
   const int chunk = W * 32;
 
   for (int e = threadIdx.x; e < E; e += blockDim.x) { cnt[e] = 0; base[e] = 0; }
+  // the expert kernels of this call accumulate max|h| per row into hmax
+  if (hmax) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) hmax[i] = 0.f;
+    for (int i = threadIdx.x; i < T; i += blockDim.x) hmax[maxTk + i] = 0.f;
+  }
   if (threadIdx.x == 0) { s_hit = 0; s_stg = 0; s_miss = 0; }
   __syncthreads();
   bool bad = false;
@@ -171,7 +176,7 @@ int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* 
                                 c ? c->slots : nullptr, c ? c->staging : nullptr, c ? c->blob_bytes : 0,
                                 c ? c->nslots : 0, c ? c->nstaging : 0, ws->num_groups, ws->grp_expert, ws->grp_off,
                                 ws->grp_slot, ws->grp_src, ws->grp_blob, ws->ent_tok, ws->ent_pos,
-                                c ? c->stats : nullptr, ws->error, W);
+                                c ? c->stats : nullptr, ws->error, W, ws->hmax, ws->maxT * ws->s.k);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

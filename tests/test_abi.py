@@ -63,7 +63,7 @@ def test_blob_pack_layout(lib, H, I):
     for (_, rows, cols), m in zip(regions, (ex.gate, ex.up, ex.down)):
         assert np.array_equal(blob[off:off + rows * cols // 16].reshape(rows, cols // 16), m[:, cols // 2:])
         off += -(-rows * cols // 16 // 256) * 256
-    assert off == blob.size
+    assert off + 256 == blob.size  # 256-byte tail guard
 
 
 def test_pack_rejects_bad_shapes(lib):

@@ -75,8 +75,8 @@ def test_layer_t8_h256_e16_k2():
 @pytest.mark.parametrize("T,H,I_,E,k,Is,frac", [
     (1, 128, 64, 12, 3, 64, 1.0),
     (5, 128, 64, 12, 3, 64, 0.5),      # ragged token count, half staged
-    (7, 256, 128, 40, 7, 32, 0.25),    # shared intermediate narrower than routed
-    (33, 64, 32, 9, 9, 0, 1.0),        # k == E, no shared expert
+    (7, 256, 128, 40, 7, 64, 0.25),    # shared intermediate narrower than routed
+    (33, 64, 64, 9, 9, 0, 1.0),        # k == E, no shared expert, narrowest rows
     (64, 1024, 256, 64, 6, 256, 0.5),
     (3, 4096, 2048, 16, 2, 2048, 1.0),  # the large-expert row widths
 ])
@@ -133,7 +133,7 @@ def test_route_same_logits_mode_ties_and_nan():
 
 def test_group_rejects_out_of_range_ids():
     from serving_router_top_gb300.model import ModelState
-    w = I.small_workload(T=4, H=64, I=32, E=8, k=2, I_shared=0)
+    w = I.small_workload(T=4, H=64, I=64, E=8, k=2, I_shared=0)
     st = ModelState(w)
     ids = torch.tensor([[0, 1], [2, 9], [3, 4], [5, 6]], dtype=torch.int32, device="cuda")
     moe.moe_group(ids, 4, 2, 8, 0, st.cache, st.ws)
