@@ -260,13 +260,11 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   const size_t o_xs = cv.take<float>(maxT);
   const size_t o_h = cv.take<float>((Tk + maxT) * Imax);
   const size_t o_hmax = cv.take<float>(Tk + maxT);
-  // split-K scratch: slicing is chosen only while row blocks <= 2 per warp of the
-  // decode grid (2 CTAs of 8 warps per SM)
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (sms <= 0) sms = 160;
-  const size_t split_blocks = size_t(sms) * 16 * 2 + 1;
+  // split-K scratch: K is sliced only for calls of at most 8 tokens, so at most
+  // min(8k, E) groups of up to max(H, I)/16 row blocks, plus the shared expert's
+  const int small_groups = (maxT < 8 ? maxT : 8) * s.k < s.E ? (maxT < 8 ? maxT : 8) * s.k : s.E;
+  const int rb_max = (s.H > s.I ? s.H : s.I) / 16;
+  const size_t split_blocks = size_t(small_groups + 1) * rb_max;
   const size_t o_part = cv.take<float>(split_blocks * 8 * 32 * 8);
   const size_t o_cnt = cv.take<int>(split_blocks);
   const size_t o_o = cv.take<float>((Tk + maxT) * s.H);

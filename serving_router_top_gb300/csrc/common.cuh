@@ -126,6 +126,31 @@ __device__ __forceinline__ float pow2_scale_for(float amax) {
   return ldexpf(1.0f, 13 - e);  // amax * 2^(13-e) in [2^12, 2^13)
 }
 
+// ---------------------------------------------------------------- launches
+// Programmatic dependent launch: every hot-path kernel lets its successor be
+// scheduled as soon as all of its own CTAs are running (pdl_trigger at entry)
+// and waits for its predecessor's grid to complete -- with its memory visible
+// -- before reading anything the predecessor may have written (pdl_wait).
+// Launch latency of the chain is hidden; data order is unchanged.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace moe
 
 // ---------------------------------------------------------------- opaque handles

@@ -16,38 +16,33 @@
 // lane's K slots map to 16 contiguous physical columns (the sum over K is
 // order-free when A and B use the same map), so a lane reads 8 contiguous code
 // bytes per row, all of one scale block.  On CUDA cores the same dequantised
-// dot product costs 2-5 instructions per weight, above the issue budget at
-// HBM speed; here it is about one.
+// dot product costs 2-5 instructions per weight, above the issue budget at HBM
+// speed; here it is about one.
+//
+// Streaming.  A task is one 16-row block of one group's matrix (gate/up: the
+// gate rows and the matching up rows) for one block of 8 activation vectors
+// over one K slice; its K range is cut into units of UC columns.  Every warp
+// runs its own pipeline over the units of its tasks: each unit's code bytes,
+// scale bytes and activation slice are copied by the warp's lanes into a
+// private ring of shared-memory stages with cp.async (rows padded so the
+// fragment reads are free of bank conflicts), three units ahead of the one
+// being computed.  No barrier spans more than one warp.  With K slices, the
+// slices' 16x8 partial tiles go to a scratch buffer and the last warp to finish
+// a row block (arrival counter) adds them in slice order, so results do not
+// depend on scheduling.
 #include "internal.h"
 
 namespace moe {
 
 // ---------------------------------------------------------------- helpers
-// Two E2M1 codes (one byte, low nibble first) -> f16 pair (exact).
-__device__ __forceinline__ uint32_t cvt_e2m1x2(uint32_t byte) {
-  uint32_t out;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(out) : "r"(byte));
-  return out;
-}
 // 16 bits = codes of K slots (2t, 2t+1) in the low byte and (2t+8, 2t+9) in the
-// high byte -> the two f16 pairs.
+// high byte -> the two f16 pairs (exact).
 __device__ __forceinline__ void e2m1_pair2(uint32_t two_bytes, uint32_t& lo, uint32_t& hi) {
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %2;\n\t"
       "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t}"
       : "=r"(lo), "=r"(hi)
       : "r"(two_bytes));
 }
-__device__ __forceinline__ uint2 ldg_stream_u2(const void* p) {
-  uint2 v;
-  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ uint32_t ldg_u8(const void* p) {
-  unsigned short v;
-  asm("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
-  return v;
-}
-constexpr int kMaxSlices = 8;
 // One E4M3 scale byte -> the f16 pair (s, s) (exact).
 __device__ __forceinline__ uint32_t scale_pair(uint32_t byte) { return e4m3x2_to_f16x2(byte | (byte << 8)); }
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
@@ -62,6 +57,21 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_small(void* dst, const void* src) {  // N = 4 or 8
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "n"(N)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 struct DecodeArgs {
   const int32_t* num_groups;
@@ -77,222 +87,302 @@ struct DecodeArgs {
   const uint8_t* shared_blob;
   int T, H, I, I_s, Imax, maxTk;
   DevBlobLayout lay_r, lay_s;
-  int nrb_r, nrb_s;      // 16-row blocks of a routed / the shared matrix
-  int ks_r, ks_s;        // K slices per row block
-  int ks_max, maxG;      // scratch geometry
-  float* part;           // split-K partial tiles
+  int l_nrb_r, l_nrb_s;  // log2 of the 16-row blocks of a routed / the shared matrix
+  int l_ks_r, l_ks_s;    // log2 of the K slices per row block
+  int l_nbp;             // log2 of the vector blocks per row block (ceil(T/8) rounded up to a power of two)
+  int maxG;              // upper bound of the group count (scratch geometry)
+  float* part;           // split-K partial tiles [row block][kMaxSlices][32 lanes][8]
   int* cnt;              // per row block arrival counters (zero between calls)
   int32_t* err;
 };
 
-// Work split.  A task is one 16-row block of one group's matrix (gate/up: the
-// gate rows and the matching up rows) over one K slice of C/KS columns; warps
-// take tasks independently (grid-stride).  Each lane loads its 8 code bytes
-// of rows g and g+8 per 64-column segment straight from the slot blob (64-bit
-// loads; the four lanes of a row read 32 contiguous bytes), four segments at
-// a time before any math.  With KS > 1 the slices' 16x8 partial tiles go to a
-// scratch buffer and the last warp to finish a row block (arrival counter)
-// adds them in slice order and writes the rows, so results do not depend on
-// scheduling.
-struct GemvTask {
+constexpr int kWarpsPerCta = 8;
+constexpr int kStages = 4;
+constexpr int kMaxSlices = 8;
+constexpr int kCodePad = 32;  // bytes after each code row of a stage
+constexpr int kXPad = 16;     // bytes after each activation vector of a stage
+
+// What the computing lanes need to know about the unit in a stage.  Written by
+// the issuing lanes, read three units later.
+struct __align__(16) UnitMeta {
   const uint8_t* blob;
-  int shared, g, rb, ks, KS, C, n, e0;
+  int task;  // -1: no unit
+  int u, units, shared, g, rb, ks, e0, nv, jbase;
+  int idx[8];  // per vector: token (gate/up) or output position (down)
 };
 
-__device__ __forceinline__ bool gemv_task(const DecodeArgs& a, bool gateup, int task, int G, GemvTask& t) {
-  const int routed = G * a.nrb_r * a.ks_r;
-  if (task < routed) {
-    t.shared = 0;
-    t.ks = task % a.ks_r;
-    const int grb = task / a.ks_r;
-    t.g = grb / a.nrb_r;
-    t.rb = grb - t.g * a.nrb_r;
-    t.KS = a.ks_r;
-    t.blob = a.grp_blob[t.g];
-    t.C = gateup ? a.H : a.I;
-    t.e0 = a.grp_off[t.g];
-    t.n = a.grp_off[t.g + 1] - t.e0;
-    return true;
-  }
-  const int st = task - routed;
-  if (st >= a.nrb_s * a.ks_s) return false;
-  t.shared = 1;
-  t.ks = st % a.ks_s;
-  t.rb = st / a.ks_s;
-  t.g = G;
-  t.KS = a.ks_s;
-  t.blob = a.shared_blob;
-  t.C = gateup ? a.H : a.I_s;
-  t.e0 = 0;
-  t.n = a.T;
-  return true;
-}
-
-constexpr int kSegUnroll = 4;
+template <bool GATEUP, int UC>
+struct StageGeo {
+  static constexpr int NM = GATEUP ? 2 : 1;
+  static constexpr int XSZ = GATEUP ? 2 : 4;         // bytes per activation element
+  static constexpr int CPR = UC / 32;                 // 16-byte code chunks per row
+  static constexpr int CROW = UC / 2 + kCodePad;      // code row stride
+  static constexpr int SROW = UC / 16;                // scale bytes per row
+  static constexpr int XROW = UC * XSZ + kXPad;       // activation vector stride
+  static constexpr int XCP = UC * XSZ / 16;           // 16-byte chunks per vector
+  static constexpr int SCALES = NM * 16 * CROW;       // offset of the scales
+  static constexpr int XS = SCALES + NM * 16 * SROW;  // offset of the activations
+  static constexpr int BYTES = (XS + 8 * XROW + 127) / 128 * 128;
+};
 
 // GATEUP: input x (f16 [T,H]) -> h[entry row][r] = SiLU(gs_g*<Wg_r,x>) * gs_u*<Wu_r,x>, and max|h| per row
 // !GATEUP: input h (fp32 rows, to f16 with a per-row power-of-two scale) -> o[position][r] = gs_d*<Wd_r,h>
-template <bool GATEUP>
-__global__ void __launch_bounds__(256, 2) k_expert_gemv(DecodeArgs a) {
-  constexpr int NM = GATEUP ? 2 : 1;
-  const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
-  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+// Task index = ((g * NRB + rb) * KS + ks) * NBP + nbk with power-of-two NRB,
+// KS, NBP, so it decodes with shifts; the shared expert's tasks follow the
+// routed ones.  A task covers C/KS columns in units of UC.
+template <bool GATEUP, int UC>
+__global__ void __launch_bounds__(kWarpsPerCta * 32, 1) k_expert_stream(DecodeArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  using SG = StageGeo<GATEUP, UC>;
+  constexpr int NM = SG::NM;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3, wib = threadIdx.x >> 5;
+  const int gw = blockIdx.x * kWarpsPerCta + wib, nw = gridDim.x * kWarpsPerCta;
+  uint8_t* wbase = smem + size_t(wib) * (kStages * (SG::BYTES + sizeof(UnitMeta)));
+  UnitMeta* meta = reinterpret_cast<UnitMeta*>(wbase + kStages * SG::BYTES);
   const int G = *a.num_groups;
-  const int total = G * a.nrb_r * a.ks_r + a.nrb_s * a.ks_s;
-  for (int task = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < total; task += nwarps) {
-    GemvTask tk;
-    if (!gemv_task(a, GATEUP, task, G, tk)) break;
-    const DevBlobLayout& lay = tk.shared ? a.lay_s : a.lay_r;
-    const int code_row = tk.C / 2, scale_row = tk.C / 16;
-    const int segs = tk.C / (64 * tk.KS), seg0 = tk.ks * segs;
-    const int row0 = tk.rb * 16 + g8;  // this lane's rows: row0 and row0 + 8
-    const uint8_t* cp[NM];
-    const uint8_t* sp[NM];
-    float gsc[NM];
-#pragma unroll
-    for (int m = 0; m < NM; ++m) {
-      const int mi = GATEUP ? m : 2;
-      cp[m] = tk.blob ? tk.blob + lay.code_off[mi] + size_t(row0) * code_row + 8 * t4 : nullptr;
-      sp[m] = tk.blob ? tk.blob + lay.scale_off[mi] + size_t(row0) * scale_row + t4 : nullptr;
-      gsc[m] = tk.blob ? reinterpret_cast<const BlobHeader*>(tk.blob)->gscale[mi] : 0.f;
+  const int lbits_r = a.l_nrb_r + a.l_ks_r + a.l_nbp, lbits_s = a.l_nrb_s + a.l_ks_s + a.l_nbp;
+  const int routed = G << lbits_r;
+  const int ntask = routed + (a.shared_blob ? (1 << lbits_s) : 0);
+  const int nbmask = (1 << a.l_nbp) - 1;
+
+  // ---- issue side: the warp's cursor over (task, unit); tasks without vectors are skipped
+  int cur = gw, cu = 0;
+  const uint8_t* i_blob = nullptr;
+  int i_shared = 0, i_g = 0, i_rb = 0, i_ks = 0, i_e0 = 0, i_nv = 0, i_jbase = 0, i_units = 0, i_C = 0, i_idx = 0;
+  auto load_task = [&]() {
+    for (; cur < ntask; cur += nw) {
+      int n, r;
+      if (cur < routed) {
+        r = cur;
+        i_shared = 0;
+        i_g = r >> lbits_r;
+        const int rest = r & ((1 << lbits_r) - 1);
+        i_rb = rest >> (a.l_ks_r + a.l_nbp);
+        i_ks = (rest >> a.l_nbp) & ((1 << a.l_ks_r) - 1);
+        i_jbase = (rest & nbmask) * 8;
+        i_e0 = a.grp_off[i_g];
+        n = a.grp_off[i_g + 1] - i_e0;
+        i_C = GATEUP ? a.H : a.I;
+        i_units = (i_C >> a.l_ks_r) / UC;
+      } else {
+        r = cur - routed;
+        i_shared = 1;
+        i_g = G;
+        i_rb = r >> (a.l_ks_s + a.l_nbp);
+        i_ks = (r >> a.l_nbp) & ((1 << a.l_ks_s) - 1);
+        i_jbase = (r & nbmask) * 8;
+        i_e0 = 0;
+        n = a.T;
+        i_C = GATEUP ? a.H : a.I_s;
+        i_units = (i_C >> a.l_ks_s) / UC;
+      }
+      if (i_jbase >= n) continue;
+      i_nv = min(8, n - i_jbase);
+      i_blob = i_shared ? a.shared_blob : a.grp_blob[i_g];
+      // lanes 0..7 hold the index of vector `lane`: its token (gate/up) or output position (down)
+      i_idx = 0;
+      if (lane < i_nv) {
+        const int jj = i_jbase + lane;
+        i_idx = i_shared ? (GATEUP ? jj : a.maxTk + jj) : (GATEUP ? a.ent_tok[i_e0 + jj] : a.ent_pos[i_e0 + jj]);
+      }
+      return;
     }
-    const int nblocks = (tk.n + 7) >> 3;
-    for (int nb = 0; nb < nblocks; ++nb) {
-      const int nv = min(8, tk.n - nb * 8);
-      // the activation vector this lane feeds to B: vector nb*8 + g8 of the group
-      const bool bvalid = g8 < nv;
-      const void* brow = nullptr;
-      float bscale = 1.f;
-      if (bvalid) {
-        const int jj = nb * 8 + g8;
-        if (GATEUP) {
-          const int tok = tk.shared ? jj : a.ent_tok[tk.e0 + jj];
-          brow = a.x16 + size_t(tok) * a.H;
-        } else {
-          const int hr = tk.shared ? a.maxTk + jj : tk.e0 + jj;
-          brow = a.h + size_t(hr) * a.Imax;
-          bscale = pow2_scale_for(a.hmax[hr]);
+  };
+  load_task();
+
+  auto issue = [&](int s) {
+    uint8_t* st = wbase + s * SG::BYTES;
+    UnitMeta& mt = meta[s];
+    if (cur < ntask) {
+      const int kcol = (i_ks * (i_C >> (i_shared ? a.l_ks_s : a.l_ks_r))) + cu * UC;
+      const int code_row = i_C >> 1, scale_row = i_C >> 4;
+      if (i_blob) {
+        const DevBlobLayout& lay = i_shared ? a.lay_s : a.lay_r;
+#pragma unroll
+        for (int c = lane; c < NM * 16 * SG::CPR; c += 32) {
+          const int m = c / (16 * SG::CPR), rr = (c / SG::CPR) % 16, q = c % SG::CPR;
+          cp_async16(st + (m * 16 + rr) * SG::CROW + q * 16,
+                     i_blob + lay.code_off[GATEUP ? m : 2] + size_t(i_rb * 16 + rr) * code_row + kcol / 2 + q * 16);
+        }
+        if (lane < NM * 16) {
+          const int m = lane >> 4, rr = lane & 15;
+          const uint8_t* src = i_blob + lay.scale_off[GATEUP ? m : 2] + size_t(i_rb * 16 + rr) * scale_row + kcol / 16;
+          uint8_t* dst = st + SG::SCALES + (m * 16 + rr) * SG::SROW;
+          if (SG::SROW == 8) cp_async_small<8>(dst, src);
+          else cp_async_small<4>(dst, src);
         }
       }
-      float acc[NM][4];
+#pragma unroll
+      for (int c = lane; c < 8 * SG::XCP; c += 32) {
+        const int v = c / SG::XCP, q = c % SG::XCP;
+        const int idx = __shfl_sync(0xffffffffu, i_idx, v);
+        if (v < i_nv) {
+          const void* src;
+          if (GATEUP) src = a.x16 + size_t(idx) * a.H + kcol + q * 8;
+          else src = a.h + size_t(i_shared ? a.maxTk + i_jbase + v : i_e0 + i_jbase + v) * a.Imax + kcol + q * 4;
+          cp_async16(st + SG::XS + v * SG::XROW + q * 16, src);
+        }
+      }
+      if (lane == 0) {
+        mt.blob = i_blob;
+        mt.task = cur;
+        mt.u = cu;
+        mt.units = i_units;
+        mt.shared = i_shared;
+        mt.g = i_g;
+        mt.rb = i_rb;
+        mt.ks = i_ks;
+        mt.e0 = i_e0;
+        mt.nv = i_nv;
+        mt.jbase = i_jbase;
+      }
+      if (lane < 8) mt.idx[lane] = i_idx;
+      if (++cu == i_units) {
+        cu = 0;
+        cur += nw;
+        load_task();
+      }
+    } else if (lane == 0) {
+      mt.task = -1;
+    }
+    cp_async_commit();
+  };
+
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) issue(s);
+
+  float acc[NM][4];
+#pragma unroll
+  for (int m = 0; m < NM; ++m)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[m][q] = 0.f;
+  for (int i = 0;; ++i) {
+    issue((i + kStages - 1) % kStages);
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    const int s = i % kStages;
+    const UnitMeta& mt = meta[s];
+    if (mt.task < 0) break;
+    const int nv = mt.nv;
+    const uint8_t* st = wbase + s * SG::BYTES;
+    if (mt.blob) {
+      float bsc = 1.f;  // down: power-of-two scale of this lane's vector
+      if (!GATEUP && g8 < nv) bsc = pow2_scale_for(a.hmax[mt.shared ? a.maxTk + mt.jbase + g8 : mt.e0 + mt.jbase + g8]);
+#pragma unroll
+      for (int seg = 0; seg < UC / 64; ++seg) {
+        // B fragments: vector g8, K slots of this lane = 16 contiguous columns
+        uint32_t bx[8];
+        if (g8 < nv) {
+          if (GATEUP) {
+            const uint4* p = reinterpret_cast<const uint4*>(st + SG::XS + g8 * SG::XROW + (seg * 64 + 16 * t4) * 2);
+            const uint4 v0 = p[0], v1 = p[1];
+            bx[0] = v0.x; bx[1] = v0.y; bx[2] = v0.z; bx[3] = v0.w;
+            bx[4] = v1.x; bx[5] = v1.y; bx[6] = v1.z; bx[7] = v1.w;
+          } else {
+            const float4* p = reinterpret_cast<const float4*>(st + SG::XS + g8 * SG::XROW + (seg * 64 + 16 * t4) * 4);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const float4 f = p[v];
+              __half2 h0 = __floats2half2_rn(f.x * bsc, f.y * bsc);
+              __half2 h1 = __floats2half2_rn(f.z * bsc, f.w * bsc);
+              bx[2 * v] = *reinterpret_cast<uint32_t*>(&h0);
+              bx[2 * v + 1] = *reinterpret_cast<uint32_t*>(&h1);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int v = 0; v < 8; ++v) bx[v] = 0u;
+        }
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          const uint8_t* c0p = st + (m * 16 + g8) * SG::CROW + seg * 32 + 8 * t4;
+          const uint2 c0 = *reinterpret_cast<const uint2*>(c0p);
+          const uint2 c1 = *reinterpret_cast<const uint2*>(c0p + 8 * SG::CROW);
+          const uint8_t* sp = st + SG::SCALES + (m * 16 + g8) * SG::SROW + seg * 4 + t4;
+          const uint32_t sc0 = scale_pair(sp[0]), sc1 = scale_pair(sp[8 * SG::SROW]);
+          const uint32_t w0[2] = {c0.x, c0.y}, w1[2] = {c1.x, c1.y};
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb) {
+            uint32_t a0, a1, a2, a3;
+            e2m1_pair2(w0[kb >> 1] >> (16 * (kb & 1)), a0, a2);  // row g: K slots 2t,2t+1 / 2t+8,2t+9
+            e2m1_pair2(w1[kb >> 1] >> (16 * (kb & 1)), a1, a3);  // row g+8
+            mma16816(acc[m], hmul2(a0, sc0), hmul2(a1, sc1), hmul2(a2, sc0), hmul2(a3, sc1), bx[2 * kb],
+                     bx[2 * kb + 1]);
+          }
+        }
+      }
+    }
+    const int u = mt.u, units = mt.units, shared = mt.shared, g = mt.g, rb = mt.rb, ks = mt.ks, e0 = mt.e0;
+    const int jbase = mt.jbase;
+    const uint8_t* blob = mt.blob;
+    const int myidx0 = mt.idx[(2 * t4) & 7], myidx1 = mt.idx[(2 * t4 + 1) & 7];
+    __syncwarp();  // the stage and its metadata are free for a later issue
+    if (u != units - 1) continue;
+
+    // ---- the task's last unit: split-K hand-off, then the rows
+    const int KS = 1 << (shared ? a.l_ks_s : a.l_ks_r);
+    bool finish = true;
+    if (KS > 1) {
+      const int grb = shared ? a.maxG * (1 << a.l_nrb_r) + rb : g * (1 << a.l_nrb_r) + rb;
+      float* pp = a.part + ((size_t(grb) * kMaxSlices + ks) * 32 + lane) * 8;
 #pragma unroll
       for (int m = 0; m < NM; ++m)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[m][q] = 0.f;
-      if (tk.blob) {
-        for (int s0 = 0; s0 < segs; s0 += kSegUnroll) {
-          uint2 cw[kSegUnroll][NM][2];
-          uint32_t sw[kSegUnroll][NM][2];
-          uint32_t bx[kSegUnroll][8];
-#pragma unroll
-          for (int u = 0; u < kSegUnroll; ++u) {
-            const int seg = seg0 + s0 + u;
-            const bool ok = s0 + u < segs;
-#pragma unroll
-            for (int m = 0; m < NM; ++m) {
-              cw[u][m][0] = ok ? ldg_stream_u2(cp[m] + seg * 32) : make_uint2(0, 0);
-              cw[u][m][1] = ok ? ldg_stream_u2(cp[m] + size_t(8) * code_row + seg * 32) : make_uint2(0, 0);
-              sw[u][m][0] = ok ? ldg_u8(sp[m] + seg * 4) : 0u;
-              sw[u][m][1] = ok ? ldg_u8(sp[m] + size_t(8) * scale_row + seg * 4) : 0u;
-            }
-            if (ok && bvalid) {
-              if (GATEUP) {
-                const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __half*>(brow) + seg * 64 + 16 * t4);
-                const uint4 v0 = p[0], v1 = p[1];
-                bx[u][0] = v0.x; bx[u][1] = v0.y; bx[u][2] = v0.z; bx[u][3] = v0.w;
-                bx[u][4] = v1.x; bx[u][5] = v1.y; bx[u][6] = v1.z; bx[u][7] = v1.w;
-              } else {
-                const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(brow) + seg * 64 + 16 * t4);
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                  const float4 f = p[v];
-                  __half2 h0 = __floats2half2_rn(f.x * bscale, f.y * bscale);
-                  __half2 h1 = __floats2half2_rn(f.z * bscale, f.w * bscale);
-                  bx[u][2 * v] = *reinterpret_cast<uint32_t*>(&h0);
-                  bx[u][2 * v + 1] = *reinterpret_cast<uint32_t*>(&h1);
-                }
-              }
-            } else {
-#pragma unroll
-              for (int v = 0; v < 8; ++v) bx[u][v] = 0u;
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < kSegUnroll; ++u) {
-            if (s0 + u < segs) {
-#pragma unroll
-              for (int m = 0; m < NM; ++m) {
-                const uint32_t sc0 = scale_pair(sw[u][m][0]), sc1 = scale_pair(sw[u][m][1]);
-                const uint32_t w0[2] = {cw[u][m][0].x, cw[u][m][0].y}, w1[2] = {cw[u][m][1].x, cw[u][m][1].y};
-#pragma unroll
-                for (int kb = 0; kb < 4; ++kb) {
-                  uint32_t a0, a1, a2, a3;
-                  e2m1_pair2(w0[kb >> 1] >> (16 * (kb & 1)), a0, a2);  // row g: K slots 2t,2t+1 / 2t+8,2t+9
-                  e2m1_pair2(w1[kb >> 1] >> (16 * (kb & 1)), a1, a3);  // row g+8
-                  mma16816(acc[m], hmul2(a0, sc0), hmul2(a1, sc1), hmul2(a2, sc0), hmul2(a3, sc1), bx[u][2 * kb],
-                           bx[u][2 * kb + 1]);
-                }
-              }
-            }
-          }
-        }
-      }
-      // ---- split-K: leave the partial, the last slice of the row block finishes it
-      bool finish = true;
-      if (tk.KS > 1) {
-        const int grb = tk.shared ? a.maxG * a.nrb_r + tk.rb : tk.g * a.nrb_r + tk.rb;
-        float* pp = a.part + ((size_t(grb) * a.ks_max + tk.ks) * 32 + lane) * 8;
+        reinterpret_cast<float4*>(pp)[m] = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+      __threadfence();
+      int old = 0;
+      if (lane == 0) old = atomicAdd(a.cnt + grb, 1);
+      old = __shfl_sync(0xffffffffu, old, 0);
+      finish = old == KS - 1;
+      if (finish) {
+        __threadfence();
 #pragma unroll
         for (int m = 0; m < NM; ++m)
-          reinterpret_cast<float4*>(pp)[m] = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
-        __threadfence();
-        int old = 0;
-        if (lane == 0) old = atomicAdd(a.cnt + grb, 1);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        finish = old == tk.KS - 1;
-        if (finish) {
-          __threadfence();
 #pragma unroll
-          for (int m = 0; m < NM; ++m)
+          for (int q = 0; q < 4; ++q) acc[m][q] = 0.f;
+        for (int k2 = 0; k2 < KS; ++k2) {
+          const float* qp = a.part + ((size_t(grb) * kMaxSlices + k2) * 32 + lane) * 8;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[m][q] = 0.f;
-          for (int s = 0; s < tk.KS; ++s) {
-            const float* qp = a.part + ((size_t(grb) * a.ks_max + s) * 32 + lane) * 8;
-#pragma unroll
-            for (int m = 0; m < NM; ++m) {
-              const float4 f = __ldcg(reinterpret_cast<const float4*>(qp) + m);
-              acc[m][0] += f.x; acc[m][1] += f.y; acc[m][2] += f.z; acc[m][3] += f.w;
-            }
+          for (int m = 0; m < NM; ++m) {
+            const float4 f = __ldcg(reinterpret_cast<const float4*>(qp) + m);
+            acc[m][0] += f.x;
+            acc[m][1] += f.y;
+            acc[m][2] += f.z;
+            acc[m][3] += f.w;
           }
-          if (lane == 0) a.cnt[grb] = 0;  // ready for the next call
         }
+        if (lane == 0) a.cnt[grb] = 0;  // ready for the next call
       }
-      if (!finish) continue;
-      // ---- epilogue: lane holds rows row0, row0+8 x vectors nb*8 + 2*t4 + {0, 1}
+    }
+    if (finish) {
+      float gsc[NM];
+#pragma unroll
+      for (int m = 0; m < NM; ++m)
+        gsc[m] = blob ? reinterpret_cast<const BlobHeader*>(blob)->gscale[GATEUP ? m : 2] : 0.f;
+      const int row0 = rb * 16 + g8;
       float hm[2] = {0.f, 0.f};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int jloc = 2 * t4 + (q & 1);
         const int r = row0 + 8 * (q >> 1);
         if (jloc < nv) {
-          const int jj = nb * 8 + jloc;
+          const int jj = jbase + jloc;
+          const int rowh = shared ? a.maxTk + jj : e0 + jj;  // h row of this vector
+          const int idx = (q & 1) ? myidx1 : myidx0;
           if (GATEUP) {
-            const int tok = tk.shared ? jj : a.ent_tok[tk.e0 + jj];
-            const float inv = 1.0f / a.xscale[tok];
-            const int hrow = tk.shared ? a.maxTk + jj : tk.e0 + jj;
-            const float hv = tk.blob ? silu_f32(acc[0][q] * inv * gsc[0]) * (acc[NM - 1][q] * inv * gsc[NM - 1]) : 0.f;
-            a.h[size_t(hrow) * a.Imax + r] = hv;
+            const float inv = 1.0f / a.xscale[idx];
+            const float hv = blob ? silu_f32(acc[0][q] * inv * gsc[0]) * (acc[NM - 1][q] * inv * gsc[NM - 1]) : 0.f;
+            a.h[size_t(rowh) * a.Imax + r] = hv;
             hm[q & 1] = fmaxf(hm[q & 1], fabsf(hv));
           } else {
-            const int hr = tk.shared ? a.maxTk + jj : tk.e0 + jj;
-            const float inv = 1.0f / pow2_scale_for(a.hmax[hr]);
-            const int orow = tk.shared ? a.maxTk + jj : a.ent_pos[tk.e0 + jj];
-            a.o[size_t(orow) * a.H + r] = tk.blob ? acc[0][q] * inv * gsc[0] : 0.f;
+            const float inv = 1.0f / pow2_scale_for(a.hmax[rowh]);
+            a.o[size_t(idx) * a.H + r] = blob ? acc[0][q] * inv * gsc[0] : 0.f;
           }
         }
       }
       if (GATEUP) {
-        // max|h| over the 16 rows of the block per vector, one atomic per vector
+        // max|h| over the block's 16 rows per vector: one atomic per vector
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
           hm[0] = fmaxf(hm[0], __shfl_xor_sync(0xffffffffu, hm[0], o));
@@ -303,15 +393,20 @@ __global__ void __launch_bounds__(256, 2) k_expert_gemv(DecodeArgs a) {
           for (int q = 0; q < 2; ++q) {
             const int jloc = 2 * t4 + q;
             if (jloc < nv) {
-              const int jj = nb * 8 + jloc;
-              const int hrow = tk.shared ? a.maxTk + jj : tk.e0 + jj;
-              atomicMax(reinterpret_cast<unsigned int*>(a.hmax) + hrow, __float_as_uint(hm[q]));
+              const int jj = jbase + jloc;
+              atomicMax(reinterpret_cast<unsigned int*>(a.hmax) + (shared ? a.maxTk + jj : e0 + jj),
+                        __float_as_uint(hm[q]));
             }
           }
         }
       }
     }
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[m][q] = 0.f;
   }
+  cp_async_wait_all();
 }
 
 // ----------------------------------------------------------------- combine
@@ -319,6 +414,8 @@ __global__ void __launch_bounds__(256, 2) k_expert_gemv(DecodeArgs a) {
 __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ o, const float* __restrict__ w,
                                                  const float* __restrict__ gate_logit, int has_shared, int T, int H,
                                                  int k, int maxTk, void* y, int y_is_fp32) {
+  pdl_trigger();
+  pdl_wait();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   const int per_tok = H / 4;
   if (idx >= T * per_tok) return;
@@ -388,56 +485,69 @@ static DecodeArgs decode_args(const moe_layer_desc* d, int T, moe_ws* ws) {
   a.lay_r = dev_layout(sh.H, sh.I);
   a.lay_s = dev_layout(sh.H, has_shared ? sh.I_shared : sh.I);
   a.err = ws->error;
+  a.part = ws->part;
+  a.cnt = ws->cnt;
   return a;
 }
 
-static int pow2_floor(int v) {
-  int p = 1;
-  while (p * 2 <= v) p *= 2;
-  return p;
+static int log2i(int v) {
+  int l = 0;
+  while ((1 << (l + 1)) <= v) ++l;
+  return l;
 }
 
-// Slices per row block: enough tasks for about four per warp, each slice at
-// least 256 columns.
-static int pick_ks(int C, int row_blocks, int nwarps) {
-  int ks = pow2_floor((4 * nwarps) / (row_blocks > 0 ? row_blocks : 1));
-  const int cap = C / 256 > 0 ? C / 256 : 1;
-  if (ks > cap) ks = cap;
+// K slices: only when every group fits one block of 8 vectors (T <= 8), then
+// one slice per 512 columns (at most kMaxSlices).
+static int slices_for(int C, int T) {
+  if (T > 8) return 1;
+  int ks = C / 512;
   if (ks > kMaxSlices) ks = kMaxSlices;
   return ks < 1 ? 1 : ks;
 }
 
-template <bool GATEUP>
-static int launch_gemv(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s) {
-  DecodeArgs a = decode_args(d, T, ws);
-  const int rows_r = GATEUP ? a.I : a.H, rows_s = GATEUP ? a.I_s : a.H;
-  a.nrb_r = rows_r / 16;
-  a.nrb_s = a.shared_blob ? rows_s / 16 : 0;
-  a.maxG = T * d->s.k < d->s.E ? T * d->s.k : d->s.E;
-  const int blocks = num_sms() * 2;
-  const int nwarps = blocks * 8;
-  const int C_r = GATEUP ? a.H : a.I, C_s = GATEUP ? a.H : (a.I_s ? a.I_s : a.I);
-  // K is split only when every group fits one block of 8 vectors (T <= 8): the
-  // partial scratch and counters are per row block, not per vector block
-  a.ks_r = T <= 8 ? pick_ks(C_r, a.maxG * a.nrb_r + a.nrb_s, nwarps) : 1;
-  a.ks_s = T <= 8 && a.shared_blob ? pick_ks(C_s, a.maxG * a.nrb_r + a.nrb_s, nwarps) : 1;
-  a.ks_max = kMaxSlices;
-  // slices only exist when row blocks are few (at most two per warp), so the
-  // scratch sized for that bound always holds them
-  if ((a.ks_r > 1 || a.ks_s > 1) && size_t(a.maxG * a.nrb_r + a.nrb_s) > ws->split_blocks) return MOE_EINVAL;
-  a.part = ws->part;
-  a.cnt = ws->cnt;
-  k_expert_gemv<GATEUP><<<blocks, 256, 0, s>>>(a);
-  MOE_LAUNCH_CHECK();
+template <bool GATEUP, int UC>
+static int launch_stream_uc(DecodeArgs a, cudaStream_t s) {
+  using SG = StageGeo<GATEUP, UC>;
+  const size_t smem = size_t(kWarpsPerCta) * kStages * (SG::BYTES + sizeof(UnitMeta));
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(k_expert_stream<GATEUP, UC>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+        cudaSuccess)
+      return MOE_ECUDA;
+    attr = true;
+  }
+  if (launch_pdl(k_expert_stream<GATEUP, UC>, dim3(num_sms()), dim3(kWarpsPerCta * 32), smem, s, a) != cudaSuccess)
+    return MOE_ECUDA;
   return MOE_OK;
 }
 
+template <bool GATEUP>
+static int launch_stream(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s) {
+  DecodeArgs a = decode_args(d, T, ws);
+  const int rows_r = GATEUP ? a.I : a.H, rows_s = GATEUP ? a.I_s : a.H;
+  const int C_r = GATEUP ? a.H : a.I, C_s = GATEUP ? a.H : (a.I_s ? a.I_s : a.I);
+  a.l_nrb_r = log2i(rows_r / 16);
+  a.l_nrb_s = a.shared_blob ? log2i(rows_s / 16) : 0;
+  int nbp = 1;
+  while (nbp * 8 < T) nbp *= 2;
+  a.l_nbp = log2i(nbp);
+  a.maxG = T * d->s.k < d->s.E ? T * d->s.k : d->s.E;
+  const int ks_r = slices_for(C_r, T), ks_s = slices_for(C_s, T);
+  a.l_ks_r = log2i(ks_r);
+  a.l_ks_s = log2i(ks_s);
+  // one unit width per launch: 128 columns, or 64 when a matrix slice is narrower
+  const int uc = (C_r / ks_r >= 128 && C_s / ks_s >= 128) ? 128 : 64;
+  if ((ks_r > 1 || ks_s > 1) && size_t(a.maxG) * (size_t(1) << a.l_nrb_r) + (rows_s / 16) > ws->split_blocks)
+    return MOE_EINVAL;
+  return uc == 128 ? launch_stream_uc<GATEUP, 128>(a, s) : launch_stream_uc<GATEUP, 64>(a, s);
+}
+
 int launch_gateup_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s) {
-  return launch_gemv<true>(d, T, ws, s);
+  return launch_stream<true>(d, T, ws, s);
 }
 
 int launch_down_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s) {
-  return launch_gemv<false>(d, T, ws, s);
+  return launch_stream<false>(d, T, ws, s);
 }
 
 int launch_combine(const moe_layer_desc* d, void* y, int y_is_fp32, int T, moe_ws* ws, cudaStream_t s) {
@@ -445,9 +555,9 @@ int launch_combine(const moe_layer_desc* d, void* y, int y_is_fp32, int T, moe_w
   const moe_layer_shape& sh = d->s;
   const int has_shared = sh.I_shared > 0 && d->shared_blob ? 1 : 0;
   const int n = T * (sh.H / 4);
-  k_combine<<<(n + 255) / 256, 256, 0, s>>>(ws->o, ws->topk_w, ws->gate_logit, has_shared, T, sh.H, sh.k,
-                                           ws->maxT * ws->s.k, y, y_is_fp32);
-  MOE_LAUNCH_CHECK();
+  if (launch_pdl(k_combine, dim3((n + 255) / 256), dim3(256), 0, s, ws->o, ws->topk_w, ws->gate_logit, has_shared, T,
+                 sh.H, sh.k, ws->maxT * ws->s.k, y, y_is_fp32) != cudaSuccess)
+    return MOE_ECUDA;
   return MOE_OK;
 }
 

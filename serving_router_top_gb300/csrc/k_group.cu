@@ -53,6 +53,8 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t* __restrict__ ids,
                                                 const uint8_t** __restrict__ grp_blob, int32_t* __restrict__ ent_tok,
                                                 int32_t* __restrict__ ent_pos, unsigned long long* stats, int32_t* err,
                                                 int W, float* __restrict__ hmax, int maxTk) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int sm[];
   int* cnt = sm;                                       // [E]
   int* off = cnt + E;                                  // [E]
@@ -172,11 +174,12 @@ int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* 
       return MOE_ECUDA;
     attr_set = true;
   }
-  k_group<<<1, 1024, smem, s>>>(ids, T, k, E, layer, c ? c->resid : nullptr, c ? c->stage : nullptr,
+  const cudaError_t rc = launch_pdl(k_group, dim3(1), dim3(1024), smem, s, ids, T, k, E, layer, c ? c->resid : nullptr, c ? c->stage : nullptr,
                                 c ? c->slots : nullptr, c ? c->staging : nullptr, c ? c->blob_bytes : 0,
                                 c ? c->nslots : 0, c ? c->nstaging : 0, ws->num_groups, ws->grp_expert, ws->grp_off,
                                 ws->grp_slot, ws->grp_src, ws->grp_blob, ws->ent_tok, ws->ent_pos,
                                 c ? c->stats : nullptr, ws->error, W, ws->hmax, ws->maxT * ws->s.k);
+  if (rc != cudaSuccess) return MOE_ECUDA;
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -19,6 +19,8 @@ namespace moe {
 // ------------------------------------------------------------- heat update
 __global__ void __launch_bounds__(1024) k_heat(float* __restrict__ heat, const int32_t* __restrict__ ids, int n, int E,
                                                int layer, int32_t* err) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int cnt[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -37,8 +39,9 @@ __global__ void __launch_bounds__(1024) k_heat(float* __restrict__ heat, const i
 
 int launch_heat_update(moe_cache* c, const int32_t* ids, int T, int k, int layer, int32_t* err, cudaStream_t s) {
   if (T <= 0) return MOE_OK;
-  k_heat<<<1, 1024, size_t(c->E) * 4, s>>>(c->heat, ids, T * k, c->E, layer, err);
-  MOE_LAUNCH_CHECK();
+  if (launch_pdl(k_heat, dim3(1), dim3(1024), size_t(c->E) * 4, s, c->heat, ids, T * k, c->E, layer, err) !=
+      cudaSuccess)
+    return MOE_ECUDA;
   return MOE_OK;
 }
 

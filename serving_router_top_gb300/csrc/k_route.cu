@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(128) k_router(const uint16_t* __restrict__ x, 
                                                 float* __restrict__ logits, float* __restrict__ gate_logit, int T,
                                                 int H, int E, int rows, __half* __restrict__ x16,
                                                 float* __restrict__ xscale) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint4 smem_x4[];  // [kRouterTokTile][H/8]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.y * kRouterTokTile;
@@ -31,9 +33,11 @@ __global__ void __launch_bounds__(128) k_router(const uint16_t* __restrict__ x, 
     const int t = i / chunks, c = i - t * chunks;
     smem_x4[t * chunks + c] = reinterpret_cast<const uint4*>(x + size_t(t0 + t) * H)[c];
   }
-  if (x16 && blockIdx.x == 0) {
-    // the first block of each token tile also writes the tile's activations as
-    // f16 times a per-token power of two (max|x_t| lands in [2^12, 2^13))
+  if (x16) {
+    // the blocks of a token tile also write its activations as f16 times a
+    // per-token power of two (max|x_t| lands in [2^12, 2^13)); every block finds
+    // the scales from its own copy and converts one slice of the columns
+    __shared__ float s_scale[kRouterTokTile];
     __syncthreads();
     const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem_x4);
     for (int t = warp; t < nt; t += blockDim.x >> 5) {
@@ -41,10 +45,16 @@ __global__ void __launch_bounds__(128) k_router(const uint16_t* __restrict__ x, 
       for (int i = lane; i < H; i += 32) m = fmaxf(m, fabsf(bf16_bits_to_f32(xs[t * H + i])));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      const float sc = pow2_scale_for(m);
-      if (lane == 0) xscale[t0 + t] = sc;
-      for (int i = lane; i < H; i += 32)
-        x16[size_t(t0 + t) * H + i] = __float2half_rn(bf16_bits_to_f32(xs[t * H + i]) * sc);
+      if (lane == 0) s_scale[t] = pow2_scale_for(m);
+    }
+    __syncthreads();
+    if (blockIdx.x == 0 && threadIdx.x < nt) xscale[t0 + threadIdx.x] = s_scale[threadIdx.x];
+    const int per = ((H + gridDim.x - 1) / gridDim.x + 7) & ~7;
+    const int c0 = blockIdx.x * per, c1 = min(H, c0 + per);
+    const int wcols = c1 - c0;
+    for (int i = threadIdx.x; wcols > 0 && i < nt * wcols; i += blockDim.x) {
+      const int t = i / wcols, c = c0 + (i - t * wcols);
+      x16[size_t(t0 + t) * H + c] = __float2half_rn(bf16_bits_to_f32(xs[t * H + c]) * s_scale[t]);
     }
   }
   const int row = blockIdx.x * (blockDim.x >> 5) + warp;
@@ -112,8 +122,9 @@ int launch_router(const uint16_t* x, const uint16_t* w_router, const float* bias
       cudaFuncSetAttribute(k_router, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
     return MOE_ECUDA;
   dim3 grid((rows + 3) / 4, tok_tiles);
-  k_router<<<grid, 128, smem, s>>>(x, w_router ? w_router : w_gate, bias, w_gate, logits, gate_logit, T, H, E_eff,
-                                   rows, x16, xscale);
+  if (launch_pdl(k_router, grid, dim3(128), smem, s, x, w_router ? w_router : w_gate, bias, w_gate, logits,
+                 gate_logit, T, H, E_eff, rows, x16, xscale) != cudaSuccess)
+    return MOE_ECUDA;
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
@@ -125,10 +136,17 @@ int launch_router(const uint16_t* x, const uint16_t* w_router, const float* bias
 // rescans.  Lane r keeps the r-th selection.  NaN logits record MOE_ENAN and
 // rank as -inf.
 __device__ __forceinline__ bool better(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
+// fp32 -> uint32 whose unsigned order is the float order (-inf lowest).
+__device__ __forceinline__ unsigned ordered_key(float f) {
+  const unsigned b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
 
 template <int KPER>
 __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E, int k,
                                               int32_t* __restrict__ ids, float* __restrict__ w, int32_t* err) {
+  pdl_trigger();
+  pdl_wait();
   const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (tok >= T) return;
   const float* lr = logits + size_t(tok) * E;
@@ -161,14 +179,12 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
   int my_id = 0;
   float my_p = 0.f, m = 0.f, den = 0.f;
   for (int r = 0; r < k; ++r) {
-    float wv = bv;
-    int wi = bi;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
-      if (better(ov, oi, wv, wi)) { wv = ov; wi = oi; }
-    }
+    // warp-wide best: the largest value (two warp reductions on order-preserving
+    // integer keys), then the lowest id among the lanes that hold it
+    const unsigned key = ordered_key(bv);
+    const unsigned kmax = __reduce_max_sync(0xffffffffu, key);
+    const int wi = int(__reduce_min_sync(0xffffffffu, key == kmax ? unsigned(bi) : 0x7fffffffu));
+    const float wv = __shfl_sync(0xffffffffu, bv, wi & 31);
     if (r == 0) m = wv;
     const float p = expf(wv - m);
     den += p;
@@ -188,14 +204,15 @@ int launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w
   if (T <= 0) return MOE_OK;
   const int blocks = (T * 32 + 255) / 256;
   const int per = (E + 31) / 32;
-  if (per <= 1) k_topk<1><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w, err);
-  else if (per <= 2) k_topk<2><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w, err);
-  else if (per <= 4) k_topk<4><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w, err);
-  else if (per <= 8) k_topk<8><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w, err);
-  else if (per <= 16) k_topk<16><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w, err);
-  else if (per <= 32) k_topk<32><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w, err);
+  cudaError_t rc = cudaSuccess;
+  if (per <= 1) rc = launch_pdl(k_topk<1>, dim3(blocks), dim3(256), 0, s, logits, T, E, k, ids, w, err);
+  else if (per <= 2) rc = launch_pdl(k_topk<2>, dim3(blocks), dim3(256), 0, s, logits, T, E, k, ids, w, err);
+  else if (per <= 4) rc = launch_pdl(k_topk<4>, dim3(blocks), dim3(256), 0, s, logits, T, E, k, ids, w, err);
+  else if (per <= 8) rc = launch_pdl(k_topk<8>, dim3(blocks), dim3(256), 0, s, logits, T, E, k, ids, w, err);
+  else if (per <= 16) rc = launch_pdl(k_topk<16>, dim3(blocks), dim3(256), 0, s, logits, T, E, k, ids, w, err);
+  else if (per <= 32) rc = launch_pdl(k_topk<32>, dim3(blocks), dim3(256), 0, s, logits, T, E, k, ids, w, err);
   else return MOE_EINVAL;
-  MOE_LAUNCH_CHECK();
+  if (rc != cudaSuccess) return MOE_ECUDA;
   return MOE_OK;
 }
 
