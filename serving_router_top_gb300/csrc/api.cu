@@ -12,6 +12,9 @@ using namespace moe;
 
 namespace {
 
+// AUTO mode runs the prefill (tcgen05 grouped GEMM) path from this many tokens on.
+constexpr int kPrefillMinTokens = 128;
+
 bool shape_ok(const moe_layer_shape& s) {
   // row widths: powers of two from 64 to 4096 (lanes per row and chunks per lane are powers of two)
   auto cols_ok = [](int c) { return c >= 64 && c <= 4096 && (c & (c - 1)) == 0; };
@@ -266,6 +269,9 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   const int rb_max = (s.H > s.I ? s.H : s.I) / 16;
   const size_t split_blocks = size_t(small_groups + 1) * rb_max;
   const size_t o_part = cv.take<float>(split_blocks * 8 * 32 * 8);
+  const size_t o_toff = cv.take<int32_t>(size_t(s.E) + 2);
+  const size_t o_h16 = cv.take<__half>((Tk + maxT) * Imax);
+  const size_t o_yacc = cv.take<float>(size_t(maxT) * s.H);
   const size_t o_cnt = cv.take<int>(split_blocks);
   const size_t o_o = cv.take<float>((Tk + maxT) * s.H);
   const size_t o_err = cv.take<int32_t>(1);
@@ -292,6 +298,9 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   w->h = reinterpret_cast<float*>(base + o_h);
   w->hmax = reinterpret_cast<float*>(base + o_hmax);
   w->part = reinterpret_cast<float*>(base + o_part);
+  w->tile_off = reinterpret_cast<int32_t*>(base + o_toff);
+  w->h16 = reinterpret_cast<__half*>(base + o_h16);
+  w->yacc = reinterpret_cast<float*>(base + o_yacc);
   w->cnt = reinterpret_cast<int*>(base + o_cnt);
   w->split_blocks = split_blocks;
   w->o = reinterpret_cast<float*>(base + o_o);
@@ -398,12 +407,21 @@ int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y
   if (T == 0) return MOE_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int rc;
+  // decode GEMVs for small windows, tcgen05 GEMMs for prefill chunks
+  const bool prefill = mode == MOE_MODE_PREFILL || (mode == MOE_MODE_AUTO && T >= kPrefillMinTokens);
+  if (prefill && (!prefill_supported(s) || (reinterpret_cast<uintptr_t>(x) & 15) ||
+                  (reinterpret_cast<uintptr_t>(d->w_router) & 15) ||
+                  (s.I_shared > 0 && (reinterpret_cast<uintptr_t>(d->w_shared_gate) & 15))))
+    return MOE_EINVAL;
   ws->prof_n = 0;
   {
     ProfScope p(ws, "router", st);
-    if ((rc = launch_router(x, d->w_router, d->bias, s.I_shared > 0 ? d->w_shared_gate : nullptr, ws->logits,
-                            ws->gate_logit, T, s.H, s.E, st, ws->x16, ws->xscale)))
-      return rc;
+    if (prefill)
+      rc = launch_prefill_router(d, x, T, ws, st);
+    else
+      rc = launch_router(x, d->w_router, d->bias, s.I_shared > 0 ? d->w_shared_gate : nullptr, ws->logits,
+                         ws->gate_logit, T, s.H, s.E, st, ws->x16, ws->xscale);
+    if (rc) return rc;
   }
   {
     ProfScope p(ws, "topk", st);
@@ -412,6 +430,10 @@ int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y
   {
     ProfScope p(ws, "group", st);
     if ((rc = launch_group(ws->topk_ids, T, s.k, s.E, d->layer, c, ws, st))) return rc;
+  }
+  if (prefill) {
+    ProfScope p(ws, "prefill_experts", st);
+    return launch_prefill_experts(d, x, y, y_is_fp32, T, ws, st);
   }
   {
     ProfScope p(ws, "gateup_decode", st);

@@ -196,6 +196,9 @@ struct moe_ws {
   float* xscale;        // [maxT] that power of two
   float* h;             // [maxT*k + maxT, max(I, I_shared)] routed entries then shared rows
   float* hmax;          // [maxT*k + maxT] max|h| per row
+  int32_t* tile_off;    // [E + 2] prefill: N tiles before each group
+  __half* h16;          // [maxT*k + maxT, max(I, I_shared)] prefill: h as f16 times a per-row power of two
+  float* yacc;          // [maxT, H] prefill: fp32 output accumulator
   float* part;          // split-K partial tiles: [split_blocks][8 slices][32 lanes][8]
   int* cnt;             // [split_blocks] arrival counters, zero between calls
   size_t split_blocks;

@@ -16,6 +16,13 @@ int launch_gateup_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_
 int launch_down_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s);
 int launch_combine(const moe_layer_desc* d, void* y, int y_is_fp32, int T, moe_ws* ws, cudaStream_t s);
 
+// Prefill path (tcgen05 GEMMs): router logits and gate logit, then the
+// experts, which write y directly.  x rows must be 16-byte aligned.
+bool prefill_supported(const moe_layer_shape& s);
+int launch_prefill_router(const moe_layer_desc* d, const uint16_t* x, int T, moe_ws* ws, cudaStream_t s);
+int launch_prefill_experts(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T, moe_ws* ws,
+                           cudaStream_t s);
+
 // Policy.
 int launch_heat_update(moe_cache* c, const int32_t* ids, int T, int k, int layer, int32_t* err, cudaStream_t s);
 int launch_plan_swaps(moe_cache* c, const moe_policy_cfg* p, moe_swap* plan, int32_t* n, cudaStream_t s);

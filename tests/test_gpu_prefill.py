@@ -1,0 +1,91 @@
+"""GPU parity of the prefill path (tcgen05 grouped GEMMs) against the oracle, through the C ABI.
+
+Small ragged shapes are compared in full; the full-size workloads are compared
+on sampled tokens (a token's output depends only on its own experts and the
+shared expert, so the oracle evaluates just those tokens, routed on the GPU's
+fp32 logits)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import layer as olayer
+from serving_router_top_gb300 import inputs as I
+from serving_router_top_gb300 import moe
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    U.require_gpu()
+
+
+def run_prefill(st, x_bits, T, bf16_out=False):
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda()
+    y = torch.zeros((T, st.H), dtype=torch.int16 if bf16_out else torch.float32, device="cuda")
+    st.forward(0, x, y, T, y_is_fp32=not bf16_out, mode=moe.MOE_MODE_PREFILL)
+    rc = moe.moe_sync_status(st.ws)
+    assert rc == moe.MOE_OK, moe.strerror(rc)
+    return U.y_to_numpy(y, bf16_out)
+
+
+def check_tokens(st, x_bits, y, tokens):
+    logits, ids, _ = st.ws.routing(x_bits.shape[0])
+    logits = logits.cpu().numpy()
+    li = st.layers[0].host
+    # routing on the GPU's own logits matches the oracle's top-k bit for bit
+    ref_ids, _ = olayer.top_k(logits[tokens], st.k)
+    assert np.array_equal(ids.cpu().numpy()[tokens], ref_ids)
+    ref = olayer.moe_layer(x_bits[tokens], li.w_router, li.bias, st.k, lambda e: st.expert_host(0, e), st.H, st.I,
+                           resid=st.resid_table(), stage=st.stage_table(), shared=li.shared, I_shared=st.I_shared,
+                           w_shared_gate_bits=li.w_shared_gate, logits=logits[tokens])
+    return ref
+
+
+@pytest.mark.parametrize("T,H,I_,E,k,Is,zipf", [
+    (300, 256, 128, 16, 2, 128, 0.8),   # ragged token count, groups of many sizes
+    (1024, 128, 64, 8, 2, 64, 0.0),     # narrowest rows; groups above 256 tokens (several N tiles)
+    (129, 512, 256, 40, 7, 0, 1.2),     # no shared expert, small groups
+])
+def test_prefill_small_shapes_full(T, H, I_, E, k, Is, zipf):
+    from serving_router_top_gb300.model import ModelState
+    w = I.small_workload(T=T, H=H, I=I_, E=E, k=k, I_shared=Is, zipf_s=zipf, resident_frac=0.5, seed=T + E)
+    st = ModelState(w)
+    x_bits = I.activations(w.seed, 0, T, H)
+    y = run_prefill(st, x_bits, T)
+    ref = check_tokens(st, x_bits, y, np.arange(T))
+    U.assert_close_layer(y, ref.y)
+    yb = run_prefill(st, x_bits, T, bf16_out=True)
+    U.assert_close_layer(yb, ref.y, bf16_out=True)
+
+
+def test_prefill_chunk_t8192_h2048_e512_k10_sampled():
+    from serving_router_top_gb300.model import ModelState
+    w = I.WORKLOADS["prefill_t8192_h2048_e512_k10"]
+    st = ModelState(w)
+    x_bits = I.activations(w.seed, 0, w.T, w.shape.H)
+    y = run_prefill(st, x_bits, w.T)
+    tokens = np.random.default_rng(4).choice(w.T, 12, replace=False)
+    tokens = np.concatenate([tokens, [0, w.T - 1]])
+    ref = check_tokens(st, x_bits, y, tokens)
+    U.assert_close_layer(y[tokens], ref.y, what="sampled y")
+    # decode and prefill paths agree on a window both can run
+    yd = torch.zeros((64, w.shape.H), dtype=torch.float32, device="cuda")
+    st.forward(0, torch.from_numpy(x_bits[:64].view(np.int16)).cuda(), yd, 64, mode=moe.MOE_MODE_DECODE)
+    assert moe.moe_sync_status(st.ws) == moe.MOE_OK
+    yd = yd.cpu().numpy().astype(np.float64)
+    ref64 = check_tokens(st, x_bits[:64], yd, np.arange(64))
+    U.assert_close_layer(yd, ref64.y, what="decode window")
+
+
+def test_prefill_large_expert_layer_sampled():
+    """One layer of the 4096-hidden, 256-expert top-6 model (I = I_shared = 2048), 4096-token chunk."""
+    from serving_router_top_gb300.model import ModelState
+    w = I.WORKLOADS["large_h4096_e256_k6"]
+    st = ModelState(w, layers=1)
+    x_bits = I.activations(w.seed, 0, w.T, w.shape.H)
+    y = run_prefill(st, x_bits, w.T)
+    tokens = np.random.default_rng(5).choice(w.T, 6, replace=False)
+    ref = check_tokens(st, x_bits, y, tokens)
+    U.assert_close_layer(y[tokens], ref.y, what="sampled y")
