@@ -41,6 +41,7 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true", help="skip the secondary prefill-chunk measurement")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget for cpu_baseline")
     return p.parse_args()
 
@@ -192,7 +193,7 @@ def run_reference(args, w):
 
 # ------------------------------------------------------------------ ours
 def algorithmic_bytes(st, G: int, T: int) -> dict:
-    """Bytes each kernel must move at minimum for one window with G routed groups."""
+    """Bytes each decode kernel must move at minimum for one window with G routed groups."""
     H, I_, E, k, Is = st.H, st.I, st.E, st.k, st.I_shared
     gu = G * 2 * I_ * (H // 2 + H // 16) + (2 * Is * (H // 2 + H // 16) if Is else 0)
     gu += T * H * 2 + (T * k + (T if Is else 0)) * I_ * 4           # activations in, h out
@@ -200,6 +201,133 @@ def algorithmic_bytes(st, G: int, T: int) -> dict:
     dn += (T * k + (T if Is else 0)) * (I_ * 4 + H * 4)               # h in, o out
     router = E * H * 2 + T * H * 2 + T * E * 4
     return {"gateup_decode": gu, "down_decode": dn, "router": router}
+
+
+def prefill_flops(st, T: int) -> dict:
+    """Dense-equivalent FLOPs of the prefill GEMMs for a T-token chunk (every token's k experts + shared)."""
+    H, I_, E, k, Is = st.H, st.I, st.E, st.k, st.I_shared
+    return {"router": 2 * T * H * (E + (1 if Is else 0)),
+            "gateup_gemm": 2 * (T * k * 2 * I_ * H + T * 2 * Is * H),
+            "down_gemm": 2 * (T * k * H * I_ + T * H * Is)}
+
+
+KERNEL_SOURCES = {"gateup_decode": "k_expert.cu", "down_decode": "k_expert.cu", "router": "k_route.cu",
+                  "gateup_gemm": "k_prefill.cu", "down_gemm": "k_prefill.cu"}
+
+
+def source_sha1(name: str) -> str:
+    import hashlib
+    with open(os.path.join(ROOT, "serving_router_top_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+def profiled_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary of `workload`
+    (a line 'bench-traffic: kernel=K source=F sha1=S bytes=N'), or None when there is
+    none or the kernel's source has changed since the counters were taken."""
+    import glob
+    import re
+    pat = re.compile(r"bench-traffic:\s*kernel=(\S+)\s+source=(\S+)\s+sha1=(\w+)\s+bytes=(\d+)")
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", f"*{workload}*.md"))):
+        with open(path) as f:
+            for line in f:
+                m = pat.search(line)
+                if m and m.group(1) == kernel:
+                    try:
+                        if source_sha1(m.group(2)) == m.group(3):
+                            return int(m.group(4))
+                    except OSError:
+                        pass
+                    return None
+    return None
+
+
+def kernel_time_pass(st, step, set_input, flush, steps: int, stream):
+    """Per-kernel durations (CUDA events recorded on the launching stream around each
+    kernel, captured into a graph of the step) averaged over `steps` flushed steps.
+    Kept out of the timed region: the event nodes lengthen the step."""
+    import torch
+    st.ws.set_profiling(True)
+    set_input(0)
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    sums, per_step = {}, 0
+    for i in range(steps):
+        set_input(i)
+        flush.zero_()
+        g.replay()
+        times = st.ws.kernel_times()
+        per_step = len(times)
+        for name, ms in times:
+            sums[name] = sums.get(name, 0.0) + ms
+    torch.cuda.synchronize()
+    st.ws.set_profiling(False)
+    del g
+    return {n: v / steps for n, v in sums.items()}, per_step
+
+
+def measure_prefill(args, peaks):
+    """A short measurement of the prefill chunk (8192 tokens through one layer)."""
+    import torch
+    from serving_router_top_gb300 import inputs as I, moe
+    from serving_router_top_gb300.model import ModelState
+    w = I.WORKLOADS["prefill_t8192_h2048_e512_k10"]
+    s, T = w.shape, w.T
+    st = ModelState(w)
+    xs = [torch.from_numpy(I.activations(w.seed, 20_000 + i, T, s.H).view(np.int16)).cuda() for i in range(2)]
+    x_in = torch.empty_like(xs[0])
+    y = torch.zeros((T, s.H), dtype=torch.int16, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step():
+        st.forward(0, x_in, y, T, y_is_fp32=False, mode=moe.MOE_MODE_PREFILL, stream=stream)
+
+    def set_input(i):
+        x_in.copy_(xs[i % 2])
+
+    with torch.cuda.stream(stream):
+        set_input(0)
+        step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        for i in range(3):
+            set_input(i)
+            flush.zero_()
+            g.replay()
+        torch.cuda.synchronize()
+        n = 20
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            set_input(i)
+            flush.zero_()
+            ev[i][0].record(stream)
+            g.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in ev) / n
+        kt, _ = kernel_time_pass(st, step, set_input, flush, 10, stream)
+    rc = moe.moe_sync_status(st.ws)
+    if rc != moe.MOE_OK:
+        raise RuntimeError(f"device error in prefill measurement: {moe.strerror(rc)}")
+    fl = prefill_flops(st, T)
+    peak = float(peaks["bf16_tflops"])
+    gemms = {}
+    for name in ("router", "gateup_gemm", "down_gemm"):
+        if name in kt:
+            tf = fl[name] / (kt[name] / 1e3) / 1e12
+            gemms[name] = {"us": 1e3 * kt[name], "tflops": tf, "frac": tf / peak}
+    total = sum(fl.values())
+    return {"workload": w.name, "tokens_per_s": T / (ms / 1e3), "ms_per_layer": ms,
+            "tflops_dense_equiv": total / (ms / 1e3) / 1e12, "peak_tflops": peak,
+            "peak_source": "measured bf16_tflops (burst); the GEMMs run kind::f16 on bf16/f16 operands",
+            "kernels_us": {n: 1e3 * v for n, v in kt.items()}, "gemms": gemms,
+            "timing": f"{n} steps, CUDA graph, L2 flushed before each"}
 
 
 def run_ours(args, w):
@@ -230,55 +358,50 @@ def run_ours(args, w):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     ids_ptr = st.ws.view.topk_ids
     ngroups = moe.device_view(st.ws.view.num_groups, (1,), "int32", st.ws)
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()
+    x_in = torch.empty_like(xs[0])
 
-    def step(x):
-        st.forward(0, x, y, T, y_is_fp32=False)
-        moe.cache_heat_update(st.cache, ids_ptr, T, s.k, 0)
+    def step():
+        st.forward(0, x_in, y, T, y_is_fp32=False, stream=stream)
+        moe.cache_heat_update(st.cache, ids_ptr, T, s.k, 0, stream=stream)
+
+    def set_input(i):
+        x_in.copy_(xs[i % P])
 
     # The whole step is captured once in a CUDA graph (the C-ABI calls allocate
     # nothing and never synchronise, so they are capture-safe) and replayed.
-    x_in = torch.empty_like(xs[0])
-    x_in.copy_(xs[0])
-    st.ws.set_profiling(True)
-    step(x_in)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step(x_in)
-    for i in range(args.warmup):
-        x_in.copy_(xs[i % P])
-        flush.zero_()
-        graph.replay()
-    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        set_input(0)
+        step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        for i in range(args.warmup):
+            set_input(i)
+            flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize()
     rc = moe.moe_sync_status(st.ws)
     if rc != moe.MOE_OK:
         raise RuntimeError(f"device error during warm-up: {moe.strerror(rc)}")
 
+    # ---- timed region: K flushed steps, one event pair per step on the launching stream
     sampler = ClockSampler(gpu_id_for(local))
     sampler.start()
     time.sleep(0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    kern_ms = {}
-    kern_bytes = {}
-    launches = 0
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        x_in.copy_(xs[i % P])
-        flush.zero_()
-        a, b = ev[i]
-        a.record(stream)
-        graph.replay()
-        b.record(stream)
-        times = st.ws.kernel_times()          # synchronises on the step's last kernel
-        G = int(ngroups.item())
-        by = algorithmic_bytes(st, G, T)
-        for name, ms in times:
-            kern_ms[name] = kern_ms.get(name, 0.0) + ms
-            kern_bytes[name] = kern_bytes.get(name, 0) + by.get(name, 0)
-        launches += len(times) + 1            # + the heat update
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            set_input(i)
+            flush.zero_()
+            a, b = ev[i]
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -288,27 +411,33 @@ def run_ours(args, w):
     rc = moe.moe_sync_status(st.ws)
     if rc != moe.MOE_OK:
         raise RuntimeError(f"device error in timed region: {moe.strerror(rc)}")
+    G = int(ngroups.item())
 
-    # End to end through the C ABI with host buffers: the graph holds the H2D
-    # copy of the window from pinned memory, the step and the D2H copy of the
-    # output; the host writes the next window into the pinned buffer first.
-    st.ws.set_profiling(False)
+    # ---- per-kernel durations for the roofline (separate pass, same inputs and flushes)
+    with torch.cuda.stream(stream):
+        kt, per_step = kernel_time_pass(st, step, set_input, flush, min(args.steps, 300), stream)
+    launches = (per_step + 1) * args.steps       # the forward's kernels + the heat update, every step
+
+    # ---- end to end through the C ABI with host buffers: the graph holds the
+    # H2D copy of the window from pinned memory, the step and the D2H copy of
+    # the output; the host writes the next window into the pinned buffer first.
     x_pin = torch.empty_like(xs_host[0]).pin_memory()
-    g2 = torch.cuda.CUDAGraph()
     x_pin.copy_(xs_host[0])
-    with torch.cuda.graph(g2):
-        x_in.copy_(x_pin, non_blocking=True)
-        step(x_in)
-        y_host.copy_(y, non_blocking=True)
-    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps):
-        x_pin.copy_(xs_host[i % P])
-        flush.zero_()
-        a, b = ev2[i]
-        a.record(stream)
-        g2.replay()
-        b.record(stream)
-        b.synchronize()
+    with torch.cuda.stream(stream):
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=stream):
+            x_in.copy_(x_pin, non_blocking=True)
+            step()
+            y_host.copy_(y, non_blocking=True)
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            x_pin.copy_(xs_host[i % P])
+            flush.zero_()
+            a, b = ev2[i]
+            a.record(stream)
+            g2.replay()
+            b.record(stream)
+            b.synchronize()
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in ev2)
 
@@ -320,37 +449,45 @@ def run_ours(args, w):
     value = tokens / (total_ms / 1e3)
     e2e_value = tokens / (e2e_ms / 1e3)
     if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
         return
     peaks, src = measured_peaks()
-    dom = max(kern_ms, key=lambda n: kern_ms[n] if n in kern_bytes and kern_bytes[n] else -1)
-    avg_ms = kern_ms[dom] / args.steps
-    avg_bytes = kern_bytes[dom] / args.steps
-    achieved = avg_bytes / (avg_ms / 1e3) / 1e9
+    by = algorithmic_bytes(st, G, T)
+    dom = max((n for n in kt if n in by), key=lambda n: kt[n])
+    avg_ms = kt[dom]
+    achieved = by[dom] / (avg_ms / 1e3) / 1e9
     peak = float(peaks["hbm_gbs"])
+    traffic = profiled_traffic(w.name, dom)
     clocks = sampler.summary()
     out = {
         "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp4-e2m1 weights, f16/f32 math",
-        "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e2m1 weights; f16 x f16 -> f32 math", "data": "synthetic",
         "config": {"workload": w.name, "tokens_per_window": T, "hidden": s.H, "experts": s.E, "top_k": s.k,
                    "intermediate": s.I, "shared_intermediate": s.I_shared, "zipf_s": w.zipf_s,
                    "resident_frac": w.resident_frac, "l2": "flushed (256 MB write) before every timed step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_source": f"{src} hbm_gbs",
-                     "algorithmic_bytes_per_launch": avg_bytes, "avg_launch_us": avg_ms * 1e3},
-        "kernels_us_per_step": {n: 1e3 * v / args.steps for n, v in kern_ms.items()},
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": f"{src} hbm_gbs",
+                     "algorithmic_bytes_per_launch": by[dom], "avg_launch_us": avg_ms * 1e3,
+                     "duration": "CUDA events around the kernel on its stream, separate pass of "
+                                 f"{min(args.steps, 300)} flushed steps"},
+        "kernels_us_per_step": {n: 1e3 * v for n, v in kt.items()},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * s.H * 2,
                 "d2h_bytes_per_step": T * s.H * 2},
         "gpu_launches": launches,
     }
+    if not args.no_prefill:
+        out["prefill"] = measure_prefill(args, peaks)
     if not args.no_cpu_baseline:
         v, tok, calls, el = oracle_sample(w, args.cpu_seconds)
         out["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                                "sample": f"{calls} oracle layer calls x {w.T} tokens ({tok} tokens, {el:.1f} s), "
-                                         f"fp64 numpy, same workload, seeded windows"}
+                                         f"fp64 numpy (BLAS threads over the host's cores), same workload, "
+                                         f"seeded windows"}
     print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()

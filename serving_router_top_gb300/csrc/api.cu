@@ -431,10 +431,7 @@ int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y
     ProfScope p(ws, "group", st);
     if ((rc = launch_group(ws->topk_ids, T, s.k, s.E, d->layer, c, ws, st))) return rc;
   }
-  if (prefill) {
-    ProfScope p(ws, "prefill_experts", st);
-    return launch_prefill_experts(d, x, y, y_is_fp32, T, ws, st);
-  }
+  if (prefill) return launch_prefill_experts(d, x, y, y_is_fp32, T, ws, st);
   {
     ProfScope p(ws, "gateup_decode", st);
     if ((rc = launch_gateup_decode(d, T, ws, st))) return rc;

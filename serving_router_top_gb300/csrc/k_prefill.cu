@@ -707,20 +707,33 @@ int launch_prefill_experts(const moe_layer_desc* d, const uint16_t* x, void* y, 
   Args a = base_args(d, T, ws);
   float* yacc = y_is_fp32 ? static_cast<float*>(y) : ws->yacc;
   a.yacc = yacc;
-  if (launch_pdl(k_tiles, dim3(1), dim3(1024), 0, s, ws->num_groups, ws->grp_off, ws->tile_off) != cudaSuccess)
-    return MOE_ECUDA;
-  MOE_CUDA_TRY(cudaMemsetAsync(yacc, 0, size_t(T) * sh.H * 4, s));
-  a.bsrc = x;
-  a.bstride = sh.H;
+  {
+    ProfScope p(ws, "tiles_zero", s);
+    if (launch_pdl(k_tiles, dim3(1), dim3(1024), 0, s, ws->num_groups, ws->grp_off, ws->tile_off) != cudaSuccess)
+      return MOE_ECUDA;
+    MOE_CUDA_TRY(cudaMemsetAsync(yacc, 0, size_t(T) * sh.H * 4, s));
+  }
   int rc;
-  if ((rc = launch_gemm<kGateUp>(a, s))) return rc;
-  if (launch_pdl(k_h16, dim3(sm_count() * 8), dim3(256), 0, s, ws->h, ws->hmax, ws->h16, ws->grp_off, ws->num_groups,
-                 a.Imax, a.maxTk, T, a.shared_blob ? 1 : 0) != cudaSuccess)
-    return MOE_ECUDA;
-  a.bsrc = reinterpret_cast<const uint16_t*>(ws->h16);
-  a.bstride = a.Imax;
-  if ((rc = launch_gemm<kDown>(a, s))) return rc;
+  {
+    ProfScope p(ws, "gateup_gemm", s);
+    a.bsrc = x;
+    a.bstride = sh.H;
+    if ((rc = launch_gemm<kGateUp>(a, s))) return rc;
+  }
+  {
+    ProfScope p(ws, "h16", s);
+    if (launch_pdl(k_h16, dim3(sm_count() * 8), dim3(256), 0, s, ws->h, ws->hmax, ws->h16, ws->grp_off,
+                   ws->num_groups, a.Imax, a.maxTk, T, a.shared_blob ? 1 : 0) != cudaSuccess)
+      return MOE_ECUDA;
+  }
+  {
+    ProfScope p(ws, "down_gemm", s);
+    a.bsrc = reinterpret_cast<const uint16_t*>(ws->h16);
+    a.bstride = a.Imax;
+    if ((rc = launch_gemm<kDown>(a, s))) return rc;
+  }
   if (!y_is_fp32) {
+    ProfScope p(ws, "cast", s);
     const size_t n4 = size_t(T) * sh.H / 4;
     if (launch_pdl(k_cast_bf16, dim3(sm_count() * 8), dim3(256), 0, s, ws->yacc, static_cast<uint16_t*>(y), n4) !=
         cudaSuccess)
