@@ -265,6 +265,31 @@ typedef struct {
  *   becomes fl32(heat * decay).  Requires L*E <= 32768 and max_swaps <= 4096. */
 int cache_plan_swaps(moe_cache* c, const moe_policy_cfg* p, moe_swap* plan_dev, int32_t* n_dev, moe_stream_t stream);
 
+/* cache_plan_swaps on caller-owned tables, allocating nothing.  The pages
+ * have no counterpart to this call: it exists for callers that cannot
+ * allocate device memory where they plan -- a serving loop whose memory is
+ * handed out by its own allocator under a fixed budget (a cudaMalloc would
+ * step outside the budget or fail when it is spent), or one that keeps the
+ * heat and residency tables in its own buffers without a moe_cache handle.
+ *   heat_dev  float [L, E] device, read and then decayed in place (as the
+ *             handle's heat table is by cache_plan_swaps);
+ *   resid_dev int32 [L, E] device, slot of each resident expert, negative
+ *             when not resident (the layout of moe_cache_view.resid).
+ * The plan, its order, n_dev and the decayed heats are exactly those of
+ * cache_plan_swaps on the same tables.  The planner's scratch is a 260 KB
+ * static device array inside the library, so the sizes it takes are capped:
+ * L <= 1024, E <= 1024, L*E <= 32768 and L*ceil(E/2) <= 16384; larger sizes
+ * (and max_swaps outside 0..4096, threshold <= 0, NULL pointers) return
+ * MOE_EINVAL before anything is launched.  Nothing in the scratch needs to
+ * start at zero.  The scratch's address is looked up on the first call on
+ * each device (with that device current); the lookup may load the module,
+ * which a stream capture does not allow, so make the first call on each
+ * device before any capture.  All calls on one device share the scratch:
+ * calls that overlap in time (other streams, other threads) race and must
+ * be serialised by the caller. */
+int cache_plan_swaps_noalloc(float* heat_dev, const int32_t* resid_dev, int L, int E, const moe_policy_cfg* p,
+                             moe_swap* plan_dev, int32_t* n_dev, moe_stream_t stream);
+
 /* Execute a plan (same section: new weights are visible only after the copy
  * completes; a slot is reused only after earlier reads finished):
  *   on `compute`: unmap each cold expert (resid = -1), record event

@@ -28,6 +28,16 @@ int launch_heat_update(moe_cache* c, const int32_t* ids, int T, int k, int layer
 int launch_plan_swaps(moe_cache* c, const moe_policy_cfg* p, moe_swap* plan, int32_t* n, cudaStream_t s);
 int launch_apply_swaps(moe_cache* c, const moe_swap* plan, const int32_t* n, int max_swaps, cudaStream_t compute,
                        cudaStream_t copy);
+// Planner kernels (defined with the policy), also launched on caller tables.
+__global__ void __launch_bounds__(1024) k_plan_layer(float* __restrict__ heat, const int32_t* __restrict__ resid, int E,
+                                                     int P, float threshold, float decay,
+                                                     unsigned long long* __restrict__ cand, int cand_stride,
+                                                     int32_t* __restrict__ cand_count, int32_t* __restrict__ cold_of);
+__global__ void __launch_bounds__(1024) k_plan_merge(const unsigned long long* __restrict__ cand, int cand_stride,
+                                                     const int32_t* __restrict__ cand_count, int L, int E, int P,
+                                                     const int32_t* __restrict__ resid,
+                                                     const int32_t* __restrict__ cold_of, int max_swaps,
+                                                     moe_swap* __restrict__ plan, int32_t* __restrict__ n_out);
 int launch_blob_copy(moe_cache* c, const int32_t* src_index, const int32_t* dst_index, int n, int to_staging,
                      cudaStream_t s);
 

@@ -26,6 +26,7 @@ EXPORTED = (
     "moe_cache_fill", "moe_cache_get_view", "moe_get_stats", "moe_ws_create", "moe_ws_destroy", "moe_ws_get_view",
     "moe_sync_status", "moe_strerror", "moe_route", "moe_group", "moe_layer_forward", "cache_heat_update",
     "cache_plan_swaps", "moe_cache_apply_swaps", "moe_ws_set_profiling", "moe_ws_kernel_times",
+    "cache_plan_swaps_noalloc",
 )
 
 
@@ -98,6 +99,7 @@ def load() -> C.CDLL:
         "moe_layer_forward": (I, [C.POINTER(moe_layer_desc), P, P, I, I, P, P, I, P]),
         "cache_heat_update": (I, [P, P, I, I, I, P, P]),
         "cache_plan_swaps": (I, [P, C.POINTER(moe_policy_cfg), P, P, P]),
+        "cache_plan_swaps_noalloc": (I, [P, P, I, I, C.POINTER(moe_policy_cfg), P, P, P]),
         "moe_cache_apply_swaps": (I, [P, P, P, P, P]),
         "moe_ws_set_profiling": (I, [P, I]),
         "moe_ws_kernel_times": (I, [P, I, P, P, C.POINTER(C.c_int)]),
@@ -316,6 +318,22 @@ def cache_plan_swaps(cache: Cache, threshold: float, max_swaps: int, decay: floa
     cfg = moe_policy_cfg(threshold, max_swaps, decay)
     _check(load().cache_plan_swaps(cache.handle, C.byref(cfg), _ptr(plan_dev), _ptr(n_dev), _stream(stream)),
            "cache_plan_swaps")
+
+
+# Capacity of the static scratch behind cache_plan_swaps_noalloc.
+NOALLOC_MAX_L, NOALLOC_MAX_E, NOALLOC_MAX_LE, NOALLOC_MAX_KEYS = 1024, 1024, 32768, 16384
+
+
+def cache_plan_swaps_noalloc(heat_dev, resid_dev, L: int, E: int, threshold: float, max_swaps: int, decay: float,
+                             plan_dev, n_dev, stream=None) -> None:
+    """Swap planning on caller-owned heat [L, E] (decayed in place) and residency [L, E] tables; allocates nothing."""
+    if not (1 <= L <= NOALLOC_MAX_L and 1 <= E <= NOALLOC_MAX_E and L * E <= NOALLOC_MAX_LE
+            and L * ((E + 1) // 2) <= NOALLOC_MAX_KEYS):
+        raise ValueError(f"cache_plan_swaps_noalloc: L={L}, E={E} exceed the static scratch (L <= {NOALLOC_MAX_L}, "
+                         f"E <= {NOALLOC_MAX_E}, L*E <= {NOALLOC_MAX_LE}, L*ceil(E/2) <= {NOALLOC_MAX_KEYS})")
+    cfg = moe_policy_cfg(threshold, max_swaps, decay)
+    _check(load().cache_plan_swaps_noalloc(_ptr(heat_dev), _ptr(resid_dev), L, E, C.byref(cfg), _ptr(plan_dev),
+                                           _ptr(n_dev), _stream(stream)), "cache_plan_swaps_noalloc")
 
 
 def moe_cache_apply_swaps(cache: Cache, plan_dev, n_dev, compute=None, copy=None) -> None:
