@@ -543,11 +543,13 @@ static int launch_stream(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_
 }
 
 int launch_gateup_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s) {
-  return launch_stream<true>(d, T, ws, s);
+  const int rc = launch_gemv_decode(true, d, T, ws, s);
+  return rc == kGemvNotApplicable ? launch_stream<true>(d, T, ws, s) : rc;
 }
 
 int launch_down_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s) {
-  return launch_stream<false>(d, T, ws, s);
+  const int rc = launch_gemv_decode(false, d, T, ws, s);
+  return rc == kGemvNotApplicable ? launch_stream<false>(d, T, ws, s) : rc;
 }
 
 int launch_combine(const moe_layer_desc* d, void* y, int y_is_fp32, int T, moe_ws* ws, cudaStream_t s) {
