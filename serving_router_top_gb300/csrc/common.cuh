@@ -126,6 +126,45 @@ __device__ __forceinline__ float pow2_scale_for(float amax) {
   return ldexpf(1.0f, 13 - e);  // amax * 2^(13-e) in [2^12, 2^13)
 }
 
+// y[t] cols 4c4..4c4+3 = sum_r w[t,r] * o[t*k + r] (rank order) + sigmoid(g_t) * o[shared t],
+// with the rows' loads issued eight at a time so their latencies overlap.
+template <bool LDCG>
+__device__ __forceinline__ float4 combine4(const float* o, const float* w, const float* gate_logit, bool has_shared,
+                                           int t, int c4, int H, int k, int maxTk) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r0 = 0; r0 < k; r0 += 8) {
+    float4 v[8];
+    float wr[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (r0 + j < k) {
+        const float4* p = reinterpret_cast<const float4*>(o + size_t(t * k + r0 + j) * H) + c4;
+        v[j] = LDCG ? __ldcg(p) : *p;
+        wr[j] = w[t * k + r0 + j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (r0 + j < k) {
+        acc.x = fmaf(wr[j], v[j].x, acc.x);
+        acc.y = fmaf(wr[j], v[j].y, acc.y);
+        acc.z = fmaf(wr[j], v[j].z, acc.z);
+        acc.w = fmaf(wr[j], v[j].w, acc.w);
+      }
+    }
+  }
+  if (has_shared) {
+    const float gm = sigmoid_f32(gate_logit[t]);
+    const float4* p = reinterpret_cast<const float4*>(o + size_t(maxTk + t) * H) + c4;
+    const float4 sv = LDCG ? __ldcg(p) : *p;
+    acc.x = fmaf(gm, sv.x, acc.x);
+    acc.y = fmaf(gm, sv.y, acc.y);
+    acc.z = fmaf(gm, sv.z, acc.z);
+    acc.w = fmaf(gm, sv.w, acc.w);
+  }
+  return acc;
+}
+
 // ---------------------------------------------------------------- launches
 // Programmatic dependent launch: every hot-path kernel lets its successor be
 // scheduled as soon as all of its own CTAs are running (pdl_trigger at entry)
@@ -203,6 +242,7 @@ struct moe_ws {
   int* cnt;             // [split_blocks] arrival counters, zero between calls
   size_t split_blocks;
   float* o;             // [maxT*k + maxT, H] routed outputs by position, then shared outputs
+  int* tick;            // [maxT/8 + 2] arrival counters of last-CTA fusions, zero between calls
   int32_t* error;       // [1]
   // optional per-kernel timing of the most recent call
   int prof_on, prof_n;

@@ -420,23 +420,7 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ o, co
   const int per_tok = H / 4;
   if (idx >= T * per_tok) return;
   const int t = idx / per_tok, c4 = idx - t * per_tok;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int r = 0; r < k; ++r) {
-    const float wr = w[t * k + r];
-    const float4 v = reinterpret_cast<const float4*>(o + size_t(t * k + r) * H)[c4];
-    acc.x = fmaf(wr, v.x, acc.x);
-    acc.y = fmaf(wr, v.y, acc.y);
-    acc.z = fmaf(wr, v.z, acc.z);
-    acc.w = fmaf(wr, v.w, acc.w);
-  }
-  if (has_shared) {
-    const float gm = sigmoid_f32(gate_logit[t]);
-    const float4 s = reinterpret_cast<const float4*>(o + size_t(maxTk + t) * H)[c4];
-    acc.x = fmaf(gm, s.x, acc.x);
-    acc.y = fmaf(gm, s.y, acc.y);
-    acc.z = fmaf(gm, s.z, acc.z);
-    acc.w = fmaf(gm, s.w, acc.w);
-  }
+  const float4 acc = combine4<false>(o, w, gate_logit, has_shared != 0, t, c4, H, k, maxTk);
   if (y_is_fp32) {
     reinterpret_cast<float4*>(y)[size_t(t) * per_tok + c4] = acc;
   } else {

@@ -33,7 +33,7 @@ constexpr int kChunk = 256;        // columns per chunk (a lane's 64 columns = o
 constexpr int kXPadH = 8;          // f16 elements after each activation row
 constexpr int kDownGroups = 4;     // down: groups whose h rows a CTA keeps in shared memory
 constexpr int kMaxRound = 16;      // tasks per round at most
-constexpr size_t kSmemBudget = 227 * 1024;
+constexpr size_t kSmemBudget = 226 * 1024;  // leaves room for static shared variables
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
@@ -106,8 +106,6 @@ struct Args {
   const uint8_t* const* grp_blob;
   const int32_t* ent_tok;
   const int32_t* ent_pos;
-  const __half* x16;     // [T, H] f16, x * xscale
-  const float* xscale;   // [T]
   float* h;              // [(maxTk + maxT) * Imax]
   float* hmax;           // [maxTk + maxT]
   float* o;              // [(maxTk + maxT) * H]
@@ -116,6 +114,8 @@ struct Args {
   DevBlobLayout lay;     // routed and shared blobs share H and I here
   Geo geo;
   int32_t* err;
+  const __half* x16;     // gate/up: [T, H] f16, x times a per-token power of two
+  const float* xscale;   // gate/up: [T] that power of two
 };
 
 struct Smem {
@@ -173,14 +173,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_gemv(Args a) {
     if (i <= a.Tk) S.blob[i] = i < G ? b : (i == G ? a.shared_blob : nullptr);
   }
   for (int i = tid; i < a.Tk; i += blockDim.x) S.idx[i] = GATEUP ? a.ent_tok[i] : a.ent_pos[i];
-  if (GATEUP)
-    for (int t = tid; t < a.T; t += blockDim.x) S.vinv[t] = 1.0f / a.xscale[t];
   const int ngr = G + (a.shared_blob ? 1 : 0);
   const int NT = ngr * g.TPG;
   const int t_begin = int((long long)blockIdx.x * NT / gridDim.x);
   const int t_end = int((long long)(blockIdx.x + 1) * NT / gridDim.x);
   __syncthreads();
-  if (t_begin >= t_end) return;  // uniform across the CTA
+  if (t_begin >= t_end) return;  // uniform across the CTA (and not counted by the combine below)
 
   const int rbw = warp / g.KPW, kc = warp - rbw * g.KPW;
   const bool computes = rbw < g.RB;
@@ -227,6 +225,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_gemv(Args a) {
       const int t = c / cpr, q = c - t * cpr;
       cp16(S.xs + size_t(t) * g.xrow + q * 8, a.x16 + size_t(t) * a.H + q * 8);
     }
+    if (tid < a.T) cp4(S.vinv + tid, a.xscale + tid);
   } else {
     const int per = a.I / 4;
     for (int gi = g_first; gi <= g_last; ++gi) {
@@ -259,7 +258,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_gemv(Args a) {
     for (int m = 0; m < NM; ++m) S.gs[2 * (g_first + tid) + m] = gsr[m];
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  if (!GATEUP) {
+  if (GATEUP) {
+    if (tid < a.T) S.vinv[tid] = 1.0f / S.vinv[tid];
+    __syncthreads();
+  } else {
     // h -> f16 times the power of two chosen from max|h| of its row
     const int per = a.I / 4;
     for (int gi = g_first; gi <= g_last; ++gi) {
@@ -418,6 +420,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_gemv(Args a) {
       }
     }
   }
+
 }
 
 }  // namespace gemv
@@ -494,15 +497,25 @@ bool make_geo(bool gateup, const moe_layer_shape& sh, int T, int Tk, int grid, g
 
 }  // namespace
 
+bool gemv_decode_applicable(bool gateup, const moe_layer_desc* d, int T) {
+  using namespace gemv;
+  const moe_layer_shape& sh = d->s;
+  const bool has_shared = sh.I_shared > 0 && d->shared_blob;
+  if (T < 1 || T > 8 || (has_shared && sh.I_shared != sh.I) ||
+      (has_shared && (reinterpret_cast<uintptr_t>(d->shared_blob) & 31)))
+    return false;
+  Geo g;
+  size_t smem = 0;
+  return make_geo(gateup, sh, T, T * sh.k, sm_count_gemv(), g, smem);
+}
+
 // Decode GEMV for windows of at most 8 tokens; returns kGemvNotApplicable when
 // the shapes call for the general kernel.
 int launch_gemv_decode(bool gateup, const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s) {
   using namespace gemv;
   const moe_layer_shape& sh = d->s;
   const bool has_shared = sh.I_shared > 0 && d->shared_blob;
-  if (T < 1 || T > 8 || (has_shared && sh.I_shared != sh.I) ||
-      (has_shared && (reinterpret_cast<uintptr_t>(d->shared_blob) & 31)))
-    return kGemvNotApplicable;
+  if (!gemv_decode_applicable(gateup, d, T)) return kGemvNotApplicable;
   const int Tk = T * sh.k;
   const int grid = sm_count_gemv();
   Args a;
@@ -513,8 +526,6 @@ int launch_gemv_decode(bool gateup, const moe_layer_desc* d, int T, moe_ws* ws, 
   a.grp_blob = ws->grp_blob;
   a.ent_tok = ws->ent_tok;
   a.ent_pos = ws->ent_pos;
-  a.x16 = ws->x16;
-  a.xscale = ws->xscale;
   a.h = ws->h;
   a.hmax = ws->hmax;
   a.o = ws->o;
@@ -527,6 +538,8 @@ int launch_gemv_decode(bool gateup, const moe_layer_desc* d, int T, moe_ws* ws, 
   a.Tk = Tk;
   a.lay = dev_layout(sh.H, sh.I);
   a.err = ws->error;
+  a.x16 = ws->x16;
+  a.xscale = ws->xscale;
   auto kern = gateup ? k_gemv<true, 2> : k_gemv<false, 3>;
   static bool attr_set[2] = {false, false};
   if (!attr_set[gateup]) {

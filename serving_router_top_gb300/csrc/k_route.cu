@@ -9,11 +9,109 @@
 
 namespace moe {
 
+// ------------------------------------------------------------------- top-k
+// One warp per token; lane j holds logits j, j+32, ... (KPER per lane).
+// Each lane keeps its best untaken entry; a round takes the warp-wide best by
+// (value desc, id asc) with a shuffle reduction and only the owning lane
+// rescans.  Lane r keeps the r-th selection.  NaN logits record MOE_ENAN and
+// rank as -inf.
+// fp32 -> uint32 whose unsigned order is the float order (-inf lowest).
+__device__ __forceinline__ unsigned ordered_key(float f) {
+  const unsigned b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// The float whose order_key is k (exact inverse).
+__device__ __forceinline__ float float_of_key(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Top-k of one token by one warp.  Lane l holds logits l, l+32, ... (KPER per
+// lane) as order-preserving keys (0 below every real key for entries past E),
+// sorted once per lane by (key desc, id asc) with a register bitonic network;
+// each round then takes the warp-wide best head -- the largest key, ties to
+// the lowest id -- and the winning lane shifts its list.  Lane r writes the
+// r-th selection; weights are exp(l - l_0) / sum over the chosen.  NaN logits
+// record MOE_ENAN and rank as -inf.  LDCG: read the logits through L2 (they
+// were written by other CTAs of the same kernel).
+template <int KPER, bool LDCG>
+__device__ __forceinline__ void topk_token(const float* lr, int E, int k, int lane, int32_t* ids, float* w,
+                                           int32_t* err) {
+  unsigned u[KPER];
+  int jj[KPER];
+  bool nan_seen = false;
+#pragma unroll
+  for (int j = 0; j < KPER; ++j) {
+    const int e = lane + 32 * j;
+    unsigned key = 0u;
+    if (e < E) {
+      float x = LDCG ? __ldcg(lr + e) : lr[e];
+      if (x != x) { nan_seen = true; x = -INFINITY; }
+      key = ordered_key(x);
+    }
+    u[j] = key;
+    jj[j] = j;
+  }
+  if (__any_sync(0xffffffffu, nan_seen) && lane == 0) set_error(err, MOE_ENAN);
+  // (key desc, j asc): j orders like the expert id within a lane
+  auto first = [](unsigned ka, int ja, unsigned kb, int jb) { return ka > kb || (ka == kb && ja < jb); };
+#pragma unroll
+  for (int size = 2; size <= KPER; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int i = 0; i < KPER; ++i) {
+        const int l = i ^ stride;
+        if (l > i) {
+          const bool desc = (i & size) == 0;
+          const bool sw = desc ? first(u[l], jj[l], u[i], jj[i]) : first(u[i], jj[i], u[l], jj[l]);
+          if (sw) {
+            const unsigned tu = u[i];
+            u[i] = u[l];
+            u[l] = tu;
+            const int tj = jj[i];
+            jj[i] = jj[l];
+            jj[l] = tj;
+          }
+        }
+      }
+    }
+  }
+  int my_id = 0;
+  float my_p = 0.f, m = 0.f, den = 0.f;
+  for (int r = 0; r < k; ++r) {
+    const unsigned kmax = __reduce_max_sync(0xffffffffu, u[0]);
+    const unsigned id = unsigned(lane + 32 * jj[0]);
+    const int wi = int(__reduce_min_sync(0xffffffffu, u[0] == kmax ? id : 0x7fffffffu));
+    const float wv = float_of_key(kmax);
+    if (r == 0) m = wv;
+    const float p = expf(wv - m);
+    den += p;
+    if (lane == r) { my_id = wi; my_p = p; }
+    if (lane == (wi & 31)) {
+#pragma unroll
+      for (int i = 0; i + 1 < KPER; ++i) {
+        u[i] = u[i + 1];
+        jj[i] = jj[i + 1];
+      }
+      u[KPER - 1] = 0u;
+      jj[KPER - 1] = KPER;
+    }
+  }
+  if (lane < k) {
+    ids[lane] = my_id;
+    w[lane] = my_p / den;
+  }
+}
+
 // ------------------------------------------------------------------ router
 // One warp per (row, token tile): row e < E is a router row, row E the
-// shared-expert gate vector.  The tile's bf16 activations sit in shared
-// memory; each lane first issues every 16-byte load of its part of the
-// weight row, then accumulates in fp32 (bf16 x bf16 products are exact).
+// shared-expert gate vector.  Each lane issues every 16-byte load of its part
+// of the weight row first -- before waiting for the previous kernel, since no
+// kernel writes the weights -- then stages the tile's bf16 activations in
+// shared memory and accumulates in fp32 (bf16 x bf16 products are exact).
+// With tick, the last CTA of each token tile to finish (an arrival counter,
+// no waiting) also runs top-k for the tile's tokens.
 constexpr int kRouterTokTile = 8;
 constexpr int kRouterMaxChunksPerLane = 16;  // H <= 4096
 
@@ -21,17 +119,41 @@ __global__ void __launch_bounds__(128) k_router(const uint16_t* __restrict__ x, 
                                                 const float* __restrict__ bias, const uint16_t* __restrict__ w_gate,
                                                 float* __restrict__ logits, float* __restrict__ gate_logit, int T,
                                                 int H, int E, int rows, __half* __restrict__ x16,
-                                                float* __restrict__ xscale) {
+                                                float* __restrict__ xscale, int k, int32_t* __restrict__ ids,
+                                                float* __restrict__ wts, int32_t* err, int* tick) {
   pdl_trigger();
-  pdl_wait();
   extern __shared__ uint4 smem_x4[];  // [kRouterTokTile][H/8]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.y * kRouterTokTile;
   const int nt = min(kRouterTokTile, T - t0);
   const int chunks = H / 8;
-  for (int i = threadIdx.x; i < nt * chunks; i += blockDim.x) {
-    const int t = i / chunks, c = i - t * chunks;
-    smem_x4[t * chunks + c] = reinterpret_cast<const uint4*>(x + size_t(t0 + t) * H)[c];
+  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
+  const bool live = row < rows;
+  const uint16_t* wrow = live ? (row < E ? w_router + size_t(row) * H : w_gate) : nullptr;
+  uint4 wv[kRouterMaxChunksPerLane];
+#pragma unroll
+  for (int i = 0; i < kRouterMaxChunksPerLane; ++i) {
+    const int c = lane + 32 * i;
+    wv[i] = (live && c < chunks) ? __ldg(reinterpret_cast<const uint4*>(wrow) + c) : make_uint4(0, 0, 0, 0);
+  }
+  pdl_wait();
+  {
+    // the tile's rows are contiguous: up to 8 independent loads in flight per thread, then the stores
+    const uint4* xt = reinterpret_cast<const uint4*>(x + size_t(t0) * H);
+    const int n = nt * chunks;
+    for (int base = 0; base < n; base += 8 * blockDim.x) {
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + j * blockDim.x + threadIdx.x;
+        if (i < n) v[j] = xt[i];
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + j * blockDim.x + threadIdx.x;
+        if (i < n) smem_x4[i] = v[j];
+      }
+    }
   }
   if (x16) {
     // the blocks of a token tile also write its activations as f16 times a
@@ -41,8 +163,12 @@ __global__ void __launch_bounds__(128) k_router(const uint16_t* __restrict__ x, 
     __syncthreads();
     const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem_x4);
     for (int t = warp; t < nt; t += blockDim.x >> 5) {
-      float m = 0.f;
-      for (int i = lane; i < H; i += 32) m = fmaxf(m, fabsf(bf16_bits_to_f32(xs[t * H + i])));
+      float mx[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+      for (int i = lane; i < H; i += 128)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (i + 32 * u < H) mx[u] = fmaxf(mx[u], fabsf(bf16_bits_to_f32(xs[t * H + i + 32 * u])));
+      float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
       if (lane == 0) s_scale[t] = pow2_scale_for(m);
@@ -57,17 +183,7 @@ __global__ void __launch_bounds__(128) k_router(const uint16_t* __restrict__ x, 
       x16[size_t(t0 + t) * H + c] = __float2half_rn(bf16_bits_to_f32(xs[t * H + c]) * s_scale[t]);
     }
   }
-  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
-  const bool live = row < rows;
-  const uint16_t* wrow = live ? (row < E ? w_router + size_t(row) * H : w_gate) : nullptr;
-  uint4 wv[kRouterMaxChunksPerLane];
-#pragma unroll
-  for (int i = 0; i < kRouterMaxChunksPerLane; ++i) {
-    const int c = lane + 32 * i;
-    wv[i] = (live && c < chunks) ? reinterpret_cast<const uint4*>(wrow)[c] : make_uint4(0, 0, 0, 0);
-  }
   __syncthreads();
-  if (!live) return;
   float acc[kRouterTokTile];
 #pragma unroll
   for (int t = 0; t < kRouterTokTile; ++t) acc[t] = 0.f;
@@ -95,7 +211,7 @@ __global__ void __launch_bounds__(128) k_router(const uint16_t* __restrict__ x, 
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
   }
-  if (lane < nt) {
+  if (live && lane < nt) {
     float v = acc[0];
 #pragma unroll
     for (int t = 1; t < kRouterTokTile; ++t)
@@ -105,11 +221,32 @@ __global__ void __launch_bounds__(128) k_router(const uint16_t* __restrict__ x, 
     else
       gate_logit[t0 + lane] = v;
   }
+  if (!tick) return;
+  __shared__ int s_ticket;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_ticket = atomicAdd(tick + blockIdx.y, 1);
+  __syncthreads();
+  if (s_ticket != int(gridDim.x) - 1) return;
+  __threadfence();
+  const int kper = (E + 31) / 32;
+  for (int t = warp; t < nt; t += blockDim.x >> 5) {
+    const float* lr = logits + size_t(t0 + t) * E;
+    int32_t* oi = ids + size_t(t0 + t) * k;
+    float* ow = wts + size_t(t0 + t) * k;
+    if (kper <= 1) topk_token<1, true>(lr, E, k, lane, oi, ow, err);
+    else if (kper <= 2) topk_token<2, true>(lr, E, k, lane, oi, ow, err);
+    else if (kper <= 4) topk_token<4, true>(lr, E, k, lane, oi, ow, err);
+    else if (kper <= 8) topk_token<8, true>(lr, E, k, lane, oi, ow, err);
+    else if (kper <= 16) topk_token<16, true>(lr, E, k, lane, oi, ow, err);
+    else topk_token<32, true>(lr, E, k, lane, oi, ow, err);
+  }
+  if (threadIdx.x == 0) tick[blockIdx.y] = 0;  // ready for the next call
 }
 
 int launch_router(const uint16_t* x, const uint16_t* w_router, const float* bias, const uint16_t* w_gate,
                   float* logits, float* gate_logit, int T, int H, int E, cudaStream_t s, __half* x16,
-                  float* xscale) {
+                  float* xscale, int k, int32_t* ids, float* wts, int32_t* err, int* tick) {
   if (T <= 0) return MOE_OK;
   if (H / 8 > 32 * kRouterMaxChunksPerLane) return MOE_EINVAL;
   // rows 0..E-1 are router rows, row E the gate vector; without a router only the gate row runs
@@ -117,29 +254,18 @@ int launch_router(const uint16_t* x, const uint16_t* w_router, const float* bias
   const int rows = E_eff + (w_gate ? 1 : 0);
   if (rows == 0) return MOE_OK;
   const int tok_tiles = (T + kRouterTokTile - 1) / kRouterTokTile;
+  // top-k runs in the router only with a router, E <= 1024 and somewhere to write it
+  if (!w_router || !ids || E > 1024 || k < 1 || k > 32) tick = nullptr;
   const size_t smem = size_t(kRouterTokTile) * H * 2;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(k_router, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
     return MOE_ECUDA;
   dim3 grid((rows + 3) / 4, tok_tiles);
   if (launch_pdl(k_router, grid, dim3(128), smem, s, x, w_router ? w_router : w_gate, bias, w_gate, logits,
-                 gate_logit, T, H, E_eff, rows, x16, xscale) != cudaSuccess)
+                 gate_logit, T, H, E_eff, rows, x16, xscale, k, ids, wts, err, tick) != cudaSuccess)
     return MOE_ECUDA;
   MOE_LAUNCH_CHECK();
   return MOE_OK;
-}
-
-// ------------------------------------------------------------------- top-k
-// One warp per token; lane j holds logits j, j+32, ... (KPER per lane).
-// Each lane keeps its best untaken entry; a round takes the warp-wide best by
-// (value desc, id asc) with a shuffle reduction and only the owning lane
-// rescans.  Lane r keeps the r-th selection.  NaN logits record MOE_ENAN and
-// rank as -inf.
-__device__ __forceinline__ bool better(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
-// fp32 -> uint32 whose unsigned order is the float order (-inf lowest).
-__device__ __forceinline__ unsigned ordered_key(float f) {
-  const unsigned b = __float_as_uint(f);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
 template <int KPER>
@@ -149,55 +275,7 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
   pdl_wait();
   const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (tok >= T) return;
-  const float* lr = logits + size_t(tok) * E;
-  float v[KPER];
-  uint32_t avail = 0;
-  bool nan_seen = false;
-#pragma unroll
-  for (int j = 0; j < KPER; ++j) {
-    const int e = lane + 32 * j;
-    float x = -INFINITY;
-    if (e < E) {
-      x = lr[e];
-      if (x != x) { nan_seen = true; x = -INFINITY; }
-      avail |= 1u << j;
-    }
-    v[j] = x;
-  }
-  if (__any_sync(0xffffffffu, nan_seen) && lane == 0) set_error(err, MOE_ENAN);
-  auto local_best = [&](float& bv, int& bi, int& bj) {
-    bv = -INFINITY;
-    bi = 0x7fffffff;
-    bj = -1;
-#pragma unroll
-    for (int j = 0; j < KPER; ++j)
-      if (((avail >> j) & 1u) && better(v[j], lane + 32 * j, bv, bi)) { bv = v[j]; bi = lane + 32 * j; bj = j; }
-  };
-  float bv;
-  int bi, bj;
-  local_best(bv, bi, bj);
-  int my_id = 0;
-  float my_p = 0.f, m = 0.f, den = 0.f;
-  for (int r = 0; r < k; ++r) {
-    // warp-wide best: the largest value (two warp reductions on order-preserving
-    // integer keys), then the lowest id among the lanes that hold it
-    const unsigned key = ordered_key(bv);
-    const unsigned kmax = __reduce_max_sync(0xffffffffu, key);
-    const int wi = int(__reduce_min_sync(0xffffffffu, key == kmax ? unsigned(bi) : 0x7fffffffu));
-    const float wv = __shfl_sync(0xffffffffu, bv, wi & 31);
-    if (r == 0) m = wv;
-    const float p = expf(wv - m);
-    den += p;
-    if (lane == r) { my_id = wi; my_p = p; }
-    if (bi == wi && bj >= 0) {
-      avail &= ~(1u << bj);
-      local_best(bv, bi, bj);
-    }
-  }
-  if (lane < k) {
-    ids[size_t(tok) * k + lane] = my_id;
-    w[size_t(tok) * k + lane] = my_p / den;
-  }
+  topk_token<KPER, false>(logits + size_t(tok) * E, E, k, lane, ids + size_t(tok) * k, w + size_t(tok) * k, err);
 }
 
 int launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* err, cudaStream_t s) {
