@@ -274,7 +274,7 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   const size_t o_yacc = cv.take<float>(size_t(maxT) * s.H);
   const size_t o_cnt = cv.take<int>(split_blocks);
   const size_t o_o = cv.take<float>((Tk + maxT) * s.H);
-  const size_t o_tick = cv.take<int>(size_t(maxT) / 8 + 2);
+  const size_t o_gscr = cv.take<int32_t>((size_t(maxT) / 256 + 2) * s.E);
   const size_t o_err = cv.take<int32_t>(1);
   uint8_t* base = nullptr;
   if (cudaMalloc(&base, cv.off) != cudaSuccess) {
@@ -305,7 +305,7 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   w->cnt = reinterpret_cast<int*>(base + o_cnt);
   w->split_blocks = split_blocks;
   w->o = reinterpret_cast<float*>(base + o_o);
-  w->tick = reinterpret_cast<int*>(base + o_tick);
+  w->grp_scratch = reinterpret_cast<int32_t*>(base + o_gscr);
   w->error = reinterpret_cast<int32_t*>(base + o_err);
   if (cudaMemset(base, 0, cv.off) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();

@@ -242,7 +242,7 @@ struct moe_ws {
   int* cnt;             // [split_blocks] arrival counters, zero between calls
   size_t split_blocks;
   float* o;             // [maxT*k + maxT, H] routed outputs by position, then shared outputs
-  int* tick;            // [maxT/8 + 2] arrival counters of last-CTA fusions, zero between calls
+  int32_t* grp_scratch; // [(maxT/256 + 1) * E + E] grouping of long windows: per-tile counts, offsets
   int32_t* error;       // [1]
   // optional per-kernel timing of the most recent call
   int prof_on, prof_n;

@@ -4,12 +4,9 @@
 
 namespace moe {
 
-// With tick (zeroed counters, one per 8-token tile), the last CTA of each tile also runs top-k
-// into ids/wts; otherwise top-k is a separate launch_topk.
 int launch_router(const uint16_t* x, const uint16_t* w_router, const float* bias, const uint16_t* w_gate,
                   float* logits, float* gate_logit, int T, int H, int E, cudaStream_t s, __half* x16 = nullptr,
-                  float* xscale = nullptr, int k = 0, int32_t* ids = nullptr, float* wts = nullptr,
-                  int32_t* err = nullptr, int* tick = nullptr);
+                  float* xscale = nullptr);
 int launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* err, cudaStream_t s);
 
 int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws, cudaStream_t s);

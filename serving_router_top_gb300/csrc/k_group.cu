@@ -44,6 +44,36 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int& total
   return before + x - v;
 }
 
+// Group g is expert e with entries from off on: its slot from the residency
+// table, else the staging table, else MISSING; counts resident/staged/missing.
+__device__ __forceinline__ void resolve_group(int g, int e, int off, int layer, int E, const int32_t* resid,
+                                              const int32_t* stage, const uint8_t* slots, const uint8_t* staging,
+                                              size_t blob_bytes, int nslots, int nstaging, int32_t* grp_expert,
+                                              int32_t* grp_off, int32_t* grp_slot, int32_t* grp_src,
+                                              const uint8_t** grp_blob, int32_t* err, int* s_hit, int* s_stg,
+                                              int* s_miss) {
+  grp_expert[g] = e;
+  grp_off[g] = off;
+  const int flat = layer * E + e;
+  int slot = resid[flat];
+  int src = MOE_SRC_MISSING;
+  const uint8_t* blob = nullptr;
+  if (slot >= 0) {
+    if (slot < nslots) { src = MOE_SRC_RESIDENT; blob = slots + size_t(slot) * blob_bytes; }
+    else { set_error(err, MOE_ERANGE); slot = -1; }
+  }
+  if (src == MOE_SRC_MISSING) {
+    int st = stage ? stage[flat] : -1;
+    if (st >= 0 && st < nstaging) { slot = st; src = MOE_SRC_STAGED; blob = staging + size_t(st) * blob_bytes; }
+    else if (st >= nstaging) set_error(err, MOE_ERANGE);
+  }
+  if (src == MOE_SRC_MISSING) { slot = -1; set_error(err, MOE_EMISSING); }
+  grp_slot[g] = slot;
+  grp_src[g] = src;
+  grp_blob[g] = blob;
+  atomicAdd(src == MOE_SRC_RESIDENT ? s_hit : src == MOE_SRC_STAGED ? s_stg : s_miss, 1);
+}
+
 __global__ void __launch_bounds__(1024) k_group(const int32_t* __restrict__ ids, int T, int k, int E, int layer,
                                                 const int32_t* __restrict__ resid, const int32_t* __restrict__ stage,
                                                 const uint8_t* slots, const uint8_t* staging, size_t blob_bytes,
@@ -89,29 +119,9 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t* __restrict__ ids,
   const int ex_c = block_excl_scan(c, warp_sums, total_entries);
   const int ex_g = block_excl_scan(c > 0 ? 1 : 0, warp_sums, total_groups);
   if (e < E) off[e] = ex_c;
-  if (e < E && c > 0) {
-    const int g = ex_g;
-    grp_expert[g] = e;
-    grp_off[g] = ex_c;
-    const int flat = layer * E + e;
-    int slot = resid[flat];
-    int src = MOE_SRC_MISSING;
-    const uint8_t* blob = nullptr;
-    if (slot >= 0) {
-      if (slot < nslots) { src = MOE_SRC_RESIDENT; blob = slots + size_t(slot) * blob_bytes; }
-      else { set_error(err, MOE_ERANGE); slot = -1; }
-    }
-    if (src == MOE_SRC_MISSING) {
-      int st = stage ? stage[flat] : -1;
-      if (st >= 0 && st < nstaging) { slot = st; src = MOE_SRC_STAGED; blob = staging + size_t(st) * blob_bytes; }
-      else if (st >= nstaging) set_error(err, MOE_ERANGE);
-    }
-    if (src == MOE_SRC_MISSING) { slot = -1; set_error(err, MOE_EMISSING); }
-    grp_slot[g] = slot;
-    grp_src[g] = src;
-    grp_blob[g] = blob;
-    atomicAdd(src == MOE_SRC_RESIDENT ? &s_hit : src == MOE_SRC_STAGED ? &s_stg : &s_miss, 1);
-  }
+  if (e < E && c > 0)
+    resolve_group(ex_g, e, ex_c, layer, E, resid, stage, slots, staging, blob_bytes, nslots, nstaging, grp_expert,
+                  grp_off, grp_slot, grp_src, grp_blob, err, &s_hit, &s_stg, &s_miss);
   __syncthreads();
   if (threadIdx.x == 0) {
     *num_groups = total_groups;
@@ -159,8 +169,153 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t* __restrict__ ids,
   }
 }
 
+// ------------------------------------------------------------------
+// Long windows (prefill chunks): the same grouping in three passes over tiles
+// of kGrpTok tokens.  (1) each CTA counts its tile's entries per expert; (2)
+// one CTA turns the counts into, per expert, the entries before each tile and
+// the group offsets, and resolves the groups as above; (3) each CTA places its
+// tile's entries: group offset + entries of earlier tiles + the popcount of
+// the tile's token bitmap below the token (ascending tokens, as above).
+constexpr int kGrpTok = 256;
+
+__global__ void __launch_bounds__(256) k_group_count(const int32_t* __restrict__ ids, int T, int k, int E,
+                                                     int32_t* __restrict__ cnt, int32_t* err) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ int sc[];  // [E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sc[e] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * kGrpTok, t1 = min(T, t0 + kGrpTok);
+  bool bad = false;
+  for (int i = t0 * k + threadIdx.x; i < t1 * k; i += blockDim.x) {
+    const int e = ids[i];
+    if (e < 0 || e >= E) { bad = true; continue; }
+    atomicAdd(&sc[e], 1);
+  }
+  if (bad) set_error(err, MOE_ERANGE);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[size_t(blockIdx.x) * E + e] = sc[e];
+}
+
+__global__ void __launch_bounds__(1024) k_group_scan(int ntile, int T, int k, int E, int layer,
+                                                     const int32_t* __restrict__ resid, const int32_t* __restrict__ stage,
+                                                     const uint8_t* slots, const uint8_t* staging, size_t blob_bytes,
+                                                     int nslots, int nstaging, int32_t* __restrict__ cnt,
+                                                     int32_t* __restrict__ eoff, int32_t* __restrict__ num_groups,
+                                                     int32_t* __restrict__ grp_expert, int32_t* __restrict__ grp_off,
+                                                     int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
+                                                     const uint8_t** __restrict__ grp_blob, unsigned long long* stats,
+                                                     int32_t* err, float* __restrict__ hmax, int maxTk) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int warp_sums[32];
+  __shared__ int s_hit, s_stg, s_miss;
+  if (threadIdx.x == 0) { s_hit = 0; s_stg = 0; s_miss = 0; }
+  const int n = T * k;
+  if (hmax) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) hmax[i] = 0.f;
+    for (int i = threadIdx.x; i < T; i += blockDim.x) hmax[maxTk + i] = 0.f;
+  }
+  // per expert: entries before each tile (in place) and the total, loads eight tiles at a time
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < E) {
+    for (int c0 = 0; c0 < ntile; c0 += 8) {
+      int v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = c0 + j < ntile ? cnt[size_t(c0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + j < ntile) {
+          cnt[size_t(c0 + j) * E + e] = total;
+          total += v[j];
+        }
+    }
+  }
+  __syncthreads();
+  int total_entries, total_groups;
+  const int ex_c = block_excl_scan(total, warp_sums, total_entries);
+  const int ex_g = block_excl_scan(total > 0 ? 1 : 0, warp_sums, total_groups);
+  if (e < E) eoff[e] = ex_c;
+  if (e < E && total > 0)
+    resolve_group(ex_g, e, ex_c, layer, E, resid, stage, slots, staging, blob_bytes, nslots, nstaging, grp_expert,
+                  grp_off, grp_slot, grp_src, grp_blob, err, &s_hit, &s_stg, &s_miss);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    *num_groups = total_groups;
+    grp_off[total_groups] = total_entries;
+    if (stats) {
+      unsigned long long* st = stats + size_t(layer) * 4;
+      atomicAdd(st + 0, (unsigned long long)total_groups);
+      atomicAdd(st + 1, (unsigned long long)s_hit);
+      atomicAdd(st + 2, (unsigned long long)s_stg);
+      atomicAdd(st + 3, (unsigned long long)s_miss);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) k_group_place(const int32_t* __restrict__ ids, int T, int k, int E,
+                                                     const int32_t* __restrict__ cnt, const int32_t* __restrict__ eoff,
+                                                     int32_t* __restrict__ ent_tok, int32_t* __restrict__ ent_pos,
+                                                     int32_t* err) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int W = kGrpTok / 32;
+  extern __shared__ uint32_t bits[];  // [E][W] tokens of this tile that chose each expert
+  for (int i = threadIdx.x; i < E * W; i += blockDim.x) bits[i] = 0u;
+  __syncthreads();
+  const int t0 = blockIdx.x * kGrpTok, t1 = min(T, t0 + kGrpTok);
+  for (int i = t0 * k + threadIdx.x; i < t1 * k; i += blockDim.x) {
+    const int ex = ids[i];
+    if (ex < 0 || ex >= E) continue;
+    const int lt = i / k - t0;
+    const uint32_t old = atomicOr(&bits[ex * W + (lt >> 5)], 1u << (lt & 31));
+    if (old & (1u << (lt & 31))) set_error(err, MOE_ERANGE);  // an expert chosen twice by one token
+  }
+  __syncthreads();
+  const int32_t* before = cnt + size_t(blockIdx.x) * E;
+  for (int i = t0 * k + threadIdx.x; i < t1 * k; i += blockDim.x) {
+    const int ex = ids[i];
+    if (ex < 0 || ex >= E) continue;
+    const int t = i / k, lt = t - t0, wd = lt >> 5;
+    const uint32_t* row = bits + ex * W;
+    int rank = __popc(row[wd] & ((1u << (lt & 31)) - 1u));
+#pragma unroll
+    for (int w = 0; w < W; ++w)
+      if (w < wd) rank += __popc(row[w]);
+    const int pos = eoff[ex] + before[ex] + rank;
+    ent_tok[pos] = t;
+    ent_pos[pos] = i;
+  }
+}
+
 int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws, cudaStream_t s) {
   if (E > 1024 || E <= 0) return MOE_EINVAL;
+  if (T * k > 4096 && ws->grp_scratch) {
+    const int ntile = (T + kGrpTok - 1) / kGrpTok;
+    int32_t* cnt = ws->grp_scratch;              // [ntile][E]
+    int32_t* eoff = cnt + size_t(ntile) * E;     // [E]
+    const size_t smem3 = size_t(E) * (kGrpTok / 32) * 4;
+    static bool attr3 = false;
+    if (!attr3) {
+      if (cudaFuncSetAttribute(k_group_place, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024) != cudaSuccess)
+        return MOE_ECUDA;
+      attr3 = true;
+    }
+    if (launch_pdl(k_group_count, dim3(ntile), dim3(256), size_t(E) * 4, s, ids, T, k, E, cnt, ws->error) !=
+        cudaSuccess)
+      return MOE_ECUDA;
+    if (launch_pdl(k_group_scan, dim3(1), dim3(1024), 0, s, ntile, T, k, E, layer, c ? c->resid : nullptr,
+                   c ? c->stage : nullptr, c ? c->slots : nullptr, c ? c->staging : nullptr, c ? c->blob_bytes : 0,
+                   c ? c->nslots : 0, c ? c->nstaging : 0, cnt, eoff, ws->num_groups, ws->grp_expert, ws->grp_off,
+                   ws->grp_slot, ws->grp_src, ws->grp_blob, c ? c->stats : nullptr, ws->error, ws->hmax,
+                   ws->maxT * ws->s.k) != cudaSuccess)
+      return MOE_ECUDA;
+    if (launch_pdl(k_group_place, dim3(ntile), dim3(256), smem3, s, ids, T, k, E, cnt, eoff, ws->ent_tok,
+                   ws->ent_pos, ws->error) != cudaSuccess)
+      return MOE_ECUDA;
+    return MOE_OK;
+  }
   // bitmap words per expert: as many as fit 64 KB, at most 32 (1024 tokens per chunk)
   int W = 16384 / E;
   if (W > 32) W = 32;

@@ -32,9 +32,8 @@ __device__ __forceinline__ float float_of_key(unsigned k) {
 // each round then takes the warp-wide best head -- the largest key, ties to
 // the lowest id -- and the winning lane shifts its list.  Lane r writes the
 // r-th selection; weights are exp(l - l_0) / sum over the chosen.  NaN logits
-// record MOE_ENAN and rank as -inf.  LDCG: read the logits through L2 (they
-// were written by other CTAs of the same kernel).
-template <int KPER, bool LDCG>
+// record MOE_ENAN and rank as -inf.
+template <int KPER>
 __device__ __forceinline__ void topk_token(const float* lr, int E, int k, int lane, int32_t* ids, float* w,
                                            int32_t* err) {
   unsigned u[KPER];
@@ -45,7 +44,7 @@ __device__ __forceinline__ void topk_token(const float* lr, int E, int k, int la
     const int e = lane + 32 * j;
     unsigned key = 0u;
     if (e < E) {
-      float x = LDCG ? __ldcg(lr + e) : lr[e];
+      float x = lr[e];
       if (x != x) { nan_seen = true; x = -INFINITY; }
       key = ordered_key(x);
     }
@@ -110,8 +109,6 @@ __device__ __forceinline__ void topk_token(const float* lr, int E, int k, int la
 // of the weight row first -- before waiting for the previous kernel, since no
 // kernel writes the weights -- then stages the tile's bf16 activations in
 // shared memory and accumulates in fp32 (bf16 x bf16 products are exact).
-// With tick, the last CTA of each token tile to finish (an arrival counter,
-// no waiting) also runs top-k for the tile's tokens.
 constexpr int kRouterTokTile = 8;
 constexpr int kRouterMaxChunksPerLane = 16;  // H <= 4096
 
@@ -119,8 +116,7 @@ __global__ void __launch_bounds__(128) k_router(const uint16_t* __restrict__ x, 
                                                 const float* __restrict__ bias, const uint16_t* __restrict__ w_gate,
                                                 float* __restrict__ logits, float* __restrict__ gate_logit, int T,
                                                 int H, int E, int rows, __half* __restrict__ x16,
-                                                float* __restrict__ xscale, int k, int32_t* __restrict__ ids,
-                                                float* __restrict__ wts, int32_t* err, int* tick) {
+                                                float* __restrict__ xscale) {
   pdl_trigger();
   extern __shared__ uint4 smem_x4[];  // [kRouterTokTile][H/8]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -221,32 +217,11 @@ __global__ void __launch_bounds__(128) k_router(const uint16_t* __restrict__ x, 
     else
       gate_logit[t0 + lane] = v;
   }
-  if (!tick) return;
-  __shared__ int s_ticket;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_ticket = atomicAdd(tick + blockIdx.y, 1);
-  __syncthreads();
-  if (s_ticket != int(gridDim.x) - 1) return;
-  __threadfence();
-  const int kper = (E + 31) / 32;
-  for (int t = warp; t < nt; t += blockDim.x >> 5) {
-    const float* lr = logits + size_t(t0 + t) * E;
-    int32_t* oi = ids + size_t(t0 + t) * k;
-    float* ow = wts + size_t(t0 + t) * k;
-    if (kper <= 1) topk_token<1, true>(lr, E, k, lane, oi, ow, err);
-    else if (kper <= 2) topk_token<2, true>(lr, E, k, lane, oi, ow, err);
-    else if (kper <= 4) topk_token<4, true>(lr, E, k, lane, oi, ow, err);
-    else if (kper <= 8) topk_token<8, true>(lr, E, k, lane, oi, ow, err);
-    else if (kper <= 16) topk_token<16, true>(lr, E, k, lane, oi, ow, err);
-    else topk_token<32, true>(lr, E, k, lane, oi, ow, err);
-  }
-  if (threadIdx.x == 0) tick[blockIdx.y] = 0;  // ready for the next call
 }
 
 int launch_router(const uint16_t* x, const uint16_t* w_router, const float* bias, const uint16_t* w_gate,
                   float* logits, float* gate_logit, int T, int H, int E, cudaStream_t s, __half* x16,
-                  float* xscale, int k, int32_t* ids, float* wts, int32_t* err, int* tick) {
+                  float* xscale) {
   if (T <= 0) return MOE_OK;
   if (H / 8 > 32 * kRouterMaxChunksPerLane) return MOE_EINVAL;
   // rows 0..E-1 are router rows, row E the gate vector; without a router only the gate row runs
@@ -254,15 +229,13 @@ int launch_router(const uint16_t* x, const uint16_t* w_router, const float* bias
   const int rows = E_eff + (w_gate ? 1 : 0);
   if (rows == 0) return MOE_OK;
   const int tok_tiles = (T + kRouterTokTile - 1) / kRouterTokTile;
-  // top-k runs in the router only with a router, E <= 1024 and somewhere to write it
-  if (!w_router || !ids || E > 1024 || k < 1 || k > 32) tick = nullptr;
   const size_t smem = size_t(kRouterTokTile) * H * 2;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(k_router, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
     return MOE_ECUDA;
   dim3 grid((rows + 3) / 4, tok_tiles);
   if (launch_pdl(k_router, grid, dim3(128), smem, s, x, w_router ? w_router : w_gate, bias, w_gate, logits,
-                 gate_logit, T, H, E_eff, rows, x16, xscale, k, ids, wts, err, tick) != cudaSuccess)
+                 gate_logit, T, H, E_eff, rows, x16, xscale) != cudaSuccess)
     return MOE_ECUDA;
   MOE_LAUNCH_CHECK();
   return MOE_OK;
@@ -275,7 +248,7 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
   pdl_wait();
   const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (tok >= T) return;
-  topk_token<KPER, false>(logits + size_t(tok) * E, E, k, lane, ids + size_t(tok) * k, w + size_t(tok) * k, err);
+  topk_token<KPER>(logits + size_t(tok) * E, E, k, lane, ids + size_t(tok) * k, w + size_t(tok) * k, err);
 }
 
 int launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* err, cudaStream_t s) {
