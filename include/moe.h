@@ -265,6 +265,21 @@ typedef struct {
  *   becomes fl32(heat * decay).  Requires L*E <= 32768 and max_swaps <= 4096. */
 int cache_plan_swaps(moe_cache* c, const moe_policy_cfg* p, moe_swap* plan_dev, int32_t* n_dev, moe_stream_t stream);
 
+/* Residual stream and RMS normalisation between the layers of a decode stack.
+ * The pages give the model as MoE layers in sequence but have no counterpart
+ * to this step: it is the wrapper of the 48-layer decode workload,
+ * x_{l+1} = x_l + MoE_l(RMSNorm(x_l)), with unit RMSNorm weight.
+ *   x_res   float [T, H] device, the residual stream, updated in place:
+ *           x_res += y_prev when y_prev != NULL (bf16 [T, H], the previous
+ *           layer's output);
+ *   xn_out  bf16 [T, H] device: bf16(x_res / sqrt(mean(x_res^2) + eps)),
+ *           the next layer's input.
+ * fp32 arithmetic (sum of squares in fp32, correctly rounded sqrt and
+ * division).  H a multiple of 4 and at most 4096, eps > 0, x_res 16-byte and
+ * the bf16 arrays 8-byte aligned, else MOE_EINVAL. */
+int moe_residual_rmsnorm(float* x_res, const uint16_t* y_prev, uint16_t* xn_out, int T, int H, float eps,
+                         moe_stream_t stream);
+
 /* cache_plan_swaps on caller-owned tables, allocating nothing.  The pages
  * have no counterpart to this call: it exists for callers that cannot
  * allocate device memory where they plan -- a serving loop whose memory is

@@ -44,14 +44,15 @@ class ModelState:
 
     ``resident``/``staged``: bool [L, E] masks (default: the workload's
     resident fraction as a seeded subset, everything else staged when
-    ``stage_rest``).  ``backing_on_device``: keep the full expert pool in HBM
+    ``stage_rest``; ``stage_all`` stages every expert, so that experts the
+    cache policy swaps out stay reachable through the staging table).  ``backing_on_device``: keep the full expert pool in HBM
     (else page-locked host memory that kernels read directly).
     """
 
     def __init__(self, w: I.Workload, layers: Optional[int] = None, resident: Optional[np.ndarray] = None,
                  staged: Optional[np.ndarray] = None, stage_rest: bool = True, nslots: Optional[int] = None,
                  nstaging: Optional[int] = None, backing_on_device: bool = True, maxT: Optional[int] = None,
-                 device: str = "cuda"):
+                 device: str = "cuda", stage_all: bool = False):
         self.w = w
         s = w.shape
         self.L = L = w.layers if layers is None else layers
@@ -59,10 +60,14 @@ class ModelState:
         self.blob_bytes = moe.moe_blob_bytes(s.H, s.I)
         if resident is None:
             resident = np.stack([I.resident_mask(w.seed, l, s.E, w.resident_frac) for l in range(L)])
-        if staged is None:
-            staged = ~resident if stage_rest else np.zeros_like(resident)
         self.resident = np.asarray(resident, dtype=bool).reshape(L, s.E)
-        self.staged = np.asarray(staged, dtype=bool).reshape(L, s.E) & ~self.resident
+        if stage_all:  # every expert also in a staging slot: an expert swapped out stays reachable
+            staged = np.ones_like(self.resident)
+        elif staged is None:
+            staged = ~self.resident if stage_rest else np.zeros_like(self.resident)
+        self.staged = np.asarray(staged, dtype=bool).reshape(L, s.E)
+        if not stage_all:
+            self.staged &= ~self.resident
         self.backing = self._build_backing(backing_on_device, device)
         nslots = int(self.resident.sum()) if nslots is None else nslots
         nstaging = int(self.staged.sum()) if nstaging is None else nstaging

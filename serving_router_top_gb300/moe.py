@@ -26,7 +26,7 @@ EXPORTED = (
     "moe_cache_fill", "moe_cache_get_view", "moe_get_stats", "moe_ws_create", "moe_ws_destroy", "moe_ws_get_view",
     "moe_sync_status", "moe_strerror", "moe_route", "moe_group", "moe_layer_forward", "cache_heat_update",
     "cache_plan_swaps", "moe_cache_apply_swaps", "moe_ws_set_profiling", "moe_ws_kernel_times",
-    "cache_plan_swaps_noalloc",
+    "cache_plan_swaps_noalloc", "moe_residual_rmsnorm",
 )
 
 
@@ -100,6 +100,7 @@ def load() -> C.CDLL:
         "cache_heat_update": (I, [P, P, I, I, I, P, P]),
         "cache_plan_swaps": (I, [P, C.POINTER(moe_policy_cfg), P, P, P]),
         "cache_plan_swaps_noalloc": (I, [P, P, I, I, C.POINTER(moe_policy_cfg), P, P, P]),
+        "moe_residual_rmsnorm": (I, [P, P, P, I, I, F, P]),
         "moe_cache_apply_swaps": (I, [P, P, P, P, P]),
         "moe_ws_set_profiling": (I, [P, I]),
         "moe_ws_kernel_times": (I, [P, I, P, P, C.POINTER(C.c_int)]),
@@ -318,6 +319,12 @@ def cache_plan_swaps(cache: Cache, threshold: float, max_swaps: int, decay: floa
     cfg = moe_policy_cfg(threshold, max_swaps, decay)
     _check(load().cache_plan_swaps(cache.handle, C.byref(cfg), _ptr(plan_dev), _ptr(n_dev), _stream(stream)),
            "cache_plan_swaps")
+
+
+def moe_residual_rmsnorm(x_res, y_prev, xn_out, T: int, H: int, eps: float = 1e-6, stream=None) -> None:
+    """x_res (fp32 [T,H]) += y_prev (bf16 bits, or None); xn_out (bf16 bits) = RMSNorm(x_res)."""
+    _check(load().moe_residual_rmsnorm(_ptr(x_res), _ptr(y_prev), _ptr(xn_out), T, H, eps, _stream(stream)),
+           "moe_residual_rmsnorm")
 
 
 # Capacity of the static scratch behind cache_plan_swaps_noalloc.

@@ -138,3 +138,22 @@ def test_group_rejects_out_of_range_ids():
     ids = torch.tensor([[0, 1], [2, 9], [3, 4], [5, 6]], dtype=torch.int32, device="cuda")
     moe.moe_group(ids, 4, 2, 8, 0, st.cache, st.ws)
     assert moe.moe_sync_status(st.ws) == moe.MOE_ERANGE
+
+
+def test_large_expert_layer_decode_batch64_sampled():
+    """One layer of the 4096-hidden, 256-expert top-6 model (I = I_shared = 2048) decoding a batch of 64
+    tokens; sampled tokens against the oracle on the GPU's own logits."""
+    from serving_router_top_gb300.model import ModelState
+    w = I.WORKLOADS["large_h4096_e256_k6"]
+    st = ModelState(w, layers=1, maxT=64)
+    T = 64
+    x_bits = I.activations(w.seed, 7, T, st.H)
+    y = run_layer(st, x_bits, T, bf16_out=False)
+    logits_t, ids_t, w_t = st.ws.routing(T)
+    logits = logits_t.cpu().numpy()
+    ids = ids_t.cpu().numpy()
+    ref_ids, ref_w = olayer.top_k(logits, st.k)
+    assert np.array_equal(ids, ref_ids)
+    toks = np.random.default_rng(11).choice(T, 8, replace=False)
+    ref = U.oracle_layer_from_state(st, 0, x_bits[toks], logits[toks])
+    U.assert_close_layer(y[toks], ref.y, what="sampled y")
