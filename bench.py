@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true", help="skip the secondary prefill-chunk measurement")
+    p.add_argument("--layers", type=int, default=8,
+                   help="layers of the workload's shape stepped through in turn (1 for small profiling runs)")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget for cpu_baseline")
     return p.parse_args()
 
@@ -233,7 +235,7 @@ def prefill_flops(st, T: int) -> dict:
             "down_gemm": 2 * (T * k * H * I_ + T * H * Is)}
 
 
-KERNEL_SOURCES = {"gateup_decode": "k_expert.cu", "down_decode": "k_expert.cu", "router": "k_route.cu",
+KERNEL_SOURCES = {"gateup_decode": "k_gemv.cu", "down_decode": "k_gemv.cu", "router": "k_route.cu",
                   "gateup_gemm": "k_prefill.cu", "down_gemm": "k_prefill.cu"}
 
 
@@ -373,7 +375,7 @@ def run_ours(args, w):
     # NL layers of the workload's shape, stepped through in turn as a model would:
     # their weights (about 40 MB each) exceed the L2, so no step finds its
     # weights cached and no flush is needed between timed steps.
-    NL = 8
+    NL = max(1, args.layers)
     st = ModelState(w, layers=NL)
     P = 8 * NL  # distinct windows, resident in HBM before the timed region
     xs_host = [torch.from_numpy(I.activations(w.seed, 10_000 * rank + i, T, s.H).view(np.int16)).pin_memory()
@@ -499,9 +501,10 @@ def run_ours(args, w):
         "dtype": "e2m1 weights; f16 x f16 -> f32 math", "data": "synthetic",
         "config": {"workload": w.name, "tokens_per_window": T, "hidden": s.H, "experts": s.E, "top_k": s.k,
                    "intermediate": s.I, "shared_intermediate": s.I_shared, "zipf_s": w.zipf_s,
-                   "resident_frac": w.resident_frac, "layers_stepped": 8,
-                   "l2": "not flushed: the timed steps go through 8 layers of this shape in turn, whose weights "
-                         "(about 40 MB each, 320 MB in all) exceed the 129 MB L2",
+                   "resident_frac": w.resident_frac, "layers_stepped": NL,
+                   "l2": f"not flushed: the timed steps go through {NL} layers of this shape in turn, whose weights "
+                         f"(about 40 MB each, {40 * NL} MB in all) exceed the 129 MB L2" if NL >= 4 else
+                         f"{NL} layer(s) only: weights may stay in L2 (profiling run, not a bench number)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": f"{src} hbm_gbs",

@@ -263,6 +263,7 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   const size_t o_xs = cv.take<float>(maxT);
   const size_t o_h = cv.take<float>((Tk + maxT) * Imax);
   const size_t o_hmax = cv.take<float>(Tk + maxT);
+  const size_t o_xinv = cv.take<float>(Tk + maxT);
   // split-K scratch: K is sliced only for calls of at most 8 tokens, so at most
   // min(8k, E) groups of up to max(H, I)/16 row blocks, plus the shared expert's
   const int small_groups = (maxT < 8 ? maxT : 8) * s.k < s.E ? (maxT < 8 ? maxT : 8) * s.k : s.E;
@@ -270,6 +271,7 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   const size_t split_blocks = size_t(small_groups + 1) * rb_max;
   const size_t o_part = cv.take<float>(split_blocks * 8 * 32 * 8);
   const size_t o_toff = cv.take<int32_t>(size_t(s.E) + 2);
+  const size_t o_tgrp = cv.take<int32_t>(size_t(s.E) + Tk / 256 + 2);
   const size_t o_h16 = cv.take<__half>((Tk + maxT) * Imax);
   const size_t o_yacc = cv.take<float>(size_t(maxT) * s.H);
   const size_t o_cnt = cv.take<int>(split_blocks);
@@ -300,7 +302,10 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   w->hmax = reinterpret_cast<float*>(base + o_hmax);
   w->part = reinterpret_cast<float*>(base + o_part);
   w->tile_off = reinterpret_cast<int32_t*>(base + o_toff);
+  w->tile_grp = reinterpret_cast<int32_t*>(base + o_tgrp);
   w->h16 = reinterpret_cast<__half*>(base + o_h16);
+  w->xg = reinterpret_cast<__half*>(base + o_o);  // (Tk+maxT)*H 16-bit values fit in (Tk+maxT)*H floats
+  w->xinv = reinterpret_cast<float*>(base + o_xinv);
   w->yacc = reinterpret_cast<float*>(base + o_yacc);
   w->cnt = reinterpret_cast<int*>(base + o_cnt);
   w->split_blocks = split_blocks;

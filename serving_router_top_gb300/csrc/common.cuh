@@ -114,8 +114,11 @@ __device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float acc)
   return acc;
 }
 
-__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
-__device__ __forceinline__ float sigmoid_f32(float z) { return 1.0f / (1.0f + __expf(-z)); }
+// SiLU and the logistic function with the fast divide (within 2 ulp; a divisor
+// above 2^126 gives 0, which is also the limit there): the IEEE divide's
+// branchy sequence would serialise an epilogue that evaluates many at once.
+__device__ __forceinline__ float silu_f32(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+__device__ __forceinline__ float sigmoid_f32(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 // Power-of-two scale that brings max|v| into [2^12, 2^13): values become f16
 // without overflow, products with an E2M1 value (|.| <= 6) stay below 2^16.
@@ -236,7 +239,10 @@ struct moe_ws {
   float* h;             // [maxT*k + maxT, max(I, I_shared)] routed entries then shared rows
   float* hmax;          // [maxT*k + maxT] max|h| per row
   int32_t* tile_off;    // [E + 2] prefill: N tiles before each group
+  int32_t* tile_grp;    // [E + maxT*k/256 + 2] prefill: group of each N tile
   __half* h16;          // [maxT*k + maxT, max(I, I_shared)] prefill: h as f16 times a per-row power of two
+  __half* xg;           // [maxT*k + maxT, H] prefill: gate/up B rows, f16 x 2^p (in the o region, unused by prefill)
+  float* xinv;          // [maxT*k + maxT] prefill: 2^-p of each xg row
   float* yacc;          // [maxT, H] prefill: fp32 output accumulator
   float* part;          // split-K partial tiles: [split_blocks][8 slices][32 lanes][8]
   int* cnt;             // [split_blocks] arrival counters, zero between calls

@@ -4,7 +4,7 @@
 // a long prompt is processed in chunks and its tokens are grouped per expert,
 // so every expert runs once per chunk as a GEMM over its group.  Here:
 //   router:   [W_r; w_gate] (E+1 x H) . X^T (H x T)      -> logits, gate logit
-//   gate/up:  [Wg; Wu] (2I x H) . X_g^T (H x n)           -> h = SiLU(g) * u, max|h| per row
+//   gate/up:  [Wg; Wu] (2I x H) . X_g^T (H x n)           -> h = SiLU(g) * u
 //   down:     Wd (H x I) . h_g^T (I x n)                  -> y += w * o        (fp32)
 //
 // Operands.  A = 128 weight rows per tile.  Expert weights are dequantised by
@@ -12,25 +12,36 @@
 // every product has at most 6 significant bits and magnitude 2^-10 .. 2688 --
 // straight into shared memory in the 128-byte-swizzled K-major layout the
 // tensor core reads (router rows are bf16 already and are copied as they
-// are).  B = up to 256 token rows of the group, gathered with cp.async: the
-// bf16 activations themselves for the router and gate/up (both operands bf16,
-// so nothing is rounded), and for the down GEMM h as f16 times a per-row power
-// of two (both operands f16; h keeps 11 significant bits -- bf16 h, with 8,
-// would leave about 1.2% of rms(y) as error).  D = fp32 in tensor memory
-// (tcgen05.mma kind::f16, issued by one thread), read back with tcgen05.ld.
+// are).  B = up to 256 token rows, one TMA box of 64 columns x 256 rows per
+// chunk from a row-major matrix in which every token tile is contiguous: for
+// the router x itself (bf16 like its weights); for gate/up the token rows
+// copied into group order as f16 times a power of two per token (exact for
+// bf16 values in the f16 normal range; see k_x16_grouped); for the down GEMM
+// h as f16 times a power of two per row (h keeps 11 significant bits -- bf16
+// h, with 8, would leave about 1.2% of rms(y) as error).  The epilogue divides
+// the powers of two out again.  D = fp32 in tensor memory (tcgen05.mma
+// kind::f16, issued by one thread), read back with tcgen05.ld.
 // The global scale is applied in the epilogue, in fp32.
 //
-// Roles (one persistent CTA per SM, 9 warps):
-//   warps 0-3  producers: cp.async of the raw code/scale row of each thread
-//              and of the token rows, dequantisation into the A stage;
-//   warps 4-7  epilogue: TMEM -> registers -> h / y / logits;
-//   warp  8    TMEM owner (512 columns = two 256-column accumulators) and
-//              MMA issuer (one lane).
-// A 4-stage ring guarded by mbarriers (full: 128 producer arrivals, empty:
-// tcgen05.commit) feeds the MMAs; the two accumulators (acc_full: commit,
-// acc_empty: 128 epilogue arrivals) let the epilogue of one tile overlap the
-// MMAs of the next.  Every wait is bounded (2 s) and reports MOE_ETIMEOUT
-// instead of hanging; the MMA issuer drains its MMAs before TMEM is freed.
+// Roles (one persistent CTA per SM, 14 warps):
+//   warps 0-7   producers: copy the raw codes and scales of four chunks at a
+//               time (whole 128-byte lines of the weight rows) with cp.async
+//               into a ring of code groups, then two threads per weight row
+//               dequantise two chunks per step into their A stages (router
+//               rows: cp.async straight into the A stage);
+//   warps 8-11  epilogue: TMEM -> registers -> h / y / logits;
+//   warp  12    TMEM owner (512 columns = two 256-column accumulators) and
+//               MMA issuer (one lane);
+//   warp  13    B loader: one TMA box per chunk.
+// Rings of 4 weight (A) and 3 token (B) stages guarded by mbarriers (full:
+// one arrival per producer warp; full_b: the loader's expected bytes; empty,
+// empty_b: tcgen05.commit) feed the MMAs; the two accumulators (acc_full:
+// commit; acc_empty: one arrival per epilogue warp) let the epilogue of one
+// tile overlap the MMAs of the next.  Every wait is bounded (2 s) and reports
+// MOE_ETIMEOUT instead of hanging; the MMA issuer drains its MMAs before TMEM
+// is freed.
+#include <cudaTypedefs.h>
+
 #include "internal.h"
 
 namespace moe {
@@ -38,18 +49,23 @@ namespace prefill {
 
 constexpr int kBK = 64;           // K per stage (one 128-byte swizzle atom of bf16)
 constexpr int kNT = 256;          // tokens per tile (accumulator columns)
-constexpr int kStages = 4;
-constexpr int kPD = kStages - 1;  // chunks in flight ahead of the one being dequantised
-constexpr int kProducers = 128;
+constexpr int kAStages = 4;  // dequantised weight tiles
+constexpr int kBStages = 3;  // token tiles
+constexpr int kProducers = 256;  // eight warps, two threads per weight row
+constexpr int kGChunks = 4;      // chunks per code group: one 128-byte line of every weight row
+constexpr int kGStages = 3;      // code groups in flight
+constexpr int kGCodeBytes = 128 * 128;  // raw codes of a group: [128 rows][128 B], 16-byte pieces swizzled
+constexpr int kGScaleBytes = 128 * 16;  // raw scales of a group: [128 rows][16 B]
 constexpr int kEpi = 128;
-constexpr int kThreads = kProducers + kEpi + 32;
+constexpr int kThreads = kProducers + kEpi + 64;
+constexpr int kMmaWarp = (kProducers + kEpi) / 32;
+constexpr int kLoadWarp = kMmaWarp + 1;
 constexpr int kABytes = 128 * kBK * 2;   // 16 KB
 constexpr int kBBytes = kNT * kBK * 2;   // 32 KB
-constexpr int kCodeBytes = 128 * 32;     // raw codes of one chunk: 32 bytes per row
-constexpr int kScaleBytes = 128 * 4;     // raw scales of one chunk: 4 bytes per row
-constexpr int kBarriers = 2 * kStages + 2 + 2 + 1;
-constexpr size_t kSmemBytes = size_t(kStages) * (kABytes + kBBytes + kCodeBytes + kScaleBytes) + kBarriers * 8 + 8 +
-                              2 * kNT * 8 + 1024;
+constexpr int kBarriers = 2 * kAStages + 2 * kBStages + kGStages + 2 + 2 + 1;
+constexpr size_t kSmemBytes = size_t(kAStages) * kABytes + size_t(kBStages) * kBBytes +
+                              size_t(kGStages) * (kGCodeBytes + kGScaleBytes) + kBarriers * 8 + 8 + 2 * kNT * 8 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint64_t kWaitNs = 2000000000ull;  // a wait that lasts this long has failed
 
 enum Mode { kGateUp = 0, kDown = 1, kRouter = 2 };
@@ -89,6 +105,20 @@ __device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t par) {
     else if ((i & 255) == 0 && now_ns() - t0 > kWaitNs) return false;
   }
 }
+// One arrival that also expects `bytes` of asynchronous copies on the barrier.
+__device__ __forceinline__ void expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+// Box of the 2-D tensor behind `tm` (64 columns x kNT rows from (col, row),
+// 128-byte swizzle, rows past the tensor read as zeros) -> dst; completion
+// counted on b.
+__device__ __forceinline__ void tile_load(void* dst, const CUtensorMap* tm, int col, int row, uint64_t* b) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(row), "r"(su32(b))
+      : "memory");
+}
 __device__ __forceinline__ void commit_to(uint64_t* b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b))
                : "memory");
@@ -98,11 +128,17 @@ __device__ __forceinline__ void commit_to(uint64_t* b) {
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(su32(dst)), "l"(src));
 }
+__device__ __forceinline__ void cp8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(su32(dst)), "l"(src));
+}
 __device__ __forceinline__ void cp4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(su32(dst)), "l"(src));
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_wait_pd() { asm volatile("cp.async.wait_group %0;" ::"n"(kPD) : "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpi) : "memory"); }
 
@@ -112,11 +148,11 @@ struct Args {
   const uint8_t* const* grp_blob;
   const int32_t* ent_tok;
   const int32_t* ent_pos;
-  const int32_t* tile_off;   // [G+1] N tiles before each group
-  const uint16_t* bsrc;      // B rows: x [T, H] bf16 (router, gate/up) or h16 [rows, Imax] f16 (down)
-  int bstride;               // elements per B row
+  const int32_t* tile_off;
+  const int32_t* tile_grp;   // [G+1] N tiles before each group
   float* h;                  // gate/up output h (fp32) [maxTk + maxT, Imax]
-  float* hmax;               // gate/up: max|h| per row [maxTk + maxT]
+  float* hmax;               // down: max|h| per row [maxTk + maxT]
+  const float* xinv;         // gate/up: inverse power of two of each B row [maxTk + maxT]
   const float* topk_w;       // [T*k]
   const float* gate_logit;   // [T]
   float* yacc;               // down output accumulator [T, H] fp32
@@ -176,12 +212,7 @@ __device__ __forceinline__ void item_of(const Args& a, const Sched& sc, int it, 
   } else if (it < sc.routed_tiles * sc.mt_r) {
     const int ti = it / sc.mt_r;
     x.mt = it - ti * sc.mt_r;
-    int lo = 0, hi = sc.G - 1;  // last group with tile_off[g] <= ti
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (a.tile_off[mid] <= ti) lo = mid;
-      else hi = mid - 1;
-    }
+    const int lo = a.tile_grp[ti];
     x.nt = ti - a.tile_off[lo];
     x.shared = 0;
     x.e0 = a.grp_off[lo];
@@ -216,35 +247,27 @@ __device__ __forceinline__ void a_row(int mt, int r, int& mat, int& wrow) {
   }
 }
 
-// B row (in bsrc) of token-tile column j.
+// First B row of a token tile; the tile's rows follow it.  Router: x [T, H];
+// gate/up: xg [maxT*k + maxT, H] and down: h16 [maxT*k + maxT, Imax], both
+// routed entries in group order, then the shared expert's rows in token order.
 template <int MODE>
-__device__ __forceinline__ int b_row(const Args& a, const Item& x, int j) {
-  const int ent = x.nt * kNT + j;
+__device__ __forceinline__ int b_row0(const Args& a, const Item& x) {
+  const int ent = x.nt * kNT;
   if (MODE == kRouter) return ent;
-  if (MODE == kGateUp) return x.shared ? ent : a.ent_tok[x.e0 + ent];
   return x.shared ? a.maxTk + ent : x.e0 + ent;
 }
 
-__device__ __forceinline__ uint32_t bf16x2_of(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// 32 code bytes + 4 E4M3 scales of one weight row chunk -> 64 values code x
-// scale (exact) as bf16 (BF16) or f16 in the row's 8 swizzled 16-byte chunks.
-template <bool BF16>
-__device__ __forceinline__ void dequant_row(const uint8_t* codes, const uint8_t* scales, uint8_t* at, int row) {
-  const uint4 c0 = *reinterpret_cast<const uint4*>(codes), c1 = *reinterpret_cast<const uint4*>(codes + 16);
-  const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scales);
-  const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+// Half of one weight row chunk: 16 code bytes (32 columns, low nibble first;
+// scale blocks 2*half and 2*half+1 of the row's four E4M3 scales sc4) ->
+// code x scale as f16 (exact) in the row's swizzled 16-byte chunks 4*half ..
+// 4*half+3.
+__device__ __forceinline__ void dequant_half(uint4 codes, uint32_t sc4, int half, uint8_t* at, int row) {
+  const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
 #pragma unroll
-  for (int blk = 0; blk < 4; ++blk) {  // 16 values = 8 code bytes, one scale
+  for (int bl = 0; bl < 2; ++bl) {
+    const int blk = 2 * half + bl;
     const uint32_t sb = (sc4 >> (8 * blk)) & 0xffu;
-    const uint32_t sh = e4m3x2_to_f16x2(sb | (sb << 8));  // the scale in both halves, f16 (exact)
-    // bf16: the scale x 2^112 (exact: at most 4 significant bits, below 2^121)
-    const float sf = BF16 ? f16x2_to_f32x2(sh).x * 0x1p112f : 0.f;
-    const uint32_t sp = BF16 ? bf16x2_of(sf, sf) : sh;
+    const uint32_t sp = e4m3x2_to_f16x2(sb | (sb << 8));  // the scale in both halves, f16 (exact)
     uint32_t hv[8];
 #pragma unroll
     for (int w2 = 0; w2 < 2; ++w2) {
@@ -253,62 +276,72 @@ __device__ __forceinline__ void dequant_row(const uint8_t* codes, const uint8_t*
           "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
           "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
           : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-          : "r"(cw[2 * blk + w2]));
+          : "r"(cw[2 * bl + w2]));
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        if (BF16) {
-          // f16 bits of an E2M1 value moved into the bf16 field layout: read as
-          // bf16 they are the value x 2^-112 (exponent bias 15 vs 127); zero
-          // stays zero and the sign stays in place.  The 2^112 in the scale
-          // operand cancels the factor, so the product is code x scale exactly.
-          const uint32_t t = ((o[b] >> 3) & 0x0fff0fffu) | (o[b] & 0x80008000u);
-          asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hv[4 * w2 + b]) : "r"(t), "r"(sp));
-        } else {
-          asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hv[4 * w2 + b]) : "r"(o[b]), "r"(sp));
-        }
-      }
+      for (int b = 0; b < 4; ++b) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hv[4 * w2 + b]) : "r"(o[b]), "r"(sp));
     }
     *reinterpret_cast<uint4*>(at + sw128(row, 2 * blk)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
     *reinterpret_cast<uint4*>(at + sw128(row, 2 * blk + 1)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
   }
 }
 
+// Non-blocking look at a phase; true once the phase with parity `par` completed.
+__device__ __forceinline__ bool bar_test(uint64_t* b, uint32_t par) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(par)
+      : "memory");
+  return ok != 0;
+}
+
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) k_gemm(Args a) {
+__global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Args a,
+                                                       const __grid_constant__ CUtensorMap tm_r,
+                                                       const __grid_constant__ CUtensorMap tm_s) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the 128-byte swizzle pattern is a function of the shared address: atoms start on 1 KB
   uint8_t* smem = smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sA = smem;                                        // [kStages][16 KB]
-  uint8_t* sB = sA + kStages * kABytes;                      // [kStages][32 KB]
-  uint8_t* sCode = sB + kStages * kBBytes;                   // [kStages][128][32]
-  uint8_t* sScale = sCode + kStages * kCodeBytes;            // [kStages][128][4]
-  uint64_t* full = reinterpret_cast<uint64_t*>(sScale + kStages * kScaleBytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;   // [2]
+  uint8_t* sA = smem;                                        // [kAStages][16 KB]
+  uint8_t* sB = sA + kAStages * kABytes;                     // [kBStages][32 KB]
+  uint8_t* sG = sB + kBStages * kBBytes;                      // [kGStages][128][128]
+  uint8_t* sGS = sG + kGStages * kGCodeBytes;                // [kGStages][128][16]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sGS + kGStages * kGScaleBytes);
+  uint64_t* empty = full + kAStages;      // [kAStages]
+  uint64_t* full_b = empty + kAStages;    // [kBStages]
+  uint64_t* empty_b = full_b + kBStages;  // [kBStages]
+  uint64_t* gfull = empty_b + kBStages;   // [kGStages]
+  uint64_t* acc_full = gfull + kGStages;  // [2]
   uint64_t* acc_empty = acc_full + 2;     // [2]
   uint64_t* drain = acc_empty + 2;
   uint32_t* taddr_s = reinterpret_cast<uint32_t*>(drain + 1);
   int32_t* s_tok = reinterpret_cast<int32_t*>(drain + 2);  // [2][kNT] down: token of each column
-  float* s_w = reinterpret_cast<float*>(s_tok + 2 * kNT);  // [2][kNT] down: its weight
+  float* s_w = reinterpret_cast<float*>(s_tok + 2 * kNT);  // [2][kNT] down: its weight; gate/up: 2^-p
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const Sched sc = make_sched<MODE>(a);
 
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(taddr_s)),
                  "r"(2 * kNT));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      bar_init(&full[s], kProducers);
+    for (int s = 0; s < kAStages; ++s) {
+      bar_init(&full[s], kProducers / 32);  // one arrival per producer warp
       bar_init(&empty[s], 1);
     }
+    for (int s = 0; s < kBStages; ++s) {
+      bar_init(&full_b[s], 1);
+      bar_init(&empty_b[s], 1);
+    }
+    for (int g = 0; g < kGStages; ++g) bar_init(&gfull[g], kProducers);  // every producer's copies
     for (int b = 0; b < 2; ++b) {
       bar_init(&acc_full[b], 1);
-      bar_init(&acc_empty[b], kEpi);
+      bar_init(&acc_empty[b], kEpi / 32);  // one arrival per epilogue warp
     }
     bar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -319,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(Args a) {
   const uint32_t taddr = *taddr_s;
   bool failed = false;
 
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int q = 0, done = 0;
@@ -328,9 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(Args a) {
         item_of<MODE>(a, sc, it, x);
         const int npad = (x.n + 15) & ~15;
         const int buf = done & 1;
-        // kind::f16: D f32, A and B both bf16 (router, gate/up) or both f16
-        // (down), both K-major, N = npad, M = 128
-        const uint32_t ab = MODE == kDown ? 0u : 1u;
+        // kind::f16: D f32, A and B both bf16 (router) or both f16 (gate/up,
+        // down), both K-major, N = npad, M = 128
+        const uint32_t ab = MODE == kRouter ? 1u : 0u;
         const uint32_t idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(npad >> 3) << 17) |
                                (uint32_t(128 >> 4) << 24);
         if (done >= 2 && !bar_wait(&acc_empty[buf], ((done >> 1) - 1) & 1)) {
@@ -339,13 +372,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(Args a) {
         }
         const uint32_t dt = taddr + uint32_t(buf * kNT);
         for (int kc = 0; kc < x.KC; ++kc, ++q) {
-          const int s = q % kStages;
-          if (!bar_wait(&full[s], (q / kStages) & 1)) {
+          const int s = q % kAStages, sb = q % kBStages;
+          if (!bar_wait(&full[s], (q / kAStages) & 1) || !bar_wait(&full_b[sb], (q / kBStages) & 1)) {
             failed = true;
             break;
           }
           asm volatile("tcgen05.fence::after_thread_sync;");
-          const uint64_t da = kmajor_desc(sA + s * kABytes), db = kmajor_desc(sB + s * kBBytes);
+          const uint64_t da = kmajor_desc(sA + s * kABytes), db = kmajor_desc(sB + sb * kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint32_t accum = (kc > 0 || k > 0) ? 1u : 0u;
@@ -355,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(Args a) {
                 "l"(da + uint64_t(k * 2)), "l"(db + uint64_t(k * 2)), "r"(idesc), "r"(accum));
           }
           commit_to(&empty[s]);
+          commit_to(&empty_b[sb]);
         }
         if (!failed) commit_to(&acc_full[buf]);
       }
@@ -363,86 +397,210 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(Args a) {
       if (!bar_wait(drain, 0)) failed = true;
       if (failed) set_error(a.err, MOE_ETIMEOUT);
     }
-  } else if (warp < 4) {
+  } else if (warp < kProducers / 32) {
     // ------------------------------------------------------------ producers
-    int iss_it = blockIdx.x, iss_kc = 0, iss_q = 0;
+    const int prow = tid >> 1, half = tid & 1;  // this thread's weight row and half of it
+    // the chunks of this CTA's items, in order: the next one to copy
+    int iss_it = blockIdx.x, iss_kc = 0;
     Item ix;
     bool iss_ok = iss_it < sc.n_items;
-    const uint16_t* bp[kNT / 16];  // this thread's token rows: j = tid/8 + 16m, chunk tid%8
-    const uint8_t* code_p = nullptr;
-    const uint8_t* scale_p = nullptr;
     const uint16_t* arow = nullptr;  // router: this thread's weight row
     auto load_item = [&]() {
       item_of<MODE>(a, sc, iss_it, ix);
-#pragma unroll
-      for (int m = 0; m < kNT / 16; ++m) {
-        const int j = (tid >> 3) + 16 * m;
-        bp[m] = j < ix.n ? a.bsrc + size_t(b_row<MODE>(a, ix, j)) * a.bstride + (tid & 7) * 8 : nullptr;
-      }
       if (MODE == kRouter) {
-        const int r = ix.mt * 128 + tid;
+        const int r = ix.mt * 128 + prow;
         arow = r < a.E ? a.w_router + size_t(r) * a.H : (r == a.E ? a.w_gate : nullptr);
-      } else {
-        int mat, wrow;
-        a_row<MODE>(ix.mt, tid, mat, wrow);
-        const DevBlobLayout& lay = ix.shared ? a.lay_s : a.lay_r;
-        code_p = ix.blob ? ix.blob + lay.code_off[mat] + size_t(wrow) * (ix.C / 2) : nullptr;
-        scale_p = ix.blob ? ix.blob + lay.scale_off[mat] + size_t(wrow) * (ix.C / 16) : nullptr;
       }
     };
     if (iss_ok) load_item();
-    auto issue = [&]() {
-      if (iss_ok) {
-        const int s = iss_q % kStages;
-        if (!failed && iss_q >= kStages && !bar_wait(&empty[s], ((iss_q / kStages) - 1) & 1)) failed = true;
-        failed = __any_sync(0xffffffffu, failed);  // warp-uniform
-        if (!failed) {
-          if (MODE == kRouter) {
-            if (arow) {
-              uint8_t* at = sA + s * kABytes;
+
+    if (MODE == kRouter) {
+      // Router rows are bf16 already: copied straight into the A stage,
+      // kAStages - 1 chunks ahead (into the stage of chunk q - 1, whose MMAs
+      // have run while chunk q was landing).
+      int iss_q = 0;
+      auto issue = [&]() {
+        if (iss_ok) {
+          const int s = iss_q % kAStages;
+          if (!failed && iss_q >= kAStages && !bar_wait(&empty[s], ((iss_q / kAStages) - 1) & 1)) failed = true;
+          failed = __any_sync(0xffffffffu, failed);  // warp-uniform
+          if (!failed && arow) {
+            uint8_t* at = sA + s * kABytes;
 #pragma unroll
-              for (int c = 0; c < 8; ++c) cp16(at + sw128(tid, c), arow + iss_kc * kBK + c * 8);
-            }
-          } else if (code_p) {
-            uint8_t* cd = sCode + s * kCodeBytes + tid * 32;
-            cp16(cd, code_p + iss_kc * 32);
-            cp16(cd + 16, code_p + iss_kc * 32 + 16);
-            cp4(sScale + s * kScaleBytes + tid * 4, scale_p + iss_kc * 4);
+            for (int c = 4 * half; c < 4 * half + 4; ++c) cp16(at + sw128(prow, c), arow + iss_kc * kBK + c * 8);
           }
-          uint8_t* bt = sB + s * kBBytes;
-#pragma unroll
-          for (int m = 0; m < kNT / 16; ++m)
-            if (bp[m]) cp16(bt + sw128((tid >> 3) + 16 * m, tid & 7), bp[m] + iss_kc * kBK);
+          ++iss_q;
+          if (++iss_kc == ix.KC) {
+            iss_kc = 0;
+            iss_it += gridDim.x;
+            iss_ok = iss_it < sc.n_items;
+            if (iss_ok) load_item();
+          }
         }
-        ++iss_q;
-        if (++iss_kc == ix.KC) {
-          iss_kc = 0;
-          iss_it += gridDim.x;
-          iss_ok = iss_it < sc.n_items;
-          if (iss_ok) load_item();
+        cp_commit();
+      };
+      for (int p = 0; p < kAStages - 1; ++p) issue();
+      int q = 0;
+      for (int it = blockIdx.x; it < sc.n_items; it += gridDim.x) {
+        Item x;
+        item_of<MODE>(a, sc, it, x);
+        for (int kc = 0; kc < x.KC; ++kc, ++q) {
+          cp_wait<kAStages - 2>();  // chunk q has landed (q+1 .. q+kAStages-2 may be in flight)
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) bar_arrive(&full[q % kAStages]);
+          issue();
         }
       }
-      cp_commit();
-    };
-    for (int p = 0; p < kPD; ++p) issue();
+      cp_wait_all();
+    } else {
+      // Expert weights come in code groups of kGChunks chunks: one 128-byte
+      // line of each of the tile's 128 weight rows (eight threads per row, so
+      // every request is a whole line) and the rows' 16 scale bytes, copied
+      // with cp.async kGStages groups ahead into a ring whose 16-byte pieces are
+      // swizzled by row; each thread's copies arrive on the group's barrier
+      // when they land.  Chunks are then dequantised two at a time into their
+      // A stages (each free once the MMAs of chunk c - kAStages completed), so
+      // the fixed costs of a step are shared by two chunks.
+      int iss_gi = 0;                  // next group to copy: group iss_gi of item iss_it
+      const uint8_t* crow[4];          // code rows (tid/8 + 32u) of the item being copied
+      const uint8_t* srow = nullptr;   // scale row tid (tid < 128)
+      int rowbytes = 0;
+      auto load_rows = [&]() {
+        for (int u = 0; u < 4; ++u) crow[u] = nullptr;
+        srow = nullptr;
+        rowbytes = ix.C / 2;
+        if (!ix.blob) return;
+        const DevBlobLayout& lay = ix.shared ? a.lay_s : a.lay_r;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          int mat, wrow;
+          a_row<MODE>(ix.mt, (tid >> 3) + 32 * u, mat, wrow);
+          crow[u] = ix.blob + lay.code_off[mat] + size_t(wrow) * rowbytes;
+        }
+        if (tid < 128) {
+          int mat, wrow;
+          a_row<MODE>(ix.mt, tid, mat, wrow);
+          srow = ix.blob + lay.scale_off[mat] + size_t(wrow) * (ix.C / 16);
+        }
+      };
+      if (iss_ok) load_rows();
+      int iss_g = 0;  // groups copied so far
+      auto copy_group = [&]() {
+        if (iss_ok) {
+          const int gs = iss_g % kGStages;
+          const int gbytes = min(128, rowbytes - iss_gi * 128);  // 32 per chunk
+          const int j = tid & 7;
+          if (j * 16 < gbytes) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int r = (tid >> 3) + 32 * u;
+              if (crow[u]) cp16(sG + gs * kGCodeBytes + r * 128 + ((j ^ (r & 7)) << 4), crow[u] + iss_gi * 128 + j * 16);
+            }
+          }
+          if (srow) {
+            uint8_t* d = sGS + gs * kGScaleBytes + tid * 16;
+            const uint8_t* sp = srow + iss_gi * 16;
+            if (gbytes == 128) cp16(d, sp);
+            else if (gbytes == 64) cp8(d, sp);
+            else cp4(d, sp);
+          }
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(&gfull[gs])) : "memory");
+          ++iss_g;
+          if (++iss_gi * 128 >= rowbytes) {
+            iss_gi = 0;
+            iss_it += gridDim.x;
+            iss_ok = iss_it < sc.n_items;
+            if (iss_ok) {
+              load_item();
+              load_rows();
+            }
+          }
+        }
+      };
+      for (int g = 0; g < kGStages; ++g) copy_group();
 
+      int c = 0, g = 0;  // chunks and groups consumed
+      for (int it = blockIdx.x; it < sc.n_items; it += gridDim.x) {
+        Item x;
+        item_of<MODE>(a, sc, it, x);
+        for (int c_in = 0; c_in < x.KC; c_in += kGChunks, ++g) {
+          const int nch = min(kGChunks, x.KC - c_in);
+          const int gs = g % kGStages;
+          if (!failed && !bar_wait(&gfull[gs], (g / kGStages) & 1)) failed = true;
+          for (int kk = 0; kk < nch;) {
+            const bool two = kk + 1 < nch;
+            const int s0 = c % kAStages, s1 = (c + 1) % kAStages;
+            // A stages free: both looks issued before either result is needed
+            if (!failed) {
+              const bool w0 = c >= kAStages, w1 = two && c + 1 >= kAStages;
+              const uint32_t p0 = ((c / kAStages) - 1) & 1, p1 = (((c + 1) / kAStages) - 1) & 1;
+              const bool f0 = !w0 || bar_test(&empty[s0], p0);
+              const bool f1 = !w1 || bar_test(&empty[s1], p1);
+              if ((!f0 && !bar_wait(&empty[s0], p0)) || (!f1 && !bar_wait(&empty[s1], p1))) failed = true;
+            }
+            failed = __any_sync(0xffffffffu, failed);  // warp-uniform
+            if (!failed && x.blob) {
+              const uint8_t* gc = sG + gs * kGCodeBytes + prow * 128;
+              const uint8_t* gsc = sGS + gs * kGScaleBytes + prow * 16;
+              const int j0 = 2 * kk + half, j1 = 2 * (kk + 1) + half;  // this thread's pieces
+              const uint4 c0 = *reinterpret_cast<const uint4*>(gc + ((j0 ^ (prow & 7)) << 4));
+              const uint32_t sc0 = *reinterpret_cast<const uint32_t*>(gsc + kk * 4);
+              uint4 c1 = make_uint4(0u, 0u, 0u, 0u);
+              uint32_t sc1 = 0u;
+              if (two) {
+                c1 = *reinterpret_cast<const uint4*>(gc + ((j1 ^ (prow & 7)) << 4));
+                sc1 = *reinterpret_cast<const uint32_t*>(gsc + (kk + 1) * 4);
+              }
+              dequant_half(c0, sc0, half, sA + s0 * kABytes, prow);
+              if (two) dequant_half(c1, sc1, half, sA + s1 * kABytes, prow);
+            }
+            // every thread's shared-memory writes are made visible to the
+            // tensor core (async proxy); after the warp has synchronised, one
+            // lane arrives for each chunk
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              bar_arrive(&full[s0]);
+              if (two) bar_arrive(&full[s1]);
+            }
+            kk += two ? 2 : 1;
+            c += two ? 2 : 1;
+          }
+          // every producer is done with the group's ring stage before it is refilled
+          asm volatile("bar.sync 2, %0;" ::"n"(kProducers) : "memory");
+          copy_group();
+        }
+      }
+      cp_wait_all();
+    }
+    if (failed) set_error(a.err, MOE_ETIMEOUT);
+  } else if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ B loader
     int q = 0;
-    for (int it = blockIdx.x; it < sc.n_items; it += gridDim.x) {
+    for (int it = blockIdx.x; it < sc.n_items && !failed; it += gridDim.x) {
       Item x;
       item_of<MODE>(a, sc, it, x);
+      // token tiles are contiguous rows: one 32 KB box per chunk (columns past
+      // n hold other rows or zeros and are never read back)
+      const CUtensorMap* tm = x.shared ? &tm_s : &tm_r;
+      const int row0 = b_row0<MODE>(a, x);
       for (int kc = 0; kc < x.KC; ++kc, ++q) {
-        issue();       // chunk q + kPD
-        cp_wait_pd();  // this thread's copies of chunk q have landed
-        const int s = q % kStages;
-        if (MODE != kRouter && x.blob && !failed)
-          dequant_row<MODE == kGateUp>(sCode + s * kCodeBytes + tid * 32, sScale + s * kScaleBytes + tid * 4,
-                                       sA + s * kABytes, tid);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        bar_arrive(&full[s]);
+        const int s = q % kBStages;
+        if (q >= kBStages && !bar_wait(&empty_b[s], ((q / kBStages) - 1) & 1)) failed = true;
+        failed = __any_sync(0xffffffffu, failed);
+        if (failed) break;
+        if (lane == 0) {
+          expect_tx(&full_b[s], kBBytes);
+          tile_load(sB + s * kBBytes, tm, kc * kBK, row0, &full_b[s]);
+        }
+        __syncwarp();
       }
     }
-    cp_wait_all();
-    if (failed) set_error(a.err, MOE_ETIMEOUT);
+    // the copies of the last stages have landed before the CTA can leave
+    for (int qq = q > kBStages ? q - kBStages : 0; qq < q; ++qq)
+      if (!bar_wait(&full_b[qq % kBStages], (qq / kBStages) & 1)) failed = true;
+    if (failed && lane == 0) set_error(a.err, MOE_ETIMEOUT);
   } else {
     // ------------------------------------------------------------ epilogue
     const int et = tid - kProducers, qw = warp & 3;
@@ -470,6 +628,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(Args a) {
           s_w[buf * kNT + j] = w / pow2_scale_for(a.hmax[hrow]);
         }
         epi_sync();
+      } else if (MODE == kGateUp) {
+        // B row = x_t x 2^p: the inverse power of two of each column
+        for (int j = et; j < x.n; j += kEpi) {
+          const int ent = x.nt * kNT + j;
+          s_w[buf * kNT + j] = a.xinv[x.shared ? a.maxTk + ent : x.e0 + ent];
+        }
+        epi_sync();
       }
       if (!failed && !bar_wait(&acc_full[buf], (done >> 1) & 1)) failed = true;
       failed = __any_sync(0xffffffffu, failed);
@@ -480,42 +645,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(Args a) {
       const uint32_t tb = taddr + uint32_t(buf * kNT) + (uint32_t(qw * 32) << 16);
       const int row = x.mt * 128 + qw * 32 + lane;  // router / down: output row of this lane
       const float rbias = (MODE == kRouter && a.bias && row < a.E) ? a.bias[row] : 0.f;
-      for (int c0 = 0; c0 < npad && !failed; c0 += 16) {
-        uint32_t v[16];
+      // gate/up: h row of column 0 of this tile and this lane's intermediate
+      float* hcol = nullptr;
+      if (MODE == kGateUp)
+        hcol = a.h + size_t(x.shared ? a.maxTk + x.nt * kNT : x.e0 + x.nt * kNT) * a.Imax + x.mt * 64 + qw * 16 +
+               (lane & 15);
+      // 32 accumulator columns per TMEM load (columns past npad are read and
+      // ignored: the 256 columns of the buffer are all allocated)
+      for (int c0 = 0; c0 < npad && !failed; c0 += 32) {
+        uint32_t v[32];
         asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
             : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+              "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+              "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
             : "r"(tb + uint32_t(c0)));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         if (MODE == kGateUp) {
-          // lanes 0-15 hold gate rows, 16-31 the matching up rows: the low lanes
-          // finish columns 0-7 of this slice, the high lanes columns 8-15
+          // lanes 0-15 hold gate rows, 16-31 the matching up rows: of each 16
+          // columns the low lanes finish the first 8, the high lanes the last 8
           const bool hi = lane >= 16;
-          const int i = x.mt * 64 + qw * 16 + (lane & 15);
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const float mine_lo = __uint_as_float(v[jj]), mine_hi = __uint_as_float(v[jj + 8]);
+          for (int jj = 0; jj < 16; ++jj) {
+            const int b = (jj >> 3) * 16 + (jj & 7);
+            const float mine_lo = __uint_as_float(v[b]), mine_hi = __uint_as_float(v[b + 8]);
             const float recv = __shfl_xor_sync(0xffffffffu, hi ? mine_lo : mine_hi, 16);
             const float g = hi ? recv : mine_lo, u = hi ? mine_hi : recv;
-            const int j = c0 + jj + (hi ? 8 : 0);
-            const int ent = x.nt * kNT + j;
-            const int hrow = x.shared ? a.maxTk + ent : x.e0 + ent;
-            float hv = 0.f;
+            const int j = c0 + b + (hi ? 8 : 0);
             if (j < x.n) {
-              hv = x.blob ? silu_f32(g * gs0) * (u * gs1) : 0.f;
-              a.h[size_t(hrow) * a.Imax + i] = hv;
+              const float xi = s_w[buf * kNT + j];
+              hcol[size_t(j) * a.Imax] = x.blob ? silu_f32(g * (gs0 * xi)) * (u * (gs1 * xi)) : 0.f;
             }
-            // max|h| of this column over the warp's 16 intermediates
-            float m = fabsf(hv);
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if ((lane & 15) == 0 && j < x.n) atomicMax(reinterpret_cast<unsigned int*>(a.hmax) + hrow, __float_as_uint(m));
           }
         } else if (MODE == kDown) {
           if (x.blob) {
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
+            for (int jj = 0; jj < 32; ++jj) {
               const int j = c0 + jj;
               if (j < x.n)
                 atomicAdd(a.yacc + size_t(s_tok[buf * kNT + j]) * a.H + row,
@@ -524,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(Args a) {
           }
         } else {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
+          for (int jj = 0; jj < 32; ++jj) {
             const int j = c0 + jj;
             const int tok = x.nt * kNT + j;
             const float d = __uint_as_float(v[jj]);
@@ -536,21 +703,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(Args a) {
         }
       }
       asm volatile("tcgen05.fence::before_thread_sync;");
-      bar_arrive(&acc_empty[buf]);
+      __syncwarp();
+      if (lane == 0) bar_arrive(&acc_empty[buf]);
     }
     if (failed) set_error(a.err, MOE_ETIMEOUT);
   }
   asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.fence::after_thread_sync;");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(2 * kNT));
   }
 }
 
-// N tiles per group, as an exclusive prefix: tile_off[g] = sum_{g'<g} ceil(n_g'/kNT).
+// N tiles per group, as an exclusive prefix: tile_off[g] = sum_{g'<g} ceil(n_g'/kNT),
+// and the group of every tile: tile_grp[t] = g for tile_off[g] <= t < tile_off[g+1].
 __global__ void __launch_bounds__(1024) k_tiles(const int32_t* __restrict__ num_groups, const int32_t* __restrict__ grp_off,
-                                                int32_t* __restrict__ tile_off) {
+                                                int32_t* __restrict__ tile_off, int32_t* __restrict__ tile_grp) {
   pdl_trigger();
   pdl_wait();
   __shared__ int ws[32];
@@ -579,34 +748,106 @@ __global__ void __launch_bounds__(1024) k_tiles(const int32_t* __restrict__ num_
     }
     __syncthreads();
     const int before = (w ? ws[w - 1] : 0) + carry;
-    if (g < G) tile_off[g] = before + x - v;
+    if (g < G) {
+      tile_off[g] = before + x - v;
+      for (int t = 0; t < v; ++t) tile_grp[before + x - v + t] = g;
+    }
     carry += ws[(blockDim.x >> 5) - 1];
     __syncthreads();
   }
   if (threadIdx.x == 0) tile_off[G] = carry;
 }
 
-// h (fp32) -> f16 times a per-row power of two chosen from max|h_row|.
-__global__ void __launch_bounds__(256) k_h16(const float* __restrict__ h, const float* __restrict__ hmax,
+// h (fp32) -> f16 times a per-row power of two chosen from max|h_row| over the
+// row's I (routed) or I_s (shared) columns; the max goes to hmax for the down
+// GEMM's epilogue, which divides the power of two out again.  One warp per row.
+__global__ void __launch_bounds__(256) k_h16(const float* __restrict__ h, float* __restrict__ hmax,
                                              __half* __restrict__ h16, const int32_t* __restrict__ grp_off,
-                                             const int32_t* __restrict__ num_groups, int Imax, int maxTk, int T,
-                                             int has_shared) {
+                                             const int32_t* __restrict__ num_groups, int Imax, int I, int I_s,
+                                             int maxTk, int T, int has_shared) {
   pdl_trigger();
   pdl_wait();
   const int routed = grp_off[*num_groups];
   const int rows = routed + (has_shared ? T : 0);
-  const int per = Imax / 4;
-  for (size_t idx = size_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < size_t(rows) * per;
-       idx += size_t(gridDim.x) * blockDim.x) {
-    const int rr = int(idx / per), c4 = int(idx - size_t(rr) * per);
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int rr = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); rr < rows; rr += nwarps) {
     const int row = rr < routed ? rr : maxTk + (rr - routed);
-    const float sc = pow2_scale_for(hmax[row]);
-    const float4 f = reinterpret_cast<const float4*>(h + size_t(row) * Imax)[c4];
-    __half2 p0 = __floats2half2_rn(f.x * sc, f.y * sc), p1 = __floats2half2_rn(f.z * sc, f.w * sc);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&p0);
-    u.y = *reinterpret_cast<uint32_t*>(&p1);
-    reinterpret_cast<uint2*>(h16 + size_t(row) * Imax)[c4] = u;
+    const int n4 = (rr < routed ? I : I_s) / 4;
+    const float4* src = reinterpret_cast<const float4*>(h + size_t(row) * Imax);
+    float m = 0.f;
+    for (int c4 = lane; c4 < n4; c4 += 32) {
+      const float4 f = src[c4];
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) hmax[row] = m;
+    const float sc = pow2_scale_for(m);
+    for (int c4 = lane; c4 < n4; c4 += 32) {
+      const float4 f = src[c4];
+      __half2 p0 = __floats2half2_rn(f.x * sc, f.y * sc), p1 = __floats2half2_rn(f.z * sc, f.w * sc);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&p0);
+      u.y = *reinterpret_cast<uint32_t*>(&p1);
+      reinterpret_cast<uint2*>(h16 + size_t(row) * Imax)[c4] = u;
+    }
+  }
+}
+
+// B rows of the gate/up GEMM: token rows as f16 times a power of two per token
+// (max|x_t| brought into [2^12, 2^13)), in group order for the routed entries
+// (row e = x[ent_tok[e]]) and in token order for the shared expert (row
+// maxTk + t); xinv gets the inverse power of two of each row.  bf16 values have
+// 8 significant bits, so the scaled value is exact in f16 unless it falls below
+// the f16 normal range, where the error stays under 2^-25 max|x_t|.  One warp
+// per row, the row held in registers: PER 16-byte pieces per lane (H <= 256 PER).
+template <int PER>
+__global__ void __launch_bounds__(256) k_x16_grouped(const uint16_t* __restrict__ x, __half* __restrict__ xg,
+                                                     float* __restrict__ xinv, const int32_t* __restrict__ ent_tok,
+                                                     const int32_t* __restrict__ grp_off,
+                                                     const int32_t* __restrict__ num_groups, int H, int maxTk, int T,
+                                                     int has_shared) {
+  pdl_trigger();
+  pdl_wait();
+  const int routed = grp_off[*num_groups];
+  const int rows = routed + (has_shared ? T : 0);
+  const int lane = threadIdx.x & 31, n16 = H / 8;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int rr = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); rr < rows; rr += nwarps) {
+    const int tok = rr < routed ? ent_tok[rr] : rr - routed;
+    const int orow = rr < routed ? rr : maxTk + (rr - routed);
+    const uint4* src = reinterpret_cast<const uint4*>(x + size_t(tok) * H);
+    uint4 v[PER];
+    float m = 0.f;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int c = u * 32 + lane;
+      v[u] = c < n16 ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xffff0000u))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float sc = pow2_scale_for(m);
+    if (lane == 0) xinv[orow] = 1.0f / sc;
+    uint4* dst = reinterpret_cast<uint4*>(xg + size_t(orow) * H);
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int c = u * 32 + lane;
+      if (c < n16) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const __half2 hh = __floats2half2_rn(__uint_as_float(w[q] << 16) * sc, __uint_as_float(w[q] & 0xffff0000u) * sc);
+          o[q] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+        dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
   }
 }
 
@@ -637,8 +878,38 @@ static int sm_count() {
   return n;
 }
 
+// Tensor map of a row-major [rows, cols] matrix of 16-bit values for the B
+// loader: boxes of 64 columns x kNT rows, 128-byte swizzle.  Needs a 16-byte
+// aligned base and cols % 8 == 0.
+static int encode_rows(CUtensorMap* tm, const void* base, int cols, int rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
+  if (!encode || (reinterpret_cast<uintptr_t>(base) & 15) || cols % 8 || rows <= 0) return MOE_ECUDA;
+  const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+  const cuuint32_t box[2] = {cuuint32_t(prefill::kBK), cuuint32_t(prefill::kNT)};
+  const cuuint32_t es[2] = {1, 1};
+  if (encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MOE_ECUDA;
+  return MOE_OK;
+}
+
+// B of routed tiles from [r_rows, cols] at r_base, of shared-expert tiles from
+// [s_rows, cols] at s_base.
 template <int MODE>
-static int launch_gemm(const prefill::Args& a, cudaStream_t s) {
+static int launch_gemm(const prefill::Args& a, const void* r_base, int r_rows, const void* s_base, int s_rows, int cols,
+                       cudaStream_t s) {
+  alignas(64) CUtensorMap tm_r, tm_s;
+  if (int rc = encode_rows(&tm_r, r_base, cols, r_rows)) return rc;
+  if (int rc = encode_rows(&tm_s, s_base, cols, s_rows)) return rc;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(prefill::k_gemm<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -646,7 +917,7 @@ static int launch_gemm(const prefill::Args& a, cudaStream_t s) {
       return MOE_ECUDA;
     attr = true;
   }
-  if (launch_pdl(prefill::k_gemm<MODE>, dim3(sm_count()), dim3(prefill::kThreads), prefill::kSmemBytes, s, a) !=
+  if (launch_pdl(prefill::k_gemm<MODE>, dim3(sm_count()), dim3(prefill::kThreads), prefill::kSmemBytes, s, a, tm_r, tm_s) !=
       cudaSuccess)
     return MOE_ECUDA;
   return MOE_OK;
@@ -666,8 +937,10 @@ static prefill::Args base_args(const moe_layer_desc* d, int T, moe_ws* ws) {
   a.ent_tok = ws->ent_tok;
   a.ent_pos = ws->ent_pos;
   a.tile_off = ws->tile_off;
+  a.tile_grp = ws->tile_grp;
   a.h = ws->h;
   a.hmax = ws->hmax;
+  a.xinv = ws->xinv;
   a.topk_w = ws->topk_w;
   a.gate_logit = ws->gate_logit;
   a.shared_blob = has_shared ? reinterpret_cast<const uint8_t*>(d->shared_blob) : nullptr;
@@ -687,18 +960,16 @@ static prefill::Args base_args(const moe_layer_desc* d, int T, moe_ws* ws) {
 
 int launch_prefill_router(const moe_layer_desc* d, const uint16_t* x, int T, moe_ws* ws, cudaStream_t s) {
   prefill::Args a = base_args(d, T, ws);
-  a.bsrc = x;
-  a.bstride = d->s.H;
   a.w_router = d->w_router;
   a.w_gate = d->s.I_shared > 0 ? d->w_shared_gate : nullptr;
   a.bias = d->bias;
   a.logits = ws->logits;
   a.gate_out = ws->gate_logit;
-  return launch_gemm<prefill::kRouter>(a, s);
+  return launch_gemm<prefill::kRouter>(a, x, T, x, T, d->s.H, s);
 }
 
-// The expert part of a prefill call: tiles, gate/up GEMM (h and max|h| per
-// row), h -> f16 times a per-row power of two, down GEMM accumulating w*o
+// The expert part of a prefill call: tiles, gate/up GEMM (h), max|h| per row
+// and h -> f16 times a per-row power of two, down GEMM accumulating w*o
 // into an fp32 buffer, and the output cast.
 int launch_prefill_experts(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T, moe_ws* ws,
                            cudaStream_t s) {
@@ -709,28 +980,34 @@ int launch_prefill_experts(const moe_layer_desc* d, const uint16_t* x, void* y, 
   a.yacc = yacc;
   {
     ProfScope p(ws, "tiles_zero", s);
-    if (launch_pdl(k_tiles, dim3(1), dim3(1024), 0, s, ws->num_groups, ws->grp_off, ws->tile_off) != cudaSuccess)
+    if (launch_pdl(k_tiles, dim3(1), dim3(1024), 0, s, ws->num_groups, ws->grp_off, ws->tile_off, ws->tile_grp) !=
+        cudaSuccess)
       return MOE_ECUDA;
     MOE_CUDA_TRY(cudaMemsetAsync(yacc, 0, size_t(T) * sh.H * 4, s));
+  }
+  {
+    ProfScope p(ws, "x16_grouped", s);
+    auto kern = sh.H <= 256 ? k_x16_grouped<1> : sh.H <= 512 ? k_x16_grouped<2> : sh.H <= 1024 ? k_x16_grouped<4>
+              : sh.H <= 2048 ? k_x16_grouped<8> : k_x16_grouped<16>;
+    if (sh.H > 4096) return MOE_EINVAL;
+    if (launch_pdl(kern, dim3(sm_count() * 8), dim3(256), 0, s, x, ws->xg, ws->xinv, ws->ent_tok, ws->grp_off,
+                   ws->num_groups, sh.H, a.maxTk, T, a.shared_blob ? 1 : 0) != cudaSuccess)
+      return MOE_ECUDA;
   }
   int rc;
   {
     ProfScope p(ws, "gateup_gemm", s);
-    a.bsrc = x;
-    a.bstride = sh.H;
-    if ((rc = launch_gemm<kGateUp>(a, s))) return rc;
+    if ((rc = launch_gemm<kGateUp>(a, ws->xg, a.maxTk + ws->maxT, ws->xg, a.maxTk + ws->maxT, sh.H, s))) return rc;
   }
   {
     ProfScope p(ws, "h16", s);
     if (launch_pdl(k_h16, dim3(sm_count() * 8), dim3(256), 0, s, ws->h, ws->hmax, ws->h16, ws->grp_off,
-                   ws->num_groups, a.Imax, a.maxTk, T, a.shared_blob ? 1 : 0) != cudaSuccess)
+                   ws->num_groups, a.Imax, a.I, a.I_s, a.maxTk, T, a.shared_blob ? 1 : 0) != cudaSuccess)
       return MOE_ECUDA;
   }
   {
     ProfScope p(ws, "down_gemm", s);
-    a.bsrc = reinterpret_cast<const uint16_t*>(ws->h16);
-    a.bstride = a.Imax;
-    if ((rc = launch_gemm<kDown>(a, s))) return rc;
+    if ((rc = launch_gemm<kDown>(a, ws->h16, a.maxTk + ws->maxT, ws->h16, a.maxTk + ws->maxT, a.Imax, s))) return rc;
   }
   if (!y_is_fp32) {
     ProfScope p(ws, "cast", s);
