@@ -71,9 +71,8 @@ typedef struct moe_ws moe_ws;       /* per-call scratch: logits, ids, groups, h,
 
 /* One MoE layer.  H hidden, I routed intermediate, E experts, k per token,
  * I_shared shared-expert intermediate (0 = no shared expert).
- * Limits: H, I, I_shared powers of two in [32, 4096]; I_shared == 0 or the
- * same number of 32-column chunks per lane as I (both <= 1024, or equal);
- * 1 <= k <= min(E, 32); 1 <= E <= 1024. */
+ * Limits: H, I and a nonzero I_shared powers of two in [64, 4096];
+ * 1 <= k <= min(E, 32); 1 <= E <= 1024.  Anything else is MOE_EINVAL. */
 typedef struct {
   int H, I, E, k, I_shared;
 } moe_layer_shape;
@@ -229,10 +228,10 @@ int moe_group(const int32_t* topk_ids, int T, int k, int E, int layer, moe_cache
  * fp32 [T, H] when y_is_fp32.  T <= the workspace's maxT.  mode selects the
  * decode kernels (CUDA-core router, GEMVs) or the prefill kernels (router and
  * grouped expert GEMMs on the tensor cores); AUTO takes prefill from 128
- * tokens on.  Prefill needs H >= 128 and 16-byte aligned x, w_router and
- * w_shared_gate, else MOE_EINVAL; its y accumulates in fp32 with atomic adds,
- * so the order of the (at most k + 1) terms per element may vary between
- * runs. */
+ * tokens on.  Prefill needs H >= 128 and 16-byte aligned x, y, w_router and
+ * w_shared_gate, else MOE_EINVAL; its y accumulates in fp32 with atomic
+ * adds, so the order of the (at most k + 1) terms per element may vary
+ * between runs. */
 int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T, moe_cache* c,
                       moe_ws* ws, int mode, moe_stream_t stream);
 

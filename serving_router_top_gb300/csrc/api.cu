@@ -271,7 +271,7 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   const size_t split_blocks = size_t(small_groups + 1) * rb_max;
   const size_t o_part = cv.take<float>(split_blocks * 8 * 32 * 8);
   const size_t o_toff = cv.take<int32_t>(size_t(s.E) + 2);
-  const size_t o_tgrp = cv.take<int32_t>(size_t(s.E) + Tk / 256 + 2);
+  const size_t o_tgrp = cv.take<int32_t>(size_t(s.E) + Tk / 128 + 2);
   const size_t o_h16 = cv.take<__half>((Tk + maxT) * Imax);
   const size_t o_yacc = cv.take<float>(size_t(maxT) * s.H);
   const size_t o_cnt = cv.take<int>(split_blocks);
@@ -304,9 +304,9 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   w->tile_off = reinterpret_cast<int32_t*>(base + o_toff);
   w->tile_grp = reinterpret_cast<int32_t*>(base + o_tgrp);
   w->h16 = reinterpret_cast<__half*>(base + o_h16);
+  w->yacc = reinterpret_cast<float*>(base + o_yacc);
   w->xg = reinterpret_cast<__half*>(base + o_o);  // (Tk+maxT)*H 16-bit values fit in (Tk+maxT)*H floats
   w->xinv = reinterpret_cast<float*>(base + o_xinv);
-  w->yacc = reinterpret_cast<float*>(base + o_yacc);
   w->cnt = reinterpret_cast<int*>(base + o_cnt);
   w->split_blocks = split_blocks;
   w->o = reinterpret_cast<float*>(base + o_o);
@@ -416,7 +416,7 @@ int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y
   int rc;
   // decode GEMVs for small windows, tcgen05 GEMMs for prefill chunks
   const bool prefill = mode == MOE_MODE_PREFILL || (mode == MOE_MODE_AUTO && T >= kPrefillMinTokens);
-  if (prefill && (!prefill_supported(s) || (reinterpret_cast<uintptr_t>(x) & 15) ||
+  if (prefill && (!prefill_supported(s) || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 15) ||
                   (reinterpret_cast<uintptr_t>(d->w_router) & 15) ||
                   (s.I_shared > 0 && (reinterpret_cast<uintptr_t>(d->w_shared_gate) & 15))))
     return MOE_EINVAL;
@@ -438,7 +438,7 @@ int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y
     ProfScope p(ws, "group", st);
     if ((rc = launch_group(ws->topk_ids, T, s.k, s.E, d->layer, c, ws, st))) return rc;
   }
-  if (prefill) return launch_prefill_experts(d, x, y, y_is_fp32, T, ws, st);
+  if (prefill) return launch_prefill_experts(d, c, x, y, y_is_fp32, T, ws, st);
   {
     ProfScope p(ws, "gateup_decode", st);
     if ((rc = launch_gateup_decode(d, T, ws, st))) return rc;

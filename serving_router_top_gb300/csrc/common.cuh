@@ -239,11 +239,12 @@ struct moe_ws {
   float* h;             // [maxT*k + maxT, max(I, I_shared)] routed entries then shared rows
   float* hmax;          // [maxT*k + maxT] max|h| per row
   int32_t* tile_off;    // [E + 2] prefill: N tiles before each group
-  int32_t* tile_grp;    // [E + maxT*k/256 + 2] prefill: group of each N tile
+  int32_t* tile_grp;    // [E + maxT*k/128 + 2] prefill: group of each N tile
   __half* h16;          // [maxT*k + maxT, max(I, I_shared)] prefill: h as f16 times a per-row power of two
-  __half* xg;           // [maxT*k + maxT, H] prefill: gate/up B rows, f16 x 2^p (in the o region, unused by prefill)
-  float* xinv;          // [maxT*k + maxT] prefill: 2^-p of each xg row
   float* yacc;          // [maxT, H] prefill: fp32 output accumulator
+  __half* xg;           // [maxT*k + maxT, H] prefill: gate/up B rows, f16 x 2^p (in the o region, unused
+                        // by prefill)
+  float* xinv;          // [maxT*k + maxT] prefill: 2^-p of each xg row
   float* part;          // split-K partial tiles: [split_blocks][8 slices][32 lanes][8]
   int* cnt;             // [split_blocks] arrival counters, zero between calls
   size_t split_blocks;

@@ -23,7 +23,8 @@ int launch_gemv_decode(bool gateup, const moe_layer_desc* d, int T, moe_ws* ws, 
 // experts, which write y directly.  x rows must be 16-byte aligned.
 bool prefill_supported(const moe_layer_shape& s);
 int launch_prefill_router(const moe_layer_desc* d, const uint16_t* x, int T, moe_ws* ws, cudaStream_t s);
-int launch_prefill_experts(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T, moe_ws* ws,
+int launch_prefill_experts(const moe_layer_desc* d, const moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
+                           moe_ws* ws,
                            cudaStream_t s);
 
 // Policy.

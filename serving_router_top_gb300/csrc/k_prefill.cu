@@ -12,7 +12,7 @@
 // every product has at most 6 significant bits and magnitude 2^-10 .. 2688 --
 // straight into shared memory in the 128-byte-swizzled K-major layout the
 // tensor core reads (router rows are bf16 already and are copied as they
-// are).  B = up to 256 token rows, one TMA box of 64 columns x 256 rows per
+// are).  B = up to 192 token rows, one TMA box of 64 columns x 192 rows per
 // chunk from a row-major matrix in which every token tile is contiguous: for
 // the router x itself (bf16 like its weights); for gate/up the token rows
 // copied into group order as f16 times a power of two per token (exact for
@@ -23,17 +23,19 @@
 // kind::f16, issued by one thread), read back with tcgen05.ld.
 // The global scale is applied in the epilogue, in fp32.
 //
-// Roles (one persistent CTA per SM, 14 warps):
-//   warps 0-7   producers: copy the raw codes and scales of four chunks at a
-//               time (whole 128-byte lines of the weight rows) with cp.async
-//               into a ring of code groups, then two threads per weight row
-//               dequantise two chunks per step into their A stages (router
-//               rows: cp.async straight into the A stage);
+// Roles (one persistent CTA per SM, 15 warps):
+//   warps 0-7   producers: two threads per weight row dequantise two chunks per
+//               step from the code ring into their A stages (router rows:
+//               cp.async straight into the A stage);
 //   warps 8-11  epilogue: TMEM -> registers -> h / y / logits;
-//   warp  12    TMEM owner (512 columns = two 256-column accumulators) and
+//   warp  12    TMEM owner (512 columns: two accumulators of up to 192) and
 //               MMA issuer (one lane);
-//   warp  13    B loader: one TMA box per chunk.
-// Rings of 4 weight (A) and 3 token (B) stages guarded by mbarriers (full:
+//   warp  13    B loader: one TMA box per chunk;
+//   warp  14    code loader: per four chunks, one TMA box (128 bytes of each
+//               of the tile's weight rows) per weight matrix from a 3-D map
+//               over the expert's arena, and the rows' scales with cp.async,
+//               into a ring of two code groups.
+// Rings of 4 weight (A) and 5 token (B) stages guarded by mbarriers (full:
 // one arrival per producer warp; full_b: the loader's expected bytes; empty,
 // empty_b: tcgen05.commit) feed the MMAs; the two accumulators (acc_full:
 // commit; acc_empty: one arrival per epilogue warp) let the epilogue of one
@@ -42,27 +44,32 @@
 // is freed.
 #include <cudaTypedefs.h>
 
+#include <cstring>
+
 #include "internal.h"
 
 namespace moe {
 namespace prefill {
 
 constexpr int kBK = 64;           // K per stage (one 128-byte swizzle atom of bf16)
-constexpr int kNT = 256;          // tokens per tile (accumulator columns)
+constexpr int kNT = 192;          // tokens per tile (accumulator columns)
+constexpr int kAccCols = 256;     // TMEM columns between the two accumulators (512 allocated)
 constexpr int kAStages = 4;  // dequantised weight tiles
-constexpr int kBStages = 3;  // token tiles
-constexpr int kProducers = 256;  // eight warps, two threads per weight row
+constexpr int kBStages = 5;  // token tiles
+constexpr int kBPrefetch = 4;  // token tiles prefetched into L2 beyond the ring
+constexpr int kProducers = 512;  // two groups of eight warps, two threads per weight row in each
 constexpr int kGChunks = 4;      // chunks per code group: one 128-byte line of every weight row
-constexpr int kGStages = 3;      // code groups in flight
+constexpr int kGStages = 2;      // code groups in flight
 constexpr int kGCodeBytes = 128 * 128;  // raw codes of a group: [128 rows][128 B], 16-byte pieces swizzled
 constexpr int kGScaleBytes = 128 * 16;  // raw scales of a group: [128 rows][16 B]
 constexpr int kEpi = 128;
-constexpr int kThreads = kProducers + kEpi + 64;
+constexpr int kThreads = kProducers + kEpi + 96;
 constexpr int kMmaWarp = (kProducers + kEpi) / 32;
 constexpr int kLoadWarp = kMmaWarp + 1;
+constexpr int kCodeWarp = kMmaWarp + 2;
 constexpr int kABytes = 128 * kBK * 2;   // 16 KB
-constexpr int kBBytes = kNT * kBK * 2;   // 32 KB
-constexpr int kBarriers = 2 * kAStages + 2 * kBStages + kGStages + 2 + 2 + 1;
+constexpr int kBBytes = kNT * kBK * 2;   // 24 KB
+constexpr int kBarriers = 2 * kAStages + 2 * kBStages + 2 * kGStages + 2 + 2 + 1;
 constexpr size_t kSmemBytes = size_t(kAStages) * kABytes + size_t(kBStages) * kBBytes +
                               size_t(kGStages) * (kGCodeBytes + kGScaleBytes) + kBarriers * 8 + 8 + 2 * kNT * 8 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -119,6 +126,14 @@ __device__ __forceinline__ void tile_load(void* dst, const CUtensorMap* tm, int 
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(row), "r"(su32(b))
       : "memory");
 }
+// Box of the 3-D tensor behind `tm` at (x, y, z) -> dst; completion counted on b.
+__device__ __forceinline__ void tile_load3(void* dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* b) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(su32(b))
+      : "memory");
+}
 __device__ __forceinline__ void commit_to(uint64_t* b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b))
                : "memory");
@@ -142,14 +157,23 @@ __device__ __forceinline__ void cp_wait() {
 __device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpi) : "memory"); }
 
+// Raw-code tensor maps of the expert GEMMs: [cache slots, staging slots, shared
+// expert][weight matrix of the tile: gate, up (gate/up GEMM) or down].
+struct CodeMaps {
+  CUtensorMap m[3][2];
+};
+
 struct Args {
+  CodeMaps cmaps;            // expert GEMMs: raw codes, one 3-D map per arena and matrix
   const int32_t* num_groups;
   const int32_t* grp_off;
   const uint8_t* const* grp_blob;
   const int32_t* ent_tok;
   const int32_t* ent_pos;
   const int32_t* tile_off;
-  const int32_t* tile_grp;   // [G+1] N tiles before each group
+  const int32_t* tile_grp;
+  const int32_t* grp_src;    // MOE_SRC_RESIDENT (cache slot) or MOE_SRC_STAGED (staging slot)
+  const int32_t* grp_slot;   // [G+1] N tiles before each group
   float* h;                  // gate/up output h (fp32) [maxTk + maxT, Imax]
   float* hmax;               // down: max|h| per row [maxTk + maxT]
   const float* xinv;         // gate/up: inverse power of two of each B row [maxTk + maxT]
@@ -170,6 +194,7 @@ struct Args {
 struct Item {
   const uint8_t* blob;
   int shared, nt, mt, n, e0, C, KC;
+  int g;  // routed: the group; -1 otherwise
 };
 
 // Work list of one GEMM: (routed N tile, M tile) pairs in group order (M tile
@@ -209,10 +234,12 @@ __device__ __forceinline__ void item_of(const Args& a, const Sched& sc, int it, 
     x.n = min(kNT, a.T - x.nt * kNT);
     x.blob = nullptr;
     x.C = a.H;
+    x.g = -1;
   } else if (it < sc.routed_tiles * sc.mt_r) {
     const int ti = it / sc.mt_r;
     x.mt = it - ti * sc.mt_r;
     const int lo = a.tile_grp[ti];
+    x.g = lo;
     x.nt = ti - a.tile_off[lo];
     x.shared = 0;
     x.e0 = a.grp_off[lo];
@@ -228,6 +255,7 @@ __device__ __forceinline__ void item_of(const Args& a, const Sched& sc, int it, 
     x.n = min(kNT, a.T - x.nt * kNT);
     x.blob = a.shared_blob;
     x.C = MODE == kGateUp ? a.H : a.I_s;
+    x.g = -1;
   }
   x.KC = x.C / kBK;
 }
@@ -314,7 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
   uint64_t* full_b = empty + kAStages;    // [kBStages]
   uint64_t* empty_b = full_b + kBStages;  // [kBStages]
   uint64_t* gfull = empty_b + kBStages;   // [kGStages]
-  uint64_t* acc_full = gfull + kGStages;  // [2]
+  uint64_t* gempty = gfull + kGStages;    // [kGStages]
+  uint64_t* acc_full = gempty + kGStages; // [2]
   uint64_t* acc_empty = acc_full + 2;     // [2]
   uint64_t* drain = acc_empty + 2;
   uint32_t* taddr_s = reinterpret_cast<uint32_t*>(drain + 1);
@@ -326,19 +355,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
 
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(taddr_s)),
-                 "r"(2 * kNT));
+                 "r"(2 * kAccCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
     for (int s = 0; s < kAStages; ++s) {
-      bar_init(&full[s], kProducers / 32);  // one arrival per producer warp
+      bar_init(&full[s], kProducers / 64);  // one arrival per warp of the producer group writing it
       bar_init(&empty[s], 1);
     }
     for (int s = 0; s < kBStages; ++s) {
       bar_init(&full_b[s], 1);
       bar_init(&empty_b[s], 1);
     }
-    for (int g = 0; g < kGStages; ++g) bar_init(&gfull[g], kProducers);  // every producer's copies
+    for (int g = 0; g < kGStages; ++g) {
+      bar_init(&gfull[g], 33);               // the code loader: expected bytes + each lane's scale copies
+      bar_init(&gempty[g], kProducers / 32);  // one arrival per producer warp
+    }
     for (int b = 0; b < 2; ++b) {
       bar_init(&acc_full[b], 1);
       bar_init(&acc_empty[b], kEpi / 32);  // one arrival per epilogue warp
@@ -356,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int q = 0, done = 0;
+      uint32_t ready = 0;  // bits: the next pair's A and B stages (1, 2: first chunk; 4, 8: second) seen full
       for (int it = blockIdx.x; it < sc.n_items && !failed; it += gridDim.x, ++done) {
         Item x;
         item_of<MODE>(a, sc, it, x);
@@ -370,25 +403,66 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
           failed = true;
           break;
         }
-        const uint32_t dt = taddr + uint32_t(buf * kNT);
-        for (int kc = 0; kc < x.KC; ++kc, ++q) {
-          const int s = q % kAStages, sb = q % kBStages;
-          if (!bar_wait(&full[s], (q / kAStages) & 1) || !bar_wait(&full_b[sb], (q / kBStages) & 1)) {
+        const uint32_t dt = taddr + uint32_t(buf * kAccCols);
+        // two chunks per step: one block takes a look at the next two chunks'
+        // barriers, issues the eight MMAs of these two, commits their stages
+        // free, and only then reads the looks' results, so the barrier
+        // round trips pass while the MMAs are issued
+        for (int kc = 0; kc < x.KC; kc += 2, q += 2) {
+          const bool two = kc + 1 < x.KC;  // an odd last chunk goes alone (its partner slot repeats it)
+          const int q1 = two ? q + 1 : q;
+          const int s0 = q % kAStages, b0 = q % kBStages, s1 = q1 % kAStages, b1 = q1 % kBStages;
+          if ((!(ready & 1) && !bar_wait(&full[s0], (q / kAStages) & 1)) ||
+              (!(ready & 2) && !bar_wait(&full_b[b0], (q / kBStages) & 1)) ||
+              (!(ready & 4) && !bar_wait(&full[s1], (q1 / kAStages) & 1)) ||
+              (!(ready & 8) && !bar_wait(&full_b[b1], (q1 / kBStages) & 1))) {
             failed = true;
             break;
           }
           asm volatile("tcgen05.fence::after_thread_sync;");
-          const uint64_t da = kmajor_desc(sA + s * kABytes), db = kmajor_desc(sB + sb * kBBytes);
-#pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint32_t accum = (kc > 0 || k > 0) ? 1u : 0u;
-            asm volatile(
-                "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dt),
-                "l"(da + uint64_t(k * 2)), "l"(db + uint64_t(k * 2)), "r"(idesc), "r"(accum));
-          }
-          commit_to(&empty[s]);
-          commit_to(&empty_b[sb]);
+          const uint64_t da0 = kmajor_desc(sA + s0 * kABytes), db0 = kmajor_desc(sB + b0 * kBBytes);
+          const uint64_t da1 = kmajor_desc(sA + s1 * kABytes), db1 = kmajor_desc(sB + b1 * kBBytes);
+          // the pair after this one, in the global chunk order
+          const int n0 = q + (two ? 2 : 1), n1 = n0 + 1;
+          const uint32_t acc0 = kc > 0 ? 1u : 0u;
+          const uint32_t two_u = two ? 1u : 0u;
+          uint32_t r0, r1, r2, r3;
+          asm volatile(
+              "{\n\t.reg .pred t0, t1, t2, t3, p0, p1, pt;\n\t"
+              "mbarrier.test_wait.parity.shared::cta.b64 t0, [%6], %7;\n\t"
+              "mbarrier.test_wait.parity.shared::cta.b64 t1, [%8], %9;\n\t"
+              "mbarrier.test_wait.parity.shared::cta.b64 t2, [%10], %11;\n\t"
+              "mbarrier.test_wait.parity.shared::cta.b64 t3, [%12], %13;\n\t"
+              "setp.ne.u32 p0, %14, 0;\n\t"
+              "setp.eq.u32 p1, %14, %14;\n\t"
+              "setp.ne.u32 pt, %15, 0;\n\t"
+              "tcgen05.mma.cta_group::1.kind::f16 [%4], %16, %17, %5, p0;\n\t"
+              "tcgen05.mma.cta_group::1.kind::f16 [%4], %18, %19, %5, p1;\n\t"
+              "tcgen05.mma.cta_group::1.kind::f16 [%4], %20, %21, %5, p1;\n\t"
+              "tcgen05.mma.cta_group::1.kind::f16 [%4], %22, %23, %5, p1;\n\t"
+              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%24];\n\t"
+              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%25];\n\t"
+              "@pt tcgen05.mma.cta_group::1.kind::f16 [%4], %26, %27, %5, p1;\n\t"
+              "@pt tcgen05.mma.cta_group::1.kind::f16 [%4], %28, %29, %5, p1;\n\t"
+              "@pt tcgen05.mma.cta_group::1.kind::f16 [%4], %30, %31, %5, p1;\n\t"
+              "@pt tcgen05.mma.cta_group::1.kind::f16 [%4], %32, %33, %5, p1;\n\t"
+              "@pt tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%34];\n\t"
+              "@pt tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%35];\n\t"
+              "selp.u32 %0, 1, 0, t0;\n\t"
+              "selp.u32 %1, 2, 0, t1;\n\t"
+              "selp.u32 %2, 4, 0, t2;\n\t"
+              "selp.u32 %3, 8, 0, t3;\n\t}"
+              : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+              : "r"(dt), "r"(idesc), "r"(su32(&full[n0 % kAStages])), "r"(uint32_t((n0 / kAStages) & 1)),
+                "r"(su32(&full_b[n0 % kBStages])), "r"(uint32_t((n0 / kBStages) & 1)),
+                "r"(su32(&full[n1 % kAStages])), "r"(uint32_t((n1 / kAStages) & 1)),
+                "r"(su32(&full_b[n1 % kBStages])), "r"(uint32_t((n1 / kBStages) & 1)), "r"(acc0), "r"(two_u),
+                "l"(da0), "l"(db0), "l"(da0 + 2), "l"(db0 + 2), "l"(da0 + 4), "l"(db0 + 4), "l"(da0 + 6), "l"(db0 + 6),
+                "r"(su32(&empty[s0])), "r"(su32(&empty_b[b0])), "l"(da1), "l"(db1), "l"(da1 + 2), "l"(db1 + 2),
+                "l"(da1 + 4), "l"(db1 + 4), "l"(da1 + 6), "l"(db1 + 6), "r"(su32(&empty[s1])), "r"(su32(&empty_b[b1]))
+              : "memory");
+          ready = r0 | r1 | r2 | r3;
+          if (!two) --q;  // the loop adds two; a lone last chunk counts one
         }
         if (!failed) commit_to(&acc_full[buf]);
       }
@@ -399,7 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
     }
   } else if (warp < kProducers / 32) {
     // ------------------------------------------------------------ producers
-    const int prow = tid >> 1, half = tid & 1;  // this thread's weight row and half of it
+    const int pg = tid >> 8;                                // producer group
+    const int prow = (tid & 255) >> 1, half = tid & 1;      // this thread's weight row and half of it
     // the chunks of this CTA's items, in order: the next one to copy
     int iss_it = blockIdx.x, iss_kc = 0;
     Item ix;
@@ -415,9 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
     if (iss_ok) load_item();
 
     if (MODE == kRouter) {
-      // Router rows are bf16 already: copied straight into the A stage,
-      // kAStages - 1 chunks ahead (into the stage of chunk q - 1, whose MMAs
-      // have run while chunk q was landing).
+      // Router rows are bf16 already: the first producer group copies them
+      // straight into the A stage, kAStages - 1 chunks ahead (into the stage
+      // of chunk q - 1, whose MMAs have run while chunk q was landing).
+      if (pg != 0) iss_ok = false;
       int iss_q = 0;
       auto issue = [&]() {
         if (iss_ok) {
@@ -441,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
       };
       for (int p = 0; p < kAStages - 1; ++p) issue();
       int q = 0;
-      for (int it = blockIdx.x; it < sc.n_items; it += gridDim.x) {
+      for (int it = blockIdx.x; it < sc.n_items && pg == 0; it += gridDim.x) {
         Item x;
         item_of<MODE>(a, sc, it, x);
         for (int kc = 0; kc < x.KC; ++kc, ++q) {
@@ -454,135 +530,101 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
       }
       cp_wait_all();
     } else {
-      // Expert weights come in code groups of kGChunks chunks: one 128-byte
-      // line of each of the tile's 128 weight rows (eight threads per row, so
-      // every request is a whole line) and the rows' 16 scale bytes, copied
-      // with cp.async kGStages groups ahead into a ring whose 16-byte pieces are
-      // swizzled by row; each thread's copies arrive on the group's barrier
-      // when they land.  Chunks are then dequantised two at a time into their
-      // A stages (each free once the MMAs of chunk c - kAStages completed), so
-      // the fixed costs of a step are shared by two chunks.
-      int iss_gi = 0;                  // next group to copy: group iss_gi of item iss_it
-      const uint8_t* crow[4];          // code rows (tid/8 + 32u) of the item being copied
-      const uint8_t* srow = nullptr;   // scale row tid (tid < 128)
-      int rowbytes = 0;
-      auto load_rows = [&]() {
-        for (int u = 0; u < 4; ++u) crow[u] = nullptr;
-        srow = nullptr;
-        rowbytes = ix.C / 2;
-        if (!ix.blob) return;
-        const DevBlobLayout& lay = ix.shared ? a.lay_s : a.lay_r;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          int mat, wrow;
-          a_row<MODE>(ix.mt, (tid >> 3) + 32 * u, mat, wrow);
-          crow[u] = ix.blob + lay.code_off[mat] + size_t(wrow) * rowbytes;
-        }
-        if (tid < 128) {
-          int mat, wrow;
-          a_row<MODE>(ix.mt, tid, mat, wrow);
-          srow = ix.blob + lay.scale_off[mat] + size_t(wrow) * (ix.C / 16);
-        }
-      };
-      if (iss_ok) load_rows();
-      int iss_g = 0;  // groups copied so far
-      auto copy_group = [&]() {
-        if (iss_ok) {
-          const int gs = iss_g % kGStages;
-          const int gbytes = min(128, rowbytes - iss_gi * 128);  // 32 per chunk
-          const int j = tid & 7;
-          if (j * 16 < gbytes) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int r = (tid >> 3) + 32 * u;
-              if (crow[u]) cp16(sG + gs * kGCodeBytes + r * 128 + ((j ^ (r & 7)) << 4), crow[u] + iss_gi * 128 + j * 16);
-            }
-          }
-          if (srow) {
-            uint8_t* d = sGS + gs * kGScaleBytes + tid * 16;
-            const uint8_t* sp = srow + iss_gi * 16;
-            if (gbytes == 128) cp16(d, sp);
-            else if (gbytes == 64) cp8(d, sp);
-            else cp4(d, sp);
-          }
-          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(&gfull[gs])) : "memory");
-          ++iss_g;
-          if (++iss_gi * 128 >= rowbytes) {
-            iss_gi = 0;
-            iss_it += gridDim.x;
-            iss_ok = iss_it < sc.n_items;
-            if (iss_ok) {
-              load_item();
-              load_rows();
-            }
-          }
-        }
-      };
-      for (int g = 0; g < kGStages; ++g) copy_group();
-
-      int c = 0, g = 0;  // chunks and groups consumed
+      // Expert weights arrive in code groups of kGChunks chunks (one 128-byte
+      // line of each of the tile's 128 weight rows, landed by the code loader
+      // in rows of the box order: for gate/up the 64 gate rows, then the 64
+      // up rows).  Producer group pg dequantises chunks 2pg and 2pg+1 of each
+      // code group into their A stages (each free once the MMAs of chunk
+      // c - kAStages completed): the two groups work on neighbouring chunks
+      // at the same time, and a group's fixed costs per step are shared by
+      // two chunks.
+      // the ring row of this thread's tile row (its 128-byte swizzle: grow & 7)
+      const int grow = MODE == kGateUp ? (((prow & 31) >= 16) ? 64 : 0) + (prow >> 5) * 16 + (prow & 15) : prow;
+      int c = 0, g = 0;  // first chunk of the code group; code groups consumed
       for (int it = blockIdx.x; it < sc.n_items; it += gridDim.x) {
         Item x;
         item_of<MODE>(a, sc, it, x);
         for (int c_in = 0; c_in < x.KC; c_in += kGChunks, ++g) {
           const int nch = min(kGChunks, x.KC - c_in);
           const int gs = g % kGStages;
+          const int kk = 2 * pg;                   // this group's first chunk in the code group
+          const int mine = max(0, min(2, nch - kk));  // chunks it dequantises: 0, 1 or 2 (warp-uniform)
           if (!failed && !bar_wait(&gfull[gs], (g / kGStages) & 1)) failed = true;
-          for (int kk = 0; kk < nch;) {
-            const bool two = kk + 1 < nch;
-            const int s0 = c % kAStages, s1 = (c + 1) % kAStages;
+          const int c0 = c + kk;
+          const bool two = mine == 2;
+          const int s0 = c0 % kAStages, s1 = (c0 + 1) % kAStages;
+          if (mine > 0) {
             // A stages free: both looks issued before either result is needed
             if (!failed) {
-              const bool w0 = c >= kAStages, w1 = two && c + 1 >= kAStages;
-              const uint32_t p0 = ((c / kAStages) - 1) & 1, p1 = (((c + 1) / kAStages) - 1) & 1;
+              const bool w0 = c0 >= kAStages, w1 = two && c0 + 1 >= kAStages;
+              const uint32_t p0 = ((c0 / kAStages) - 1) & 1, p1 = (((c0 + 1) / kAStages) - 1) & 1;
               const bool f0 = !w0 || bar_test(&empty[s0], p0);
               const bool f1 = !w1 || bar_test(&empty[s1], p1);
               if ((!f0 && !bar_wait(&empty[s0], p0)) || (!f1 && !bar_wait(&empty[s1], p1))) failed = true;
             }
             failed = __any_sync(0xffffffffu, failed);  // warp-uniform
             if (!failed && x.blob) {
-              const uint8_t* gc = sG + gs * kGCodeBytes + prow * 128;
-              const uint8_t* gsc = sGS + gs * kGScaleBytes + prow * 16;
-              const int j0 = 2 * kk + half, j1 = 2 * (kk + 1) + half;  // this thread's pieces
-              const uint4 c0 = *reinterpret_cast<const uint4*>(gc + ((j0 ^ (prow & 7)) << 4));
+              const uint8_t* gc = sG + gs * kGCodeBytes + grow * 128;
+              const uint8_t* gsc = sGS + gs * kGScaleBytes + grow * 16;
+              const int j0 = 2 * kk + half, j1 = 2 * (kk + 1) + half;  // this thread's 16-byte pieces
+              const uint4 cw0 = *reinterpret_cast<const uint4*>(gc + ((j0 ^ (grow & 7)) << 4));
               const uint32_t sc0 = *reinterpret_cast<const uint32_t*>(gsc + kk * 4);
-              uint4 c1 = make_uint4(0u, 0u, 0u, 0u);
+              uint4 cw1 = make_uint4(0u, 0u, 0u, 0u);
               uint32_t sc1 = 0u;
               if (two) {
-                c1 = *reinterpret_cast<const uint4*>(gc + ((j1 ^ (prow & 7)) << 4));
+                cw1 = *reinterpret_cast<const uint4*>(gc + ((j1 ^ (grow & 7)) << 4));
                 sc1 = *reinterpret_cast<const uint32_t*>(gsc + (kk + 1) * 4);
               }
-              dequant_half(c0, sc0, half, sA + s0 * kABytes, prow);
-              if (two) dequant_half(c1, sc1, half, sA + s1 * kABytes, prow);
+              dequant_half(cw0, sc0, half, sA + s0 * kABytes, prow);
+              if (two) dequant_half(cw1, sc1, half, sA + s1 * kABytes, prow);
             }
             // every thread's shared-memory writes are made visible to the
-            // tensor core (async proxy); after the warp has synchronised, one
-            // lane arrives for each chunk
+            // tensor core (async proxy) before one lane of the synchronised
+            // warp arrives for each chunk
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) {
-              bar_arrive(&full[s0]);
-              if (two) bar_arrive(&full[s1]);
-            }
-            kk += two ? 2 : 1;
-            c += two ? 2 : 1;
           }
-          // every producer is done with the group's ring stage before it is refilled
-          asm volatile("bar.sync 2, %0;" ::"n"(kProducers) : "memory");
-          copy_group();
+          __syncwarp();
+          if (lane == 0) {
+            if (mine > 0) bar_arrive(&full[s0]);
+            if (two) bar_arrive(&full[s1]);
+            bar_arrive(&gempty[gs]);  // the warp is done with the code group
+          }
+          c += nch;
         }
       }
-      cp_wait_all();
     }
     if (failed) set_error(a.err, MOE_ETIMEOUT);
   } else if (warp == kLoadWarp) {
     // ------------------------------------------------------------ B loader
+    // Token tiles are contiguous rows: one box per chunk into the B ring
+    // (columns past n hold other rows or zeros and are never read back), and
+    // an L2 prefetch of the box kBPrefetch chunks further on, so that the load
+    // into a freshly freed stage finds its rows in L2.
     int q = 0;
+    int pf_it = blockIdx.x, pf_kc = 0;  // the chunk to prefetch next
+    Item px;
+    bool pf_ok = pf_it < sc.n_items;
+    if (pf_ok) item_of<MODE>(a, sc, pf_it, px);
+    auto prefetch_next = [&]() {
+      if (!pf_ok) return;
+      if (lane == 0) {
+        const CUtensorMap* tm = px.shared ? &tm_s : &tm_r;
+        asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                         reinterpret_cast<uint64_t>(tm)),
+                     "r"(pf_kc * kBK), "r"(b_row0<MODE>(a, px))
+                     : "memory");
+      }
+      if (++pf_kc == px.KC) {
+        pf_kc = 0;
+        pf_it += gridDim.x;
+        pf_ok = pf_it < sc.n_items;
+        if (pf_ok) item_of<MODE>(a, sc, pf_it, px);
+      }
+    };
+    for (int p = 0; p < kBStages + kBPrefetch; ++p) prefetch_next();
     for (int it = blockIdx.x; it < sc.n_items && !failed; it += gridDim.x) {
       Item x;
       item_of<MODE>(a, sc, it, x);
-      // token tiles are contiguous rows: one 32 KB box per chunk (columns past
-      // n hold other rows or zeros and are never read back)
       const CUtensorMap* tm = x.shared ? &tm_s : &tm_r;
       const int row0 = b_row0<MODE>(a, x);
       for (int kc = 0; kc < x.KC; ++kc, ++q) {
@@ -595,12 +637,79 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
           tile_load(sB + s * kBBytes, tm, kc * kBK, row0, &full_b[s]);
         }
         __syncwarp();
+        prefetch_next();
       }
     }
     // the copies of the last stages have landed before the CTA can leave
     for (int qq = q > kBStages ? q - kBStages : 0; qq < q; ++qq)
       if (!bar_wait(&full_b[qq % kBStages], (qq / kBStages) & 1)) failed = true;
     if (failed && lane == 0) set_error(a.err, MOE_ETIMEOUT);
+  } else if (warp == kCodeWarp) {
+    // ------------------------------------------------------------ code loader
+    // Per code group: one TMA box (128 bytes x 64 or 128 rows) of raw codes per
+    // weight matrix of the tile from the 3-D map of the expert's arena (cache
+    // slots, staging slots or the shared expert), and the rows' scale bytes
+    // with cp.async, four rows per lane.
+    if (MODE != kRouter) {
+      int g = 0;
+      for (int it = blockIdx.x; it < sc.n_items && !failed; it += gridDim.x) {
+        Item x;
+        item_of<MODE>(a, sc, it, x);
+        int arena = 2, slot = 0;  // shared expert
+        if (!x.shared) {
+          arena = a.grp_src[x.g] == MOE_SRC_STAGED ? 1 : 0;
+          slot = max(a.grp_slot[x.g], 0);
+        }
+        const DevBlobLayout& lay = x.shared ? a.lay_s : a.lay_r;
+        const uint8_t* srow[4];  // scale rows lane + 32u, in box order
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int r = lane + 32 * u;
+          int mat, wrow;
+          if (MODE == kGateUp) {
+            mat = r >= 64 ? 1 : 0;
+            wrow = x.mt * 64 + (r & 63);
+          } else {
+            mat = 2;
+            wrow = x.mt * 128 + r;
+          }
+          srow[u] = x.blob ? x.blob + lay.scale_off[mat] + size_t(wrow) * (x.C / 16) : nullptr;
+        }
+        const int rowbytes = x.C / 2;
+        for (int gi = 0; gi * 128 < rowbytes; ++gi, ++g) {
+          const int gs = g % kGStages;
+          if (g >= kGStages && !bar_wait(&gempty[gs], ((g / kGStages) - 1) & 1)) failed = true;
+          failed = __any_sync(0xffffffffu, failed);
+          if (failed) break;
+          if (lane == 0) {
+            expect_tx(&gfull[gs], kGCodeBytes);
+            uint8_t* dst = sG + gs * kGCodeBytes;
+            if (MODE == kGateUp) {
+              tile_load3(dst, &a.cmaps.m[arena][0], gi * 128, x.mt * 64, slot, &gfull[gs]);
+              tile_load3(dst + 64 * 128, &a.cmaps.m[arena][1], gi * 128, x.mt * 64, slot, &gfull[gs]);
+            } else {
+              tile_load3(dst, &a.cmaps.m[arena][0], gi * 128, x.mt * 128, slot, &gfull[gs]);
+            }
+          }
+          const int gbytes = min(128, rowbytes - gi * 128);  // 32 per chunk
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (!srow[u]) continue;
+            uint8_t* d = sGS + gs * kGScaleBytes + (lane + 32 * u) * 16;
+            const uint8_t* sp = srow[u] + gi * 16;
+            if (gbytes == 128) cp16(d, sp);
+            else if (gbytes == 64) cp8(d, sp);
+            else cp4(d, sp);
+          }
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(&gfull[gs])) : "memory");
+        }
+      }
+      // every copy has landed before the CTA can leave
+      cp_wait_all();
+      for (int gg = g > kGStages ? g - kGStages : 0; gg < g; ++gg)
+        if (!bar_wait(&gfull[gg % kGStages], (gg / kGStages) & 1)) failed = true;
+      if (failed && lane == 0) set_error(a.err, MOE_ETIMEOUT);
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int et = tid - kProducers, qw = warp & 3;
@@ -642,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
       const float gs0 = x.blob ? reinterpret_cast<const BlobHeader*>(x.blob)->gscale[MODE == kGateUp ? 0 : 2] : 0.f;
       const float gs1 = x.blob ? reinterpret_cast<const BlobHeader*>(x.blob)->gscale[1] : 0.f;
       const int npad = (x.n + 15) & ~15;
-      const uint32_t tb = taddr + uint32_t(buf * kNT) + (uint32_t(qw * 32) << 16);
+      const uint32_t tb = taddr + uint32_t(buf * kAccCols) + (uint32_t(qw * 32) << 16);
       const int row = x.mt * 128 + qw * 32 + lane;  // router / down: output row of this lane
       const float rbias = (MODE == kRouter && a.bias && row < a.E) ? a.bias[row] : 0.f;
       // gate/up: h row of column 0 of this tile and this lane's intermediate
@@ -651,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
         hcol = a.h + size_t(x.shared ? a.maxTk + x.nt * kNT : x.e0 + x.nt * kNT) * a.Imax + x.mt * 64 + qw * 16 +
                (lane & 15);
       // 32 accumulator columns per TMEM load (columns past npad are read and
-      // ignored: the 256 columns of the buffer are all allocated)
+      // ignored: the buffer's 256 columns are all allocated)
       for (int c0 = 0; c0 < npad && !failed; c0 += 32) {
         uint32_t v[32];
         asm volatile(
@@ -680,6 +789,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
             }
           }
         } else if (MODE == kDown) {
+          // y[token] += w x o_e (fp32 atomic adds in L2: a token's k + 1
+          // terms come from different CTAs); a missing expert adds nothing
           if (x.blob) {
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
@@ -712,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
   __syncthreads();
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.fence::after_thread_sync;");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(2 * kNT));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(2 * kAccCols));
   }
 }
 
@@ -904,6 +1015,60 @@ static int encode_rows(CUtensorMap* tm, const void* base, int cols, int rows) {
 
 // B of routed tiles from [r_rows, cols] at r_base, of shared-expert tiles from
 // [s_rows, cols] at s_base.
+// Map of the raw codes of one weight matrix in n blobs spaced `stride` bytes
+// apart (a cache arena, or one blob): [n][rows][rowbytes] bytes, boxes of
+// 128 bytes (four chunks of a row) x boxrows rows, 128-byte swizzle.
+static int encode_codes(CUtensorMap* tm, const uint8_t* base, int rowbytes, int rows, int n, size_t stride,
+                        int boxrows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return MOE_ECUDA;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || rowbytes % 16 || stride % 16 || n <= 0 || rows <= 0) return MOE_ECUDA;
+  const cuuint64_t dims[3] = {cuuint64_t(rowbytes), cuuint64_t(rows), cuuint64_t(n)};
+  const cuuint64_t strides[2] = {cuuint64_t(rowbytes), cuuint64_t(stride)};
+  const cuuint32_t box[3] = {128, cuuint32_t(boxrows), 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  if (encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MOE_ECUDA;
+  return MOE_OK;
+}
+
+// The raw-code maps of a GEMM over the cache arenas and the shared expert.
+static int code_maps(prefill::CodeMaps* cm, bool gateup, const moe_layer_desc* d, const moe_cache* c) {
+  using namespace prefill;
+  std::memset(cm, 0, sizeof(*cm));
+  const moe_layer_shape& sh = d->s;
+  const int nmat = gateup ? 2 : 1;
+  for (int i = 0; i < nmat; ++i) {
+    const int mat = gateup ? i : 2;
+    const DevBlobLayout lr = dev_layout(sh.H, sh.I);
+    const int rowbytes = (gateup ? sh.H : sh.I) / 2, rows = gateup ? sh.I : sh.H, boxrows = gateup ? 64 : 128;
+    int rc;
+    if (c->nslots > 0 &&
+        (rc = encode_codes(&cm->m[0][i], c->slots + lr.code_off[mat], rowbytes, rows, c->nslots, c->blob_bytes, boxrows)))
+      return rc;
+    if (c->nstaging > 0 && (rc = encode_codes(&cm->m[1][i], c->staging + lr.code_off[mat], rowbytes, rows,
+                                              c->nstaging, c->blob_bytes, boxrows)))
+      return rc;
+    if (sh.I_shared > 0 && d->shared_blob) {
+      const DevBlobLayout ls = dev_layout(sh.H, sh.I_shared);
+      const int srb = (gateup ? sh.H : sh.I_shared) / 2, srows = gateup ? sh.I_shared : sh.H;
+      if ((rc = encode_codes(&cm->m[2][i], static_cast<const uint8_t*>(d->shared_blob) + ls.code_off[mat], srb, srows,
+                             1, (size_t(srb) * srows + 15) & ~size_t(15), boxrows)))
+        return rc;
+    }
+  }
+  return MOE_OK;
+}
+
 template <int MODE>
 static int launch_gemm(const prefill::Args& a, const void* r_base, int r_rows, const void* s_base, int s_rows, int cols,
                        cudaStream_t s) {
@@ -938,6 +1103,8 @@ static prefill::Args base_args(const moe_layer_desc* d, int T, moe_ws* ws) {
   a.ent_pos = ws->ent_pos;
   a.tile_off = ws->tile_off;
   a.tile_grp = ws->tile_grp;
+  a.grp_src = ws->grp_src;
+  a.grp_slot = ws->grp_slot;
   a.h = ws->h;
   a.hmax = ws->hmax;
   a.xinv = ws->xinv;
@@ -971,7 +1138,8 @@ int launch_prefill_router(const moe_layer_desc* d, const uint16_t* x, int T, moe
 // The expert part of a prefill call: tiles, gate/up GEMM (h), max|h| per row
 // and h -> f16 times a per-row power of two, down GEMM accumulating w*o
 // into an fp32 buffer, and the output cast.
-int launch_prefill_experts(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T, moe_ws* ws,
+int launch_prefill_experts(const moe_layer_desc* d, const moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
+                           moe_ws* ws,
                            cudaStream_t s) {
   using namespace prefill;
   const moe_layer_shape& sh = d->s;
@@ -997,6 +1165,7 @@ int launch_prefill_experts(const moe_layer_desc* d, const uint16_t* x, void* y, 
   int rc;
   {
     ProfScope p(ws, "gateup_gemm", s);
+    if ((rc = code_maps(&a.cmaps, true, d, c))) return rc;
     if ((rc = launch_gemm<kGateUp>(a, ws->xg, a.maxTk + ws->maxT, ws->xg, a.maxTk + ws->maxT, sh.H, s))) return rc;
   }
   {
@@ -1007,6 +1176,7 @@ int launch_prefill_experts(const moe_layer_desc* d, const uint16_t* x, void* y, 
   }
   {
     ProfScope p(ws, "down_gemm", s);
+    if ((rc = code_maps(&a.cmaps, false, d, c))) return rc;
     if ((rc = launch_gemm<kDown>(a, ws->h16, a.maxTk + ws->maxT, ws->h16, a.maxTk + ws->maxT, a.Imax, s))) return rc;
   }
   if (!y_is_fp32) {
