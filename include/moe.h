@@ -235,6 +235,24 @@ int moe_group(const int32_t* topk_ids, int T, int k, int E, int layer, moe_cache
 int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T, moe_cache* c,
                       moe_ws* ws, int mode, moe_stream_t stream);
 
+/* The prefill forward with the layer's routed experts streamed through the
+ * staging pool (Strata expert paths, "PCIe 搬运怎样与计算重叠？": the copy stream
+ * fills a staging slot and records `copied`, the compute stream waits on it,
+ * computes and records `used`, and the copy stream waits on `used` before it
+ * overwrites the slot).  The residency and staging tables are not consulted:
+ * experts e in [u*U, u*U + U) form unit u; copy_stream copies their blobs
+ * (one cudaMemcpyAsync of n*blob_bytes per unit, n <= U, from the cache's
+ * backing pool, device or pinned host) into staging slots (u % 2)*U ..; stream
+ * runs the grouped GEMMs of that unit's groups once they have landed.  The
+ * shared expert runs with unit 0.  Same arguments, layout and result as
+ * moe_layer_forward in prefill mode, plus: U >= 1 with 2*U <= the cache's
+ * staging slots, a backing pool, and copy_stream a stream other than stream,
+ * else MOE_EINVAL.  Both streams may be used again as soon as the call
+ * returns; the staging slots' contents and table entries are left undefined
+ * for lookups (the staging table itself is not changed). */
+int moe_layer_forward_streamed(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T,
+                               moe_cache* c, moe_ws* ws, int U, moe_stream_t stream, moe_stream_t copy_stream);
+
 /* Heat update (Strata page, "哪些专家能长期留在显存？": accumulate how often
  * each expert is routed to): heat[layer*E+e] = fl32(heat + (float)count_e)
  * with count_e the number of (token, rank) selections of e in topk_ids

@@ -131,6 +131,7 @@ int moe_cache_create(moe_cache** out, int L, int E, int H, int I, int nslots, in
   if (ok && nstaging > 0) ok = cudaMalloc(&c->staging, size_t(nstaging) * c->blob_bytes) == cudaSuccess;
   if (ok) ok = cudaEventCreateWithFlags(&c->ev_unmapped, cudaEventDisableTiming) == cudaSuccess &&
                cudaEventCreateWithFlags(&c->ev_copied, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; ok && i < 5; ++i) ok = cudaEventCreateWithFlags(&c->ev_ring[i], cudaEventDisableTiming) == cudaSuccess;
   if (ok)
     ok = cudaMemset(c->resid, 0xff, LE * 4) == cudaSuccess && cudaMemset(c->stage, 0xff, LE * 4) == cudaSuccess &&
          cudaMemset(c->heat, 0, LE * 4) == cudaSuccess &&
@@ -160,6 +161,8 @@ int moe_cache_destroy(moe_cache* c) {
   cudaFree(c->staging);
   if (c->ev_unmapped) cudaEventDestroy(c->ev_unmapped);
   if (c->ev_copied) cudaEventDestroy(c->ev_copied);
+  for (int i = 0; i < 5; ++i)
+    if (c->ev_ring[i]) cudaEventDestroy(c->ev_ring[i]);
   free(c);
   return MOE_OK;
 }
@@ -272,6 +275,7 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   const size_t o_part = cv.take<float>(split_blocks * 8 * 32 * 8);
   const size_t o_toff = cv.take<int32_t>(size_t(s.E) + 2);
   const size_t o_tgrp = cv.take<int32_t>(size_t(s.E) + Tk / 128 + 2);
+  const size_t o_grange = cv.take<int32_t>(2 * size_t(s.E) + 2);
   const size_t o_h16 = cv.take<__half>((Tk + maxT) * Imax);
   const size_t o_yacc = cv.take<float>(size_t(maxT) * s.H);
   const size_t o_cnt = cv.take<int>(split_blocks);
@@ -303,6 +307,7 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   w->part = reinterpret_cast<float*>(base + o_part);
   w->tile_off = reinterpret_cast<int32_t*>(base + o_toff);
   w->tile_grp = reinterpret_cast<int32_t*>(base + o_tgrp);
+  w->grange = reinterpret_cast<int32_t*>(base + o_grange);
   w->h16 = reinterpret_cast<__half*>(base + o_h16);
   w->yacc = reinterpret_cast<float*>(base + o_yacc);
   w->xg = reinterpret_cast<__half*>(base + o_o);  // (Tk+maxT)*H 16-bit values fit in (Tk+maxT)*H floats
@@ -399,6 +404,47 @@ int moe_group(const int32_t* topk_ids, int T, int k, int E, int layer, moe_cache
     return MOE_EINVAL;
   if (T == 0) return MOE_OK;
   return launch_group(topk_ids, T, k, E, layer, c, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Argument checks shared by the forward calls; MOE_OK when they pass.
+static int forward_args_ok(const moe_layer_desc* d, const uint16_t* x, void* y, int T, const moe_cache* c,
+                           const moe_ws* ws, bool prefill) {
+  if (!d || !x || !y || !c || !ws || !d->w_router) return MOE_EINVAL;
+  const moe_layer_shape& s = d->s;
+  if (!shape_ok(s) || T < 0 || T > ws->maxT || s.H != ws->s.H || s.k != ws->s.k || s.E != ws->s.E ||
+      s.I > ws->s.I || s.I_shared > ws->s.I_shared || s.E != c->E || s.H != c->H || s.I != c->I || d->layer < 0 ||
+      d->layer >= c->L)
+    return MOE_EINVAL;
+  if (s.I_shared > 0 && (!d->shared_blob || !d->w_shared_gate)) return MOE_EINVAL;
+  if (prefill && (!prefill_supported(s) || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 15) ||
+                  (reinterpret_cast<uintptr_t>(d->w_router) & 15) ||
+                  (s.I_shared > 0 && (reinterpret_cast<uintptr_t>(d->w_shared_gate) & 15))))
+    return MOE_EINVAL;
+  return MOE_OK;
+}
+
+int moe_layer_forward_streamed(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T,
+                               moe_cache* c, moe_ws* ws, int U, moe_stream_t stream, moe_stream_t copy_stream) {
+  int rc;
+  if ((rc = forward_args_ok(d, x, y, T, c, ws, true))) return rc;
+  if (U < 1 || 2 * U > c->nstaging || !c->backing || !copy_stream || copy_stream == stream) return MOE_EINVAL;
+  if (T == 0) return MOE_OK;
+  const moe_layer_shape& s = d->s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ws->prof_n = 0;
+  {
+    ProfScope p(ws, "router", st);
+    if ((rc = launch_prefill_router(d, x, T, ws, st))) return rc;
+  }
+  {
+    ProfScope p(ws, "topk", st);
+    if ((rc = launch_topk(ws->logits, T, s.E, s.k, ws->topk_ids, ws->topk_w, ws->error, st))) return rc;
+  }
+  {
+    ProfScope p(ws, "group", st);
+    if ((rc = launch_group(ws->topk_ids, T, s.k, s.E, d->layer, c, ws, st, false))) return rc;
+  }
+  return launch_prefill_streamed(d, c, x, y, y_is_fp32, T, U, ws, st, reinterpret_cast<cudaStream_t>(copy_stream));
 }
 
 int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T, moe_cache* c,

@@ -213,6 +213,7 @@ struct moe_cache {
   void* plan_scratch;
   size_t plan_scratch_bytes;
   cudaEvent_t ev_unmapped, ev_copied;
+  cudaEvent_t ev_ring[5];     // streamed prefill: copied[2], used[2], start
   int next_free_slot, next_free_staging;
 };
 
@@ -240,6 +241,7 @@ struct moe_ws {
   float* hmax;          // [maxT*k + maxT] max|h| per row
   int32_t* tile_off;    // [E + 2] prefill: N tiles before each group
   int32_t* tile_grp;    // [E + maxT*k/128 + 2] prefill: group of each N tile
+  int32_t* grange;      // [2E + 2] streamed prefill: the group range of each unit
   __half* h16;          // [maxT*k + maxT, max(I, I_shared)] prefill: h as f16 times a per-row power of two
   float* yacc;          // [maxT, H] prefill: fp32 output accumulator
   __half* xg;           // [maxT*k + maxT, H] prefill: gate/up B rows, f16 x 2^p (in the o region, unused

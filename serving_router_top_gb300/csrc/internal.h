@@ -9,7 +9,9 @@ int launch_router(const uint16_t* x, const uint16_t* w_router, const float* bias
                   float* xscale = nullptr);
 int launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* err, cudaStream_t s);
 
-int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws, cudaStream_t s);
+// lookup = false: the groups' sources are left for the caller to bind (streamed prefill)
+int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws, cudaStream_t s,
+                 bool lookup = true);
 
 // Decode expert path (CUDA-core GEMVs over the slot blobs).
 int launch_gateup_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s);
@@ -24,8 +26,9 @@ int launch_gemv_decode(bool gateup, const moe_layer_desc* d, int T, moe_ws* ws, 
 bool prefill_supported(const moe_layer_shape& s);
 int launch_prefill_router(const moe_layer_desc* d, const uint16_t* x, int T, moe_ws* ws, cudaStream_t s);
 int launch_prefill_experts(const moe_layer_desc* d, const moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
-                           moe_ws* ws,
-                           cudaStream_t s);
+                           moe_ws* ws, cudaStream_t s);
+int launch_prefill_streamed(const moe_layer_desc* d, moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
+                            int U, moe_ws* ws, cudaStream_t s, cudaStream_t cs);
 
 // Policy.
 int launch_heat_update(moe_cache* c, const int32_t* ids, int T, int k, int layer, int32_t* err, cudaStream_t s);

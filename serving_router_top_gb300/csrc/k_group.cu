@@ -55,6 +55,14 @@ __device__ __forceinline__ void resolve_group(int g, int e, int off, int layer, 
   grp_expert[g] = e;
   grp_off[g] = off;
   const int flat = layer * E + e;
+  // no residency table: the groups are bound to staging slots later (streamed prefill)
+  if (!resid) {
+    grp_slot[g] = -1;
+    grp_src[g] = MOE_SRC_STAGED;
+    grp_blob[g] = nullptr;
+    atomicAdd(s_stg, 1);
+    return;
+  }
   int slot = resid[flat];
   int src = MOE_SRC_MISSING;
   const uint8_t* blob = nullptr;
@@ -289,7 +297,10 @@ __global__ void __launch_bounds__(256) k_group_place(const int32_t* __restrict__
   }
 }
 
-int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws, cudaStream_t s) {
+int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws, cudaStream_t s,
+                 bool lookup) {
+  const int32_t* resid = c && lookup ? c->resid : nullptr;
+  const int32_t* stage = c && lookup ? c->stage : nullptr;
   if (E > 1024 || E <= 0) return MOE_EINVAL;
   if (T * k > 4096 && ws->grp_scratch) {
     const int ntile = (T + kGrpTok - 1) / kGrpTok;
@@ -305,8 +316,7 @@ int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* 
     if (launch_pdl(k_group_count, dim3(ntile), dim3(256), size_t(E) * 4, s, ids, T, k, E, cnt, ws->error) !=
         cudaSuccess)
       return MOE_ECUDA;
-    if (launch_pdl(k_group_scan, dim3(1), dim3(1024), 0, s, ntile, T, k, E, layer, c ? c->resid : nullptr,
-                   c ? c->stage : nullptr, c ? c->slots : nullptr, c ? c->staging : nullptr, c ? c->blob_bytes : 0,
+    if (launch_pdl(k_group_scan, dim3(1), dim3(1024), 0, s, ntile, T, k, E, layer, resid, stage, c ? c->slots : nullptr, c ? c->staging : nullptr, c ? c->blob_bytes : 0,
                    c ? c->nslots : 0, c ? c->nstaging : 0, cnt, eoff, ws->num_groups, ws->grp_expert, ws->grp_off,
                    ws->grp_slot, ws->grp_src, ws->grp_blob, c ? c->stats : nullptr, ws->error, ws->hmax,
                    ws->maxT * ws->s.k) != cudaSuccess)
@@ -329,7 +339,7 @@ int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* 
       return MOE_ECUDA;
     attr_set = true;
   }
-  const cudaError_t rc = launch_pdl(k_group, dim3(1), dim3(1024), smem, s, ids, T, k, E, layer, c ? c->resid : nullptr, c ? c->stage : nullptr,
+  const cudaError_t rc = launch_pdl(k_group, dim3(1), dim3(1024), smem, s, ids, T, k, E, layer, resid, stage,
                                 c ? c->slots : nullptr, c ? c->staging : nullptr, c ? c->blob_bytes : 0,
                                 c ? c->nslots : 0, c ? c->nstaging : 0, ws->num_groups, ws->grp_expert, ws->grp_off,
                                 ws->grp_slot, ws->grp_src, ws->grp_blob, ws->ent_tok, ws->ent_pos,

@@ -172,6 +172,8 @@ struct Args {
   const int32_t* ent_pos;
   const int32_t* tile_off;
   const int32_t* tile_grp;
+  const int32_t* grange;     // [2] groups g0 .. g1-1 of this launch, or null for all
+  int with_shared;           // this launch also runs the shared expert's tiles
   const int32_t* grp_src;    // MOE_SRC_RESIDENT (cache slot) or MOE_SRC_STAGED (staging slot)
   const int32_t* grp_slot;   // [G+1] N tiles before each group
   float* h;                  // gate/up output h (fp32) [maxTk + maxT, Imax]
@@ -201,7 +203,7 @@ struct Item {
 // fastest, so CTAs running at the same time share the token tile in L2), then
 // the shared expert's tiles; for the router, (token tile, row tile) pairs.
 struct Sched {
-  int G, routed_tiles, mt_r, mt_s, n_items;
+  int t0, routed_tiles, mt_r, mt_s, n_items;  // t0: the first N tile of the group range
 };
 
 template <int MODE>
@@ -209,17 +211,19 @@ __device__ __forceinline__ Sched make_sched(const Args& a) {
   Sched s;
   const int ntok = (a.T + kNT - 1) / kNT;
   if (MODE == kRouter) {
-    s.G = 0;
+    s.t0 = 0;
     s.routed_tiles = 0;
     s.mt_r = (a.E + (a.w_gate ? 1 : 0) + 127) / 128;
     s.mt_s = 0;
     s.n_items = ntok * s.mt_r;
     return s;
   }
-  s.G = *a.num_groups;
-  s.routed_tiles = a.tile_off[s.G];
+  // the groups [g0, g1) of this launch: all of them, or one unit of a streamed call
+  const int g0 = a.grange ? a.grange[0] : 0, g1 = a.grange ? a.grange[1] : *a.num_groups;
+  s.t0 = a.tile_off[g0];
+  s.routed_tiles = a.tile_off[g1] - s.t0;
   s.mt_r = MODE == kGateUp ? (2 * a.I) / 128 : a.H / 128;
-  s.mt_s = a.shared_blob ? (MODE == kGateUp ? (2 * a.I_s) / 128 : a.H / 128) : 0;
+  s.mt_s = a.shared_blob && a.with_shared ? (MODE == kGateUp ? (2 * a.I_s) / 128 : a.H / 128) : 0;
   s.n_items = s.routed_tiles * s.mt_r + ntok * s.mt_s;
   return s;
 }
@@ -236,8 +240,9 @@ __device__ __forceinline__ void item_of(const Args& a, const Sched& sc, int it, 
     x.C = a.H;
     x.g = -1;
   } else if (it < sc.routed_tiles * sc.mt_r) {
-    const int ti = it / sc.mt_r;
-    x.mt = it - ti * sc.mt_r;
+    const int tl = it / sc.mt_r;
+    x.mt = it - tl * sc.mt_r;
+    const int ti = sc.t0 + tl;
     const int lo = a.tile_grp[ti];
     x.g = lo;
     x.nt = ti - a.tile_off[lo];
@@ -874,16 +879,19 @@ __global__ void __launch_bounds__(1024) k_tiles(const int32_t* __restrict__ num_
 // GEMM's epilogue, which divides the power of two out again.  One warp per row.
 __global__ void __launch_bounds__(256) k_h16(const float* __restrict__ h, float* __restrict__ hmax,
                                              __half* __restrict__ h16, const int32_t* __restrict__ grp_off,
-                                             const int32_t* __restrict__ num_groups, int Imax, int I, int I_s,
+                                             const int32_t* __restrict__ num_groups,
+                                             const int32_t* __restrict__ grange, int Imax, int I, int I_s,
                                              int maxTk, int T, int has_shared) {
   pdl_trigger();
   pdl_wait();
-  const int routed = grp_off[*num_groups];
+  // the entries of groups [g0, g1) (all groups, or one unit), then the shared rows
+  const int e0 = grange ? grp_off[grange[0]] : 0;
+  const int routed = (grange ? grp_off[grange[1]] : grp_off[*num_groups]) - e0;
   const int rows = routed + (has_shared ? T : 0);
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   for (int rr = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); rr < rows; rr += nwarps) {
-    const int row = rr < routed ? rr : maxTk + (rr - routed);
+    const int row = rr < routed ? e0 + rr : maxTk + (rr - routed);
     const int n4 = (rr < routed ? I : I_s) / 4;
     const float4* src = reinterpret_cast<const float4*>(h + size_t(row) * Imax);
     float m = 0.f;
@@ -959,6 +967,40 @@ __global__ void __launch_bounds__(256) k_x16_grouped(const uint16_t* __restrict_
         dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
+  }
+}
+
+// One unit of a streamed prefill call: the groups of experts u*U .. u*U+U-1
+// (groups are in ascending expert id, so they are a contiguous range) take
+// their weights from staging slots base + (e - u*U); grange gets the range.
+__global__ void __launch_bounds__(256) k_unit_bind(int u, int U, int base, const int32_t* __restrict__ num_groups,
+                                                   const int32_t* __restrict__ grp_expert, int32_t* __restrict__ grp_src,
+                                                   int32_t* __restrict__ grp_slot, const uint8_t** __restrict__ grp_blob,
+                                                   const uint8_t* staging, size_t blob_bytes, int32_t* __restrict__ grange) {
+  pdl_trigger();
+  pdl_wait();
+  const int G = *num_groups;
+  const int lo_e = u * U, hi_e = lo_e + U;
+  // first group with expert >= lo_e, and >= hi_e (binary searches)
+  auto lower = [&](int v) {
+    int lo = 0, hi = G;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (grp_expert[mid] < v) lo = mid + 1;
+      else hi = mid;
+    }
+    return lo;
+  };
+  const int g0 = lower(lo_e), g1 = lower(hi_e);
+  for (int g = g0 + int(threadIdx.x); g < g1; g += blockDim.x) {
+    const int slot = base + (grp_expert[g] - lo_e);
+    grp_src[g] = MOE_SRC_STAGED;
+    grp_slot[g] = slot;
+    grp_blob[g] = staging + size_t(slot) * blob_bytes;
+  }
+  if (threadIdx.x == 0) {
+    grange[0] = g0;
+    grange[1] = g1;
   }
 }
 
@@ -1138,12 +1180,12 @@ int launch_prefill_router(const moe_layer_desc* d, const uint16_t* x, int T, moe
 // The expert part of a prefill call: tiles, gate/up GEMM (h), max|h| per row
 // and h -> f16 times a per-row power of two, down GEMM accumulating w*o
 // into an fp32 buffer, and the output cast.
-int launch_prefill_experts(const moe_layer_desc* d, const moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
-                           moe_ws* ws,
-                           cudaStream_t s) {
+// The start of a prefill call's expert part: N tiles per group, the zeroed
+// fp32 accumulator, the gate/up B rows in group order.
+static int prefill_begin(prefill::Args& a, const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T,
+                         moe_ws* ws, cudaStream_t s) {
   using namespace prefill;
   const moe_layer_shape& sh = d->s;
-  Args a = base_args(d, T, ws);
   float* yacc = y_is_fp32 ? static_cast<float*>(y) : ws->yacc;
   a.yacc = yacc;
   {
@@ -1162,31 +1204,101 @@ int launch_prefill_experts(const moe_layer_desc* d, const moe_cache* c, const ui
                    ws->num_groups, sh.H, a.maxTk, T, a.shared_blob ? 1 : 0) != cudaSuccess)
       return MOE_ECUDA;
   }
+  return MOE_OK;
+}
+
+// gate/up GEMM, h -> f16, down GEMM over the groups in grange (null: all of
+// them), with the shared expert's tiles when with_shared.
+static int prefill_groups(prefill::Args& a, const moe_layer_desc* d, const moe_cache* c, int T, moe_ws* ws,
+                          const int32_t* grange, int with_shared, bool prof, cudaStream_t s) {
+  using namespace prefill;
+  const moe_layer_shape& sh = d->s;
+  a.grange = grange;
+  a.with_shared = with_shared;
   int rc;
   {
-    ProfScope p(ws, "gateup_gemm", s);
+    ProfScope p(prof ? ws : nullptr, "gateup_gemm", s);
     if ((rc = code_maps(&a.cmaps, true, d, c))) return rc;
     if ((rc = launch_gemm<kGateUp>(a, ws->xg, a.maxTk + ws->maxT, ws->xg, a.maxTk + ws->maxT, sh.H, s))) return rc;
   }
   {
-    ProfScope p(ws, "h16", s);
+    ProfScope p(prof ? ws : nullptr, "h16", s);
     if (launch_pdl(k_h16, dim3(sm_count() * 8), dim3(256), 0, s, ws->h, ws->hmax, ws->h16, ws->grp_off,
-                   ws->num_groups, a.Imax, a.I, a.I_s, a.maxTk, T, a.shared_blob ? 1 : 0) != cudaSuccess)
+                   ws->num_groups, grange, a.Imax, a.I, a.I_s, a.maxTk, T, a.shared_blob && with_shared ? 1 : 0) !=
+        cudaSuccess)
       return MOE_ECUDA;
   }
   {
-    ProfScope p(ws, "down_gemm", s);
+    ProfScope p(prof ? ws : nullptr, "down_gemm", s);
     if ((rc = code_maps(&a.cmaps, false, d, c))) return rc;
     if ((rc = launch_gemm<kDown>(a, ws->h16, a.maxTk + ws->maxT, ws->h16, a.maxTk + ws->maxT, a.Imax, s))) return rc;
   }
+  return MOE_OK;
+}
+
+// y = bf16 of the accumulator (fp32 outputs were accumulated in place).
+static int prefill_end(const moe_layer_desc* d, void* y, int y_is_fp32, int T, moe_ws* ws, cudaStream_t s) {
+  using namespace prefill;
   if (!y_is_fp32) {
     ProfScope p(ws, "cast", s);
-    const size_t n4 = size_t(T) * sh.H / 4;
+    const size_t n4 = size_t(T) * d->s.H / 4;
     if (launch_pdl(k_cast_bf16, dim3(sm_count() * 8), dim3(256), 0, s, ws->yacc, static_cast<uint16_t*>(y), n4) !=
         cudaSuccess)
       return MOE_ECUDA;
   }
   return MOE_OK;
+}
+
+// The expert part of a prefill call: tiles, gate/up GEMM (h), max|h| per row
+// and h -> f16 times a per-row power of two, down GEMM accumulating w*o
+// into an fp32 buffer, and the output cast.
+int launch_prefill_experts(const moe_layer_desc* d, const moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
+                           moe_ws* ws, cudaStream_t s) {
+  prefill::Args a = base_args(d, T, ws);
+  int rc;
+  if ((rc = prefill_begin(a, d, x, y, y_is_fp32, T, ws, s))) return rc;
+  if ((rc = prefill_groups(a, d, c, T, ws, nullptr, 1, true, s))) return rc;
+  return prefill_end(d, y, y_is_fp32, T, ws, s);
+}
+
+// The expert part of a streamed prefill call (Strata expert paths: the copy
+// stream fills a staging slot and records `copied`, the compute stream waits
+// on it, runs the unit and records `used`, and the copy stream waits on `used`
+// before it overwrites the slot).  Units of U consecutive expert ids go from
+// the cache's backing pool (one copy of n*blob_bytes per unit) into half u%2 of
+// the staging pool; the unit's groups are bound to those slots and only they
+// run.  The shared expert runs with the first unit.
+int launch_prefill_streamed(const moe_layer_desc* d, moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
+                            int U, moe_ws* ws, cudaStream_t s, cudaStream_t cs) {
+  using namespace prefill;
+  const moe_layer_shape& sh = d->s;
+  prefill::Args a = base_args(d, T, ws);
+  int rc;
+  // the copy stream starts after everything already queued on the compute
+  // stream (an earlier call may still read the staging pool)
+  MOE_CUDA_TRY(cudaEventRecord(c->ev_ring[4], s));
+  MOE_CUDA_TRY(cudaStreamWaitEvent(cs, c->ev_ring[4], 0));
+  if ((rc = prefill_begin(a, d, x, y, y_is_fp32, T, ws, s))) return rc;
+  const int nunits = (sh.E + U - 1) / U;
+  const uint8_t* pool = static_cast<const uint8_t*>(c->backing) + size_t(d->layer) * sh.E * c->blob_bytes;
+  for (int u = 0; u < nunits; ++u) {
+    const int half = u & 1, n = sh.E - u * U < U ? sh.E - u * U : U;
+    cudaEvent_t copied = c->ev_ring[half], used = c->ev_ring[2 + half];
+    if (u >= 2) MOE_CUDA_TRY(cudaStreamWaitEvent(cs, used, 0));
+    MOE_CUDA_TRY(cudaMemcpyAsync(c->staging + size_t(half) * U * c->blob_bytes, pool + size_t(u) * U * c->blob_bytes,
+                                 size_t(n) * c->blob_bytes, cudaMemcpyDefault, cs));
+    MOE_CUDA_TRY(cudaEventRecord(copied, cs));
+    MOE_CUDA_TRY(cudaStreamWaitEvent(s, copied, 0));
+    int32_t* grange = ws->grange + 2 * u;
+    if (launch_pdl(k_unit_bind, dim3(1), dim3(256), 0, s, u, U, half * U, ws->num_groups, ws->grp_expert, ws->grp_src,
+                   ws->grp_slot, ws->grp_blob, static_cast<const uint8_t*>(c->staging), c->blob_bytes, grange) !=
+        cudaSuccess)
+      return MOE_ECUDA;
+    if ((rc = prefill_groups(a, d, c, T, ws, grange, u == 0 ? 1 : 0, false, s))) return rc;
+    MOE_CUDA_TRY(cudaEventRecord(used, s));
+  }
+  // the copy stream's last work is behind the compute stream's last wait
+  return prefill_end(d, y, y_is_fp32, T, ws, s);
 }
 
 }  // namespace moe

@@ -119,3 +119,12 @@ class ModelState:
     def forward(self, layer: int, x: torch.Tensor, y: torch.Tensor, T: int, y_is_fp32: bool = True,
                 mode: int = moe.MOE_MODE_AUTO, stream=None) -> None:
         moe.moe_layer_forward(self.layers[layer].desc, x, y, y_is_fp32, T, self.cache, self.ws, mode, stream)
+
+    def forward_streamed(self, layer: int, x: torch.Tensor, y: torch.Tensor, T: int, U: int,
+                         y_is_fp32: bool = True, stream=None) -> None:
+        """Prefill forward with the layer's experts streamed from the backing pool through the
+        staging pool in units of U (needs at least 2*U staging slots)."""
+        if getattr(self, "_copy_stream", None) is None:
+            self._copy_stream = torch.cuda.Stream()
+        moe.moe_layer_forward_streamed(self.layers[layer].desc, x, y, y_is_fp32, T, self.cache, self.ws, U,
+                                       stream, self._copy_stream)

@@ -26,7 +26,7 @@ EXPORTED = (
     "moe_cache_fill", "moe_cache_get_view", "moe_get_stats", "moe_ws_create", "moe_ws_destroy", "moe_ws_get_view",
     "moe_sync_status", "moe_strerror", "moe_route", "moe_group", "moe_layer_forward", "cache_heat_update",
     "cache_plan_swaps", "moe_cache_apply_swaps", "moe_ws_set_profiling", "moe_ws_kernel_times",
-    "cache_plan_swaps_noalloc", "moe_residual_rmsnorm",
+    "cache_plan_swaps_noalloc", "moe_residual_rmsnorm", "moe_layer_forward_streamed",
 )
 
 
@@ -97,6 +97,7 @@ def load() -> C.CDLL:
         "moe_route": (I, [P, P, P, P, I, I, I, I, P, P, P, P]),
         "moe_group": (I, [P, I, I, I, I, P, P, P]),
         "moe_layer_forward": (I, [C.POINTER(moe_layer_desc), P, P, I, I, P, P, I, P]),
+        "moe_layer_forward_streamed": (I, [C.POINTER(moe_layer_desc), P, P, I, I, P, P, I, P, P]),
         "cache_heat_update": (I, [P, P, I, I, I, P, P]),
         "cache_plan_swaps": (I, [P, C.POINTER(moe_policy_cfg), P, P, P]),
         "cache_plan_swaps_noalloc": (I, [P, P, I, I, C.POINTER(moe_policy_cfg), P, P, P]),
@@ -307,6 +308,13 @@ def moe_layer_forward(desc: moe_layer_desc, x, y, y_is_fp32: bool, T: int, cache
                       mode: int = MOE_MODE_AUTO, stream=None) -> None:
     _check(load().moe_layer_forward(C.byref(desc), _ptr(x), _ptr(y), 1 if y_is_fp32 else 0, T, cache.handle,
                                     ws.handle, mode, _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_streamed(desc: moe_layer_desc, x, y, y_is_fp32: bool, T: int, cache: Cache, ws: Workspace,
+                               U: int, stream=None, copy_stream=None) -> None:
+    _check(load().moe_layer_forward_streamed(C.byref(desc), _ptr(x), _ptr(y), 1 if y_is_fp32 else 0, T, cache.handle,
+                                             ws.handle, U, _stream(stream), _stream(copy_stream)),
+           "moe_layer_forward_streamed")
 
 
 def cache_heat_update(cache: Cache, topk_ids, T: int, k: int, layer: int, err=None, stream=None) -> None:

@@ -89,3 +89,68 @@ def test_prefill_large_expert_layer_sampled():
     tokens = np.random.default_rng(5).choice(w.T, 6, replace=False)
     ref = check_tokens(st, x_bits, y, tokens)
     U.assert_close_layer(y[tokens], ref.y, what="sampled y")
+
+
+def run_streamed(st, x_bits, T, U_, bf16_out=False):
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda()
+    y = torch.zeros((T, st.H), dtype=torch.int16 if bf16_out else torch.float32, device="cuda")
+    st.forward_streamed(0, x, y, T, U_, y_is_fp32=not bf16_out)
+    torch.cuda.synchronize()
+    rc = moe.moe_sync_status(st.ws)
+    assert rc == moe.MOE_OK, moe.strerror(rc)
+    return U.y_to_numpy(y, bf16_out)
+
+
+def check_tokens_streamed(st, x_bits, tokens):
+    """Reference for a streamed call: every expert of the layer is available (no residency tables)."""
+    logits, ids, _ = st.ws.routing(x_bits.shape[0])
+    logits = logits.cpu().numpy()
+    li = st.layers[0].host
+    ref_ids, _ = olayer.top_k(logits[tokens], st.k)
+    assert np.array_equal(ids.cpu().numpy()[tokens], ref_ids)
+    return olayer.moe_layer(x_bits[tokens], li.w_router, li.bias, st.k, lambda e: st.expert_host(0, e), st.H, st.I,
+                            shared=li.shared, I_shared=st.I_shared, w_shared_gate_bits=li.w_shared_gate,
+                            logits=logits[tokens])
+
+
+@pytest.mark.parametrize("T,H,I_,E,k,Is,U_", [
+    (300, 256, 128, 16, 2, 128, 3),   # six units, the last of one expert; each staging half reused three times
+    (129, 512, 256, 40, 7, 0, 8),     # no shared expert
+    (1024, 128, 64, 8, 2, 64, 8),     # one unit holding every expert
+])
+def test_prefill_streamed_small_shapes_full(T, H, I_, E, k, Is, U_):
+    """Experts streamed from the backing pool through two halves of the staging pool (copy
+    stream: copied; compute stream: used) give the layer with every expert available, although
+    half of them are neither resident nor staged in the cache's tables."""
+    from serving_router_top_gb300.model import ModelState
+    w = I.small_workload(T=T, H=H, I=I_, E=E, k=k, I_shared=Is, zipf_s=0.8, resident_frac=0.5, seed=T + E)
+    st = ModelState(w, stage_rest=False, nstaging=2 * U_)
+    x_bits = I.activations(w.seed, 1, T, H)
+    y = run_streamed(st, x_bits, T, U_)
+    ref = check_tokens_streamed(st, x_bits, np.arange(T))
+    U.assert_close_layer(y, ref.y)
+    yb = run_streamed(st, x_bits, T, U_, bf16_out=True)
+    U.assert_close_layer(yb, ref.y, bf16_out=True)
+
+
+def test_prefill_streamed_chunk_t8192_sampled():
+    """The 8192-token chunk with all 512 experts streamed in eight units of 64 (113 MB each)."""
+    from serving_router_top_gb300.model import ModelState
+    w = I.WORKLOADS["prefill_t8192_h2048_e512_k10"]
+    st = ModelState(w, resident=np.zeros((1, w.shape.E), dtype=bool), stage_rest=False, nslots=1, nstaging=128)
+    x_bits = I.activations(w.seed, 2, w.T, w.shape.H)
+    y = run_streamed(st, x_bits, w.T, 64)
+    tokens = np.concatenate([np.random.default_rng(6).choice(w.T, 10, replace=False), [0, w.T - 1]])
+    ref = check_tokens_streamed(st, x_bits, tokens)
+    U.assert_close_layer(y[tokens], ref.y, what="sampled y")
+
+
+def test_prefill_streamed_rejects_bad_units():
+    from serving_router_top_gb300.model import ModelState
+    w = I.small_workload(T=64, H=128, I=64, E=8, k=2, I_shared=0, zipf_s=0.0, resident_frac=1.0, seed=3)
+    st = ModelState(w, nstaging=4)
+    x = torch.zeros((64, 128), dtype=torch.int16, device="cuda")
+    y = torch.zeros((64, 128), dtype=torch.float32, device="cuda")
+    for bad in (0, 3):  # 2*U must fit the four staging slots
+        with pytest.raises(moe.MoeError):
+            st.forward_streamed(0, x, y, 64, bad)
