@@ -476,13 +476,18 @@ int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y
                          ws->gate_logit, T, s.H, s.E, st, ws->x16, ws->xscale);
     if (rc) return rc;
   }
-  {
-    ProfScope p(ws, "topk", st);
-    if ((rc = launch_topk(ws->logits, T, s.E, s.k, ws->topk_ids, ws->topk_w, ws->error, st))) return rc;
-  }
-  {
-    ProfScope p(ws, "group", st);
-    if ((rc = launch_group(ws->topk_ids, T, s.k, s.E, d->layer, c, ws, st))) return rc;
+  if (!prefill && T <= 32 && T * s.k <= 4096) {  // small windows: top-k and grouping in one launch
+    ProfScope p(ws, "topk_group", st);
+    if ((rc = launch_topk_group(ws->logits, T, s.k, s.E, d->layer, c, ws, st))) return rc;
+  } else {
+    {
+      ProfScope p(ws, "topk", st);
+      if ((rc = launch_topk(ws->logits, T, s.E, s.k, ws->topk_ids, ws->topk_w, ws->error, st))) return rc;
+    }
+    {
+      ProfScope p(ws, "group", st);
+      if ((rc = launch_group(ws->topk_ids, T, s.k, s.E, d->layer, c, ws, st))) return rc;
+    }
   }
   if (prefill) return launch_prefill_experts(d, c, x, y, y_is_fp32, T, ws, st);
   {

@@ -9,6 +9,8 @@ int launch_router(const uint16_t* x, const uint16_t* w_router, const float* bias
                   float* xscale = nullptr);
 int launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* err, cudaStream_t s);
 
+constexpr int kNotFused = -2;
+int launch_topk_group(const float* logits, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws, cudaStream_t s);
 // lookup = false: the groups' sources are left for the caller to bind (streamed prefill)
 int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws, cudaStream_t s,
                  bool lookup = true);

@@ -156,7 +156,6 @@ struct Unit {
 // Group G (after the routed groups) is the shared expert, whose entries are the T tokens.
 template <bool GATEUP, int D>
 __global__ void __launch_bounds__(kWarps * 32, 1) k_gemv(Args a) {
-  pdl_trigger();
   pdl_wait();
   constexpr int NM = GATEUP ? 2 : 1;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -396,6 +395,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_gemv(Args a) {
     for (int d = 0; d < D; ++d) {
       const int u = base + d;
       if (u < NU) {  // uniform across the CTA
+        // the next kernel's blocks launch when this CTA enters its last D units
+        // (launched at the start, waiting blocks slowed the running kernels)
+        if (u == (NU > D ? NU - D : 0)) pdl_trigger();
         if (computes) compute_unit(u, ring[d]);
         load_unit(u + D, ring[d]);
         const int tl = u >> g.l_cpw;

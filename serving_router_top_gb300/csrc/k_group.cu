@@ -14,7 +14,7 @@
 // experts, then placement in token chunks -- within a chunk each expert keeps
 // a bitmap of the tokens that chose it, and an entry's rank in its group is
 // the experts' running count plus the popcount of the bits below its token.
-#include "internal.h"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -82,18 +82,18 @@ __device__ __forceinline__ void resolve_group(int g, int e, int off, int layer, 
   atomicAdd(src == MOE_SRC_RESIDENT ? s_hit : src == MOE_SRC_STAGED ? s_stg : s_miss, 1);
 }
 
-__global__ void __launch_bounds__(1024) k_group(const int32_t* __restrict__ ids, int T, int k, int E, int layer,
-                                                const int32_t* __restrict__ resid, const int32_t* __restrict__ stage,
-                                                const uint8_t* slots, const uint8_t* staging, size_t blob_bytes,
-                                                int nslots, int nstaging, int32_t* __restrict__ num_groups,
-                                                int32_t* __restrict__ grp_expert, int32_t* __restrict__ grp_off,
-                                                int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
-                                                const uint8_t** __restrict__ grp_blob, int32_t* __restrict__ ent_tok,
-                                                int32_t* __restrict__ ent_pos, unsigned long long* stats, int32_t* err,
-                                                int W, float* __restrict__ hmax, int maxTk) {
-  pdl_trigger();
-  pdl_wait();
-  extern __shared__ int sm[];
+// The single-CTA grouping of T*k <= 4096 entries (the CTA's threads, sm: its
+// dynamic shared memory of 3E + E*W ints): counts, scans, group table with
+// the lookup, stable placement in token order.
+__device__ __forceinline__ void group_body(int* sm, const int32_t* __restrict__ ids, int T, int k, int E, int layer,
+                                           const int32_t* __restrict__ resid, const int32_t* __restrict__ stage,
+                                           const uint8_t* slots, const uint8_t* staging, size_t blob_bytes, int nslots,
+                                           int nstaging, int32_t* __restrict__ num_groups,
+                                           int32_t* __restrict__ grp_expert, int32_t* __restrict__ grp_off,
+                                           int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
+                                           const uint8_t** __restrict__ grp_blob, int32_t* __restrict__ ent_tok,
+                                           int32_t* __restrict__ ent_pos, unsigned long long* stats, int32_t* err, int W,
+                                           float* __restrict__ hmax, int maxTk) {
   int* cnt = sm;                                       // [E]
   int* off = cnt + E;                                  // [E]
   int* base = off + E;                                 // [E]
@@ -175,6 +175,46 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t* __restrict__ ids,
     }
     __syncthreads();
   }
+}
+
+__global__ void __launch_bounds__(1024) k_group(const int32_t* __restrict__ ids, int T, int k, int E, int layer,
+                                                const int32_t* __restrict__ resid, const int32_t* __restrict__ stage,
+                                                const uint8_t* slots, const uint8_t* staging, size_t blob_bytes, int nslots,
+                                                int nstaging, int32_t* __restrict__ num_groups,
+                                                int32_t* __restrict__ grp_expert, int32_t* __restrict__ grp_off,
+                                                int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
+                                                const uint8_t** __restrict__ grp_blob, int32_t* __restrict__ ent_tok,
+                                                int32_t* __restrict__ ent_pos, unsigned long long* stats, int32_t* err, int W,
+                                                float* __restrict__ hmax, int maxTk) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ int sm[];
+  group_body(sm, ids, T, k, E, layer, resid, stage, slots, staging, blob_bytes, nslots, nstaging, num_groups, grp_expert, grp_off,
+             grp_slot, grp_src, grp_blob, ent_tok, ent_pos, stats, err, W, hmax, maxTk);
+}
+
+// Top-k of every token (one warp per token) and then the grouping, in one CTA:
+// for decode windows, where each would otherwise be a launch of its own.
+template <int KPER>
+__global__ void __launch_bounds__(1024) k_topk_group(const float* __restrict__ logits, float* __restrict__ topk_w,
+                                                     int32_t* __restrict__ ids, int T, int k, int E, int layer,
+                                                     const int32_t* __restrict__ resid, const int32_t* __restrict__ stage,
+                                                     const uint8_t* slots, const uint8_t* staging, size_t blob_bytes, int nslots,
+                                                     int nstaging, int32_t* __restrict__ num_groups,
+                                                     int32_t* __restrict__ grp_expert, int32_t* __restrict__ grp_off,
+                                                     int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
+                                                     const uint8_t** __restrict__ grp_blob, int32_t* __restrict__ ent_tok,
+                                                     int32_t* __restrict__ ent_pos, unsigned long long* stats, int32_t* err, int W,
+                                                     float* __restrict__ hmax, int maxTk) {
+  pdl_wait();
+  extern __shared__ int sm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int tok = warp; tok < T; tok += blockDim.x >> 5)
+    topk_token<KPER>(logits + size_t(tok) * E, E, k, lane, ids + size_t(tok) * k, topk_w + size_t(tok) * k, err);
+  pdl_trigger();    // the expert kernels launch while the groups are built
+  __syncthreads();  // the ids written above are read by other threads of the CTA
+  group_body(sm, ids, T, k, E, layer, resid, stage, slots, staging, blob_bytes, nslots, nstaging, num_groups, grp_expert, grp_off,
+             grp_slot, grp_src, grp_blob, ent_tok, ent_pos, stats, err, W, hmax, maxTk);
 }
 
 // ------------------------------------------------------------------
@@ -347,6 +387,45 @@ int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* 
   if (rc != cudaSuccess) return MOE_ECUDA;
   MOE_LAUNCH_CHECK();
   return MOE_OK;
+}
+
+}  // namespace moe
+
+namespace moe {
+
+// Top-k and grouping in one launch for windows of at most 32 tokens; the same
+// results as launch_topk followed by launch_group.  kNotFused when the window
+// is larger (the caller then launches them apart).
+int launch_topk_group(const float* logits, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws, cudaStream_t s) {
+  if (T > 32 || T * k > 4096 || E > 1024 || E <= 0) return kNotFused;
+  int W = 16384 / E;  // bitmap words per expert, as launch_group chooses them
+  if (W > 32) W = 32;
+  if (W < 1) W = 1;
+  const int needW = (T + 31) / 32;
+  if (W > needW) W = needW > 0 ? needW : 1;
+  const size_t smem = size_t(3 * E) * 4 + size_t(E) * W * 4;
+  const int per = (E + 31) / 32;
+  auto args = [&](auto kern) {
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024) != cudaSuccess)
+        return cudaErrorInvalidValue;
+      attr = true;
+    }
+    return launch_pdl(kern, dim3(1), dim3(1024), smem, s, logits, ws->topk_w, ws->topk_ids, T, k, E, layer,
+                      c ? c->resid : nullptr, c ? c->stage : nullptr, c ? c->slots : nullptr,
+                      c ? c->staging : nullptr, c ? c->blob_bytes : 0, c ? c->nslots : 0, c ? c->nstaging : 0,
+                      ws->num_groups, ws->grp_expert, ws->grp_off, ws->grp_slot, ws->grp_src, ws->grp_blob,
+                      ws->ent_tok, ws->ent_pos, c ? c->stats : nullptr, ws->error, W, ws->hmax, ws->maxT * ws->s.k);
+  };
+  cudaError_t rc;
+  if (per <= 1) rc = args(k_topk_group<1>);
+  else if (per <= 2) rc = args(k_topk_group<2>);
+  else if (per <= 4) rc = args(k_topk_group<4>);
+  else if (per <= 8) rc = args(k_topk_group<8>);
+  else if (per <= 16) rc = args(k_topk_group<16>);
+  else rc = args(k_topk_group<32>);
+  return rc == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
 
 }  // namespace moe
