@@ -193,10 +193,10 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t* __restrict__ ids,
              grp_slot, grp_src, grp_blob, ent_tok, ent_pos, stats, err, W, hmax, maxTk);
 }
 
-// Top-k of every token (one warp per token) and then the grouping, in one CTA:
+// Top-k of every token (G warps per token) and then the grouping, in one CTA:
 // for decode windows, where each would otherwise be a launch of its own.
-template <int KPER>
-__global__ void __launch_bounds__(1024) k_topk_group(const float* __restrict__ logits, float* __restrict__ topk_w,
+template <int KP1>
+__global__ void __launch_bounds__(1024) k_topk_group(int G, const float* __restrict__ logits, float* __restrict__ topk_w,
                                                      int32_t* __restrict__ ids, int T, int k, int E, int layer,
                                                      const int32_t* __restrict__ resid, const int32_t* __restrict__ stage,
                                                      const uint8_t* slots, const uint8_t* staging, size_t blob_bytes, int nslots,
@@ -208,9 +208,8 @@ __global__ void __launch_bounds__(1024) k_topk_group(const float* __restrict__ l
                                                      float* __restrict__ hmax, int maxTk) {
   pdl_wait();
   extern __shared__ int sm[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int tok = warp; tok < T; tok += blockDim.x >> 5)
-    topk_token<KPER>(logits + size_t(tok) * E, E, k, lane, ids + size_t(tok) * k, topk_w + size_t(tok) * k, err);
+  __shared__ unsigned long long cand[32 * 128];  // per token: G*k <= 128 candidates
+  topk_tokens_cta<KP1>(logits, T, E, k, G, ids, topk_w, err, cand);
   pdl_trigger();    // the expert kernels launch while the groups are built
   __syncthreads();  // the ids written above are read by other threads of the CTA
   group_body(sm, ids, T, k, E, layer, resid, stage, slots, staging, blob_bytes, nslots, nstaging, num_groups, grp_expert, grp_off,
@@ -404,7 +403,12 @@ int launch_topk_group(const float* logits, int T, int k, int E, int layer, moe_c
   const int needW = (T + 31) / 32;
   if (W > needW) W = needW > 0 ? needW : 1;
   const size_t smem = size_t(3 * E) * 4 + size_t(E) * W * 4;
-  const int per = (E + 31) / 32;
+  // G warps per token: a power of two with T*G <= 32 and G*k <= 128
+  int Tp = 1;
+  while (Tp < T) Tp <<= 1;
+  int G = 32 / Tp;
+  while (G > 1 && G * k > 128) G >>= 1;
+  const int per = ((E + G - 1) / G + 31) / 32;  // logits per lane of a warp's slice
   auto args = [&](auto kern) {
     static bool attr = false;
     if (!attr) {
@@ -412,7 +416,7 @@ int launch_topk_group(const float* logits, int T, int k, int E, int layer, moe_c
         return cudaErrorInvalidValue;
       attr = true;
     }
-    return launch_pdl(kern, dim3(1), dim3(1024), smem, s, logits, ws->topk_w, ws->topk_ids, T, k, E, layer,
+    return launch_pdl(kern, dim3(1), dim3(1024), smem, s, G, logits, ws->topk_w, ws->topk_ids, T, k, E, layer,
                       c ? c->resid : nullptr, c ? c->stage : nullptr, c ? c->slots : nullptr,
                       c ? c->staging : nullptr, c ? c->blob_bytes : 0, c ? c->nslots : 0, c ? c->nstaging : 0,
                       ws->num_groups, ws->grp_expert, ws->grp_off, ws->grp_slot, ws->grp_src, ws->grp_blob,

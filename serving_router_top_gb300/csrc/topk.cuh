@@ -104,3 +104,109 @@ __device__ __forceinline__ void topk_token(const float* lr, int E, int k, int la
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// Top-k of up to 32 tokens by one CTA, G warps per token (warps tok*G ..
+// tok*G + G - 1; G*k <= 128).  Warp wg of a token takes the k best of its
+// slice of ceil(E/G) experts by selection rounds (KP1 logits per lane; the
+// lane's best by value desc, id asc, then the warp's best key and, among equal
+// keys, the lowest id), writing them to cand as (key << 32 | ~id); after a CTA
+// barrier the token's first warp takes the k best of the G*k candidates the
+// same way.  Ids and weights equal topk_token's: the same order (value desc,
+// id asc) and the weights' terms summed in rank order.  Every thread of the CTA
+// must call this (it holds one __syncthreads).
+template <int KP1>
+__device__ __forceinline__ void topk_tokens_cta(const float* __restrict__ logits, int T, int E, int k, int G,
+                                                int32_t* __restrict__ ids, float* __restrict__ w, int32_t* err,
+                                                unsigned long long* cand) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tok = warp / G, wg = warp - tok * G;
+  const int nslice = (E + G - 1) / G;
+  if (tok < T) {
+    const float* lr = logits + size_t(tok) * E;
+    const int e0 = wg * nslice, e1 = min(E, e0 + nslice);
+    unsigned key[KP1];
+    bool nan_seen = false;
+#pragma unroll
+    for (int j = 0; j < KP1; ++j) {
+      const int e = e0 + lane + 32 * j;
+      unsigned kk = 0u;
+      if (e < e1) {
+        float x = lr[e];
+        if (x != x) {
+          nan_seen = true;
+          x = -INFINITY;
+        }
+        kk = ordered_key(x);
+      }
+      key[j] = kk;
+    }
+    if (__any_sync(0xffffffffu, nan_seen) && lane == 0) set_error(err, MOE_ENAN);
+    unsigned long long* out = cand + size_t(tok * G + wg) * k;
+    for (int r = 0; r < k; ++r) {
+      unsigned bk = key[0];
+      int bj = 0;
+#pragma unroll
+      for (int j = 1; j < KP1; ++j)
+        if (key[j] > bk) {  // strict: an equal key at a higher j has a higher id
+          bk = key[j];
+          bj = j;
+        }
+      const unsigned kmax = __reduce_max_sync(0xffffffffu, bk);
+      const unsigned mine = unsigned(e0 + lane + 32 * bj);
+      const unsigned wid = __reduce_min_sync(0xffffffffu, bk == kmax ? mine : 0xffffffffu);
+      if (lane == 0) out[r] = (static_cast<unsigned long long>(kmax) << 32) | (0xffffffffu - wid);
+      if (bk == kmax && mine == wid) {
+#pragma unroll
+        for (int j = 0; j < KP1; ++j)
+          if (j == bj) key[j] = 0u;
+      }
+    }
+  }
+  __syncthreads();
+  if (tok < T && wg == 0) {
+    const int nc = G * k;
+    const unsigned long long* cc = cand + size_t(tok) * G * k;
+    unsigned long long c[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = lane + 32 * q;
+      c[q] = i < nc ? cc[i] : 0ull;
+    }
+    int my_id = 0;
+    float m = 0.f, den = 0.f, my_p = 0.f;
+    for (int r = 0; r < k; ++r) {
+      unsigned long long b = c[0];
+      int bq = 0;
+#pragma unroll
+      for (int q = 1; q < 4; ++q)
+        if (c[q] > b) {
+          b = c[q];
+          bq = q;
+        }
+      const unsigned hi = __reduce_max_sync(0xffffffffu, unsigned(b >> 32));
+      const unsigned lo = __reduce_max_sync(0xffffffffu, unsigned(b >> 32) == hi ? unsigned(b) : 0u);
+      const unsigned long long best = (static_cast<unsigned long long>(hi) << 32) | lo;
+      if (b == best) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q == bq) c[q] = 0ull;
+      }
+      const float wv = float_of_key(hi);
+      if (r == 0) m = wv;
+      const float p = expf(wv - m);
+      den += p;
+      if (lane == r) {
+        my_id = int(0xffffffffu - lo);
+        my_p = p;
+      }
+    }
+    if (lane < k) {
+      ids[size_t(tok) * k + lane] = my_id;
+      w[size_t(tok) * k + lane] = my_p / den;
+    }
+  }
+}
+
+}  // namespace moe
