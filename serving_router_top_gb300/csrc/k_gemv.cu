@@ -247,16 +247,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_gemv(Args a) {
     for (int m = 0; m < NM; ++m) gsr[m] = b ? reinterpret_cast<const BlobHeader*>(b)->gscale[GATEUP ? m : 2] : 0.f;
   }
 
-  // ---- then the weight stream
-  Unit<NM> ring[D];
-#pragma unroll
-  for (int d = 0; d < D; ++d) load_unit(d, ring[d]);
-
   if (g_first + tid <= g_last)
 #pragma unroll
     for (int m = 0; m < NM; ++m) S.gs[2 * (g_first + tid) + m] = gsr[m];
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
+  // ---- then the weight stream, once the small operands have landed (issued
+  // together, they queued behind the weights and arrived last)
+  Unit<NM> ring[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) load_unit(d, ring[d]);
   if (GATEUP) {
     if (tid < a.T) S.vinv[tid] = 1.0f / S.vinv[tid];
     __syncthreads();
