@@ -157,3 +157,40 @@ def test_large_expert_layer_decode_batch64_sampled():
     toks = np.random.default_rng(11).choice(T, 8, replace=False)
     ref = U.oracle_layer_from_state(st, 0, x_bits[toks], logits[toks])
     U.assert_close_layer(y[toks], ref.y, what="sampled y")
+
+
+@pytest.mark.parametrize("T,H,I_,E,k,frac", [
+    (1, 2048, 512, 512, 10, 0.5),   # eight warps per token
+    (4, 2048, 512, 512, 10, 0.5),   # the decode window: eight warps per token
+    (16, 256, 128, 64, 6, 0.4),     # two warps per token
+    (32, 256, 128, 40, 7, 0.6),     # one warp per token, E not a multiple of the slices
+])
+def test_fused_topk_group_equals_separate_kernels(T, H, I_, E, k, frac):
+    """The decode forward's single-CTA top-k + grouping (several warps per token) gives the
+    same ids, weights (bit for bit) and groups as the separate top-k kernel and grouping call
+    on the same logits."""
+    from serving_router_top_gb300.model import ModelState
+    w = I.small_workload(T=T, H=H, I=I_, E=E, k=k, I_shared=0, zipf_s=1.0, resident_frac=frac, seed=7 * T + E)
+    st = ModelState(w)
+    x = torch.from_numpy(I.activations(w.seed, 3, T, H).view(np.int16)).cuda()
+    y = torch.zeros((T, H), dtype=torch.float32, device="cuda")
+    st.forward(0, x, y, T, mode=moe.MOE_MODE_DECODE)
+    assert moe.moe_sync_status(st.ws) == moe.MOE_OK
+    logits_t, ids_t, w_t = st.ws.routing(T)
+    logits = logits_t.clone()
+    fused_ids, fused_w = ids_t.cpu().numpy().copy(), w_t.cpu().numpy().copy()
+    fused_groups = st.ws.groups(T)
+    ids = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    wts = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_route(None, None, None, logits, T, 0, E, k, ids, wts, err)
+    moe.moe_group(ids, T, k, E, 0, st.cache, st.ws)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(ids.cpu().numpy(), fused_ids)
+    assert np.array_equal(wts.cpu().numpy().view(np.uint32), fused_w.view(np.uint32))
+    for a, b in zip(st.ws.groups(T), fused_groups):
+        assert np.array_equal(a, b)
+    # and both are the oracle's top-k on these logits
+    ref_ids, _ = olayer.top_k(logits.cpu().numpy(), k)
+    assert np.array_equal(fused_ids, ref_ids)
