@@ -64,6 +64,7 @@ __device__ __forceinline__ void resolve_group(int g, int e, int off, int layer, 
     return;
   }
   int slot = resid[flat];
+  const int st = stage ? stage[flat] : -1;  // read with the residency entry: one round trip, not two
   int src = MOE_SRC_MISSING;
   const uint8_t* blob = nullptr;
   if (slot >= 0) {
@@ -71,7 +72,6 @@ __device__ __forceinline__ void resolve_group(int g, int e, int off, int layer, 
     else { set_error(err, MOE_ERANGE); slot = -1; }
   }
   if (src == MOE_SRC_MISSING) {
-    int st = stage ? stage[flat] : -1;
     if (st >= 0 && st < nstaging) { slot = st; src = MOE_SRC_STAGED; blob = staging + size_t(st) * blob_bytes; }
     else if (st >= nstaging) set_error(err, MOE_ERANGE);
   }
