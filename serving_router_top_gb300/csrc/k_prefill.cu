@@ -718,30 +718,61 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
   } else {
     // ------------------------------------------------------------ epilogue
     const int et = tid - kProducers, qw = warp & 3;
+    // down: each thread's columns et and et + kEpi of an item -- the token, the
+    // routing weight (or the shared gate logit) and max|h| of the row -- are
+    // loaded one item ahead, so their dependent loads run under the previous
+    // item's atomic adds
+    constexpr int kCols = (kNT + kEpi - 1) / kEpi;
+    int c_tok[kCols];
+    float c_w[kCols], c_hm[kCols];
+    auto fetch_cols = [&](const Item& xi) {
+#pragma unroll
+      for (int q = 0; q < kCols; ++q) {
+        const int j = et + q * kEpi;
+        c_tok[q] = 0;
+        c_w[q] = 0.f;
+        c_hm[q] = 0.f;
+        if (j < xi.n) {
+          const int ent = xi.nt * kNT + j;
+          if (xi.shared) {
+            c_tok[q] = ent;
+            c_w[q] = a.gate_logit[ent];
+            c_hm[q] = a.hmax[a.maxTk + ent];
+          } else {
+            const int pos = a.ent_pos[xi.e0 + ent];
+            c_tok[q] = pos;  // the token is pos / k
+            c_w[q] = a.topk_w[pos];
+            c_hm[q] = a.hmax[xi.e0 + ent];
+          }
+        }
+      }
+    };
+    if (MODE == kDown && blockIdx.x < sc.n_items) {
+      Item x0;
+      item_of<MODE>(a, sc, blockIdx.x, x0);
+      fetch_cols(x0);
+    }
     int done = 0;
     for (int it = blockIdx.x; it < sc.n_items; it += gridDim.x, ++done) {
       Item x;
       item_of<MODE>(a, sc, it, x);
       const int buf = done & 1;
       if (MODE == kDown) {
-        for (int j = et; j < x.n; j += kEpi) {
-          const int ent = x.nt * kNT + j;
-          int tok;
-          float w;
-          if (x.shared) {
-            tok = ent;
-            w = sigmoid_f32(a.gate_logit[tok]);
-          } else {
-            const int pos = a.ent_pos[x.e0 + ent];
-            tok = pos / a.k;
-            w = a.topk_w[pos];
+#pragma unroll
+        for (int q = 0; q < kCols; ++q) {
+          const int j = et + q * kEpi;
+          if (j < x.n) {
+            // B row = h x 2^p (the power of two the conversion to f16 chose)
+            s_tok[buf * kNT + j] = x.shared ? c_tok[q] : c_tok[q] / a.k;
+            s_w[buf * kNT + j] = (x.shared ? sigmoid_f32(c_w[q]) : c_w[q]) / pow2_scale_for(c_hm[q]);
           }
-          // B row = h x 2^p (the power of two the conversion to f16 chose)
-          const int hrow = x.shared ? a.maxTk + ent : x.e0 + ent;
-          s_tok[buf * kNT + j] = tok;
-          s_w[buf * kNT + j] = w / pow2_scale_for(a.hmax[hrow]);
         }
         epi_sync();
+        if (it + int(gridDim.x) < sc.n_items) {
+          Item xn;
+          item_of<MODE>(a, sc, it + gridDim.x, xn);
+          fetch_cols(xn);
+        }
       } else if (MODE == kGateUp) {
         // B row = x_t x 2^p: the inverse power of two of each column
         for (int j = et; j < x.n; j += kEpi) {
