@@ -23,15 +23,16 @@
 // kind::f16, issued by one thread), read back with tcgen05.ld.
 // The global scale is applied in the epilogue, in fp32.
 //
-// Roles (one persistent CTA per SM, 15 warps):
+// Roles (one persistent CTA per SM, 19 warps):
 //   warps 0-7   producers: two threads per weight row dequantise two chunks per
 //               step from the code ring into their A stages (router rows:
 //               cp.async straight into the A stage);
-//   warps 8-11  epilogue: TMEM -> registers -> h / y / logits;
-//   warp  12    TMEM owner (512 columns: two accumulators of up to 192) and
+//   warps 8-15  epilogue: TMEM -> registers -> h / y / logits, two warps per
+//               TMEM lane quadrant, each taking 16 of every 32 columns;
+//   warp  16    TMEM owner (512 columns: two accumulators of up to 192) and
 //               MMA issuer (one lane);
-//   warp  13    B loader: one TMA box per chunk;
-//   warp  14    code loader: per four chunks, one TMA box (128 bytes of each
+//   warp  17    B loader: one TMA box per chunk;
+//   warp  18    code loader: per four chunks, one TMA box (128 bytes of each
 //               of the tile's weight rows) per weight matrix from a 3-D map
 //               over the expert's arena, and the rows' scales with cp.async,
 //               into a ring of two code groups.
@@ -57,12 +58,13 @@ constexpr int kAccCols = 256;     // TMEM columns between the two accumulators (
 constexpr int kAStages = 4;  // dequantised weight tiles
 constexpr int kBStages = 5;  // token tiles
 constexpr int kBPrefetch = 4;  // token tiles prefetched into L2 beyond the ring
-constexpr int kProducers = 512;  // two groups of eight warps, two threads per weight row in each
+constexpr int kProducers = 256;  // groups of eight warps, two threads per weight row in each
+constexpr int kPGroups = kProducers / 256;
 constexpr int kGChunks = 4;      // chunks per code group: one 128-byte line of every weight row
 constexpr int kGStages = 2;      // code groups in flight
 constexpr int kGCodeBytes = 128 * 128;  // raw codes of a group: [128 rows][128 B], 16-byte pieces swizzled
 constexpr int kGScaleBytes = 128 * 16;  // raw scales of a group: [128 rows][16 B]
-constexpr int kEpi = 128;
+constexpr int kEpi = 256;  // eight warps: two per TMEM lane quadrant, each taking 16 of every 32 columns
 constexpr int kThreads = kProducers + kEpi + 96;
 constexpr int kMmaWarp = (kProducers + kEpi) / 32;
 constexpr int kLoadWarp = kMmaWarp + 1;
@@ -365,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
   }
   if (tid == 0) {
     for (int s = 0; s < kAStages; ++s) {
-      bar_init(&full[s], kProducers / 64);  // one arrival per warp of the producer group writing it
+      bar_init(&full[s], 8);  // one arrival per warp of the producer group writing it
       bar_init(&empty[s], 1);
     }
     for (int s = 0; s < kBStages; ++s) {
@@ -552,13 +554,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
         for (int c_in = 0; c_in < x.KC; c_in += kGChunks, ++g) {
           const int nch = min(kGChunks, x.KC - c_in);
           const int gs = g % kGStages;
-          const int kk = 2 * pg;                   // this group's first chunk in the code group
-          const int mine = max(0, min(2, nch - kk));  // chunks it dequantises: 0, 1 or 2 (warp-uniform)
           if (!failed && !bar_wait(&gfull[gs], (g / kGStages) & 1)) failed = true;
-          const int c0 = c + kk;
-          const bool two = mine == 2;
-          const int s0 = c0 % kAStages, s1 = (c0 + 1) % kAStages;
-          if (mine > 0) {
+          // this group's chunk pairs of the code group: chunks kk, kk + 1 for
+          // kk = 2 pg, 2 pg + 2 kPGroups, ...
+          for (int kk = 2 * pg; kk < nch; kk += 2 * kPGroups) {
+            const int mine = min(2, nch - kk);  // chunks it dequantises: 1 or 2 (warp-uniform)
+            const int c0 = c + kk;
+            const bool two = mine == 2;
+            const int s0 = c0 % kAStages, s1 = (c0 + 1) % kAStages;
             // A stages free: both looks issued before either result is needed
             if (!failed) {
               const bool w0 = c0 >= kAStages, w1 = two && c0 + 1 >= kAStages;
@@ -587,13 +590,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
             // tensor core (async proxy) before one lane of the synchronised
             // warp arrives for each chunk
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              bar_arrive(&full[s0]);
+              if (two) bar_arrive(&full[s1]);
+            }
           }
           __syncwarp();
-          if (lane == 0) {
-            if (mine > 0) bar_arrive(&full[s0]);
-            if (two) bar_arrive(&full[s1]);
-            bar_arrive(&gempty[gs]);  // the warp is done with the code group
-          }
+          if (lane == 0) bar_arrive(&gempty[gs]);  // the warp is done with the code group
           c += nch;
         }
       }
@@ -795,30 +799,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
       if (MODE == kGateUp)
         hcol = a.h + size_t(x.shared ? a.maxTk + x.nt * kNT : x.e0 + x.nt * kNT) * a.Imax + x.mt * 64 + qw * 16 +
                (lane & 15);
-      // 32 accumulator columns per TMEM load (columns past npad are read and
-      // ignored: the buffer's 256 columns are all allocated)
+      // of every 32 accumulator columns this warp takes 16 (the other warp of its
+      // lane quadrant the other 16); columns past npad are read and ignored: the
+      // buffer's 256 columns are all allocated
+      const int eh = (warp - kProducers / 32) >> 2;
       for (int c0 = 0; c0 < npad && !failed; c0 += 32) {
-        uint32_t v[32];
+        const int cb = c0 + 16 * eh;  // this warp's first column
+        uint32_t v[16];
         asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
             : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
-              "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
-              "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-            : "r"(tb + uint32_t(c0)));
+              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+            : "r"(tb + uint32_t(cb)));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         if (MODE == kGateUp) {
-          // lanes 0-15 hold gate rows, 16-31 the matching up rows: of each 16
+          // lanes 0-15 hold gate rows, 16-31 the matching up rows: of the 16
           // columns the low lanes finish the first 8, the high lanes the last 8
           const bool hi = lane >= 16;
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int b = (jj >> 3) * 16 + (jj & 7);
+          for (int b = 0; b < 8; ++b) {
             const float mine_lo = __uint_as_float(v[b]), mine_hi = __uint_as_float(v[b + 8]);
             const float recv = __shfl_xor_sync(0xffffffffu, hi ? mine_lo : mine_hi, 16);
             const float g = hi ? recv : mine_lo, u = hi ? mine_hi : recv;
-            const int j = c0 + b + (hi ? 8 : 0);
+            const int j = cb + b + (hi ? 8 : 0);
             if (j < x.n) {
               const float xi = s_w[buf * kNT + j];
               hcol[size_t(j) * a.Imax] = x.blob ? silu_f32(g * (gs0 * xi)) * (u * (gs1 * xi)) : 0.f;
@@ -829,8 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
           // terms come from different CTAs); a missing expert adds nothing
           if (x.blob) {
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const int j = c0 + jj;
+            for (int jj = 0; jj < 16; ++jj) {
+              const int j = cb + jj;
               if (j < x.n)
                 atomicAdd(a.yacc + size_t(s_tok[buf * kNT + j]) * a.H + row,
                           __uint_as_float(v[jj]) * gs0 * s_w[buf * kNT + j]);
@@ -838,8 +841,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
           }
         } else {
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int j = c0 + jj;
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = cb + jj;
             const int tok = x.nt * kNT + j;
             const float d = __uint_as_float(v[jj]);
             if (j < x.n) {
