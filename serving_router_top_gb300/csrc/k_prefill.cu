@@ -23,16 +23,16 @@
 // kind::f16, issued by one thread), read back with tcgen05.ld.
 // The global scale is applied in the epilogue, in fp32.
 //
-// Roles (one persistent CTA per SM, 19 warps):
+// Roles (one persistent CTA per SM, 27 warps):
 //   warps 0-7   producers: two threads per weight row dequantise two chunks per
 //               step from the code ring into their A stages (router rows:
 //               cp.async straight into the A stage);
-//   warps 8-15  epilogue: TMEM -> registers -> h / y / logits, two warps per
-//               TMEM lane quadrant, each taking 16 of every 32 columns;
-//   warp  16    TMEM owner (512 columns: two accumulators of up to 192) and
+//   warps 8-23  epilogue: TMEM -> registers -> h / y / logits, four warps per
+//               TMEM lane quadrant, each taking 16 of every 64 columns;
+//   warp  24    TMEM owner (512 columns: two accumulators of up to 192) and
 //               MMA issuer (one lane);
-//   warp  17    B loader: one TMA box per chunk;
-//   warp  18    code loader: per four chunks, one TMA box (128 bytes of each
+//   warp  25    B loader: one TMA box per chunk;
+//   warp  26    code loader: per four chunks, one TMA box (128 bytes of each
 //               of the tile's weight rows) per weight matrix from a 3-D map
 //               over the expert's arena, and the rows' scales with cp.async,
 //               into a ring of two code groups.
@@ -64,7 +64,8 @@ constexpr int kGChunks = 4;      // chunks per code group: one 128-byte line of 
 constexpr int kGStages = 2;      // code groups in flight
 constexpr int kGCodeBytes = 128 * 128;  // raw codes of a group: [128 rows][128 B], 16-byte pieces swizzled
 constexpr int kGScaleBytes = 128 * 16;  // raw scales of a group: [128 rows][16 B]
-constexpr int kEpi = 256;  // eight warps: two per TMEM lane quadrant, each taking 16 of every 32 columns
+constexpr int kEpi = 512;  // sixteen warps: four per TMEM lane quadrant, each taking 16 of every 64 columns
+constexpr int kEpiPerQuad = kEpi / 128;
 constexpr int kThreads = kProducers + kEpi + 96;
 constexpr int kMmaWarp = (kProducers + kEpi) / 32;
 constexpr int kLoadWarp = kMmaWarp + 1;
@@ -799,11 +800,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
       if (MODE == kGateUp)
         hcol = a.h + size_t(x.shared ? a.maxTk + x.nt * kNT : x.e0 + x.nt * kNT) * a.Imax + x.mt * 64 + qw * 16 +
                (lane & 15);
-      // of every 32 accumulator columns this warp takes 16 (the other warp of its
-      // lane quadrant the other 16); columns past npad are read and ignored: the
-      // buffer's 256 columns are all allocated
+      // of every 16 kEpiPerQuad accumulator columns this warp takes 16 (the other
+      // warps of its lane quadrant the others); columns past npad are read and
+      // ignored: the buffer's 256 columns are all allocated
       const int eh = (warp - kProducers / 32) >> 2;
-      for (int c0 = 0; c0 < npad && !failed; c0 += 32) {
+      for (int c0 = 0; c0 < npad && !failed; c0 += 16 * kEpiPerQuad) {
         const int cb = c0 + 16 * eh;  // this warp's first column
         uint32_t v[16];
         asm volatile(
