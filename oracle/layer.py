@@ -16,6 +16,12 @@ Sources (page titles as headed in the source material):
     (layer, expert) to a slot or returns a special value when not resident.
   * FreeToken reading notes (zhongzhuzhou.org), section 3.2: CPU and GPU
     partial results merge exactly -- the layer output is the plain weighted sum.
+  * Strata page, "还有一条会改变输出的路径：跳过尾部专家" (optional tail skip):
+    with a threshold of 7 on zero-based ranks, an expert that is not resident
+    and that every token of the window choosing it ranks 7th or later adds
+    nothing; one token ranking it higher, or residency, keeps it; the other
+    weights are not renormalised, so the output moves by minus the skipped
+    experts' weighted outputs.
 
 Readings where the pages are silent (each listed in the design notes):
   * top-k: softmax over all E then renormalise over the k chosen equals a
@@ -26,6 +32,9 @@ Readings where the pages are silent (each listed in the design notes):
   * residency sentinel: -1.  A non-resident expert may sit in a staging slot
     (second table); neither -> MISSING.
   * shared-expert gate: ``sigmoid(x . w_sg)``; activation SiLU(z) = z/(1+e^-z).
+  * tail skip: an entry's rank is its position r in the token's list (weight
+    descending); "not resident" means staged or missing, and a skipped
+    expert that is also missing is not an error.  Off unless asked for.
 """
 from __future__ import annotations
 
@@ -37,7 +46,7 @@ import numpy as np
 from .formats import bf16_value, dequantize
 
 MISSING = -1
-SRC_RESIDENT, SRC_STAGED, SRC_MISSING = 0, 1, -1
+SRC_RESIDENT, SRC_STAGED, SRC_MISSING, SRC_SKIPPED = 0, 1, -1, 2
 
 
 class OracleError(RuntimeError):
@@ -119,6 +128,23 @@ def lookup(experts: np.ndarray, layer: int, E: int, resid: np.ndarray,
     return slot, src
 
 
+def tail_skip_mask(groups: Groups, src: np.ndarray, k: int, min_rank: int) -> np.ndarray:
+    """Groups dropped by the tail skip (Strata page, "跳过尾部专家").
+
+    Group g is dropped when its expert is not resident and every entry has a
+    zero-based rank ``pos % k`` of at least ``min_rank``.  ``min_rank <= 0``
+    drops nothing.
+    """
+    G = groups.num_groups
+    drop = np.zeros(G, dtype=bool)
+    if min_rank <= 0:
+        return drop
+    for g in range(G):
+        ranks = groups.ent_pos[groups.off[g]:groups.off[g + 1]] % k
+        drop[g] = src[g] != SRC_RESIDENT and int(ranks.min()) >= min_rank
+    return drop
+
+
 def silu(z: np.ndarray) -> np.ndarray:
     with np.errstate(over="ignore"):
         return z / (1.0 + np.exp(-z))
@@ -167,13 +193,16 @@ def moe_layer(x_bits: np.ndarray, w_router_bits: Optional[np.ndarray], bias: Opt
               get_expert: Callable[[int], object], H: int, I: int, layer: int = 0,
               resid: Optional[np.ndarray] = None, stage: Optional[np.ndarray] = None,
               shared=None, I_shared: int = 0, w_shared_gate_bits: Optional[np.ndarray] = None,
-              logits: Optional[np.ndarray] = None, x_values: Optional[np.ndarray] = None) -> LayerResult:
+              logits: Optional[np.ndarray] = None, x_values: Optional[np.ndarray] = None,
+              tail_skip: int = 0) -> LayerResult:
     """One MoE layer forward, in the order the Strata page walks it.
 
     ``get_expert(e)`` returns the canonical-format weights of routed expert e
     of this layer.  ``logits`` (fp32) replaces the router when given.
     ``x_values`` (fp64 ``[T,H]``) overrides the decoded bf16 input, for callers
-    that feed an already-normalised activation.
+    that feed an already-normalised activation.  ``tail_skip > 0`` drops the
+    groups ``tail_skip_mask`` names: their source becomes SRC_SKIPPED, their
+    slot MISSING, and their entries' outputs stay zero.
     """
     x = bf16_value(x_bits) if x_values is None else np.asarray(x_values, dtype=np.float64)
     T = x.shape[0]
@@ -185,10 +214,15 @@ def moe_layer(x_bits: np.ndarray, w_router_bits: Optional[np.ndarray], bias: Opt
     if resid is None:
         resid = np.arange((layer + 1) * E, dtype=np.int32)  # all resident
     slot, src = lookup(groups.experts, layer, E, resid, stage)
+    drop = tail_skip_mask(groups, src, k, tail_skip)
+    src[drop] = SRC_SKIPPED
+    slot[drop] = MISSING
     if (src == SRC_MISSING).any():
         raise OracleError("expert neither resident nor staged")
     o = np.zeros((T * k, H), dtype=np.float64)
     for gi, e in enumerate(groups.experts):
+        if drop[gi]:
+            continue
         a, b = groups.off[gi], groups.off[gi + 1]
         toks = groups.ent_tok[a:b]
         o[groups.ent_pos[a:b]] = swiglu_expert(x[toks], dequantize_expert(get_expert(int(e)), H, I))

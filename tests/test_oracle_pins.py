@@ -378,3 +378,101 @@ def test_qstar_rounding_and_minimum_fill():
 def test_hit_rate_arithmetic():
     g = {r[0]: float(r[1]) for r in read_golden("hit_rate.txt")}
     assert round(100 * g["hits"] / g["lookups"], 1) == g["printed_percent"]
+
+
+# ---------------------------------------------------------------- tail skip (Strata page, "跳过尾部专家")
+
+def test_tail_skip_rules_worked_by_hand():
+    """Threshold 7 on zero-based ranks, k = 10.  Expert 7: ranks {7, 9}, resident -> kept.
+    Expert 8: rank {8}, staged -> dropped.  Expert 9: ranks {9, 7}, missing -> dropped
+    (and not an error).  Expert 3: ranks {3, 8}, staged -> kept (one token ranks it in
+    the top seven).  Everything else ranks below 7 somewhere or is resident."""
+    E, k = 20, 10
+    ids = np.array([[0, 1, 2, 3, 4, 5, 6, 7, 8, 9],
+                    [10, 11, 12, 13, 14, 15, 16, 9, 3, 7]], dtype=np.int32)
+    resid = np.full(E, -1, dtype=np.int32)
+    stage = np.full(E, -1, dtype=np.int32)
+    for e in (0, 1, 2, 4, 5, 6, 7, 10, 11, 12, 13, 14, 15, 16):
+        resid[e] = e
+    stage[3], stage[8] = 0, 1           # expert 9: neither table
+    g = layer.expert_groups(ids)
+    slot, src = layer.lookup(g.experts, 0, E, resid, stage)
+    drop = layer.tail_skip_mask(g, src, k, 7)
+    assert sorted(int(e) for e in g.experts[drop]) == [8, 9]
+    assert not layer.tail_skip_mask(g, src, k, 0).any()
+    assert not layer.tail_skip_mask(g, src, k, k).any()
+    # threshold 9: only an expert every chooser ranks last -- none here (9 is 7th for token 1)
+    assert not layer.tail_skip_mask(g, src, k, 9).any()
+    assert sorted(int(e) for e in g.experts[layer.tail_skip_mask(g, src, k, 8)]) == [8]
+
+
+def _skip_workload():
+    w = inputs.small_workload(T=3, H=64, I=32, E=24, k=6, I_shared=32, zipf_s=0.5)
+    s = w.shape
+    li = inputs.layer_inputs(w)
+    experts = {e: ex for e, ex in inputs.experts_of_layer(w, 0)}
+    # every odd expert staged, every even one resident
+    resid = np.array([e if e % 2 == 0 else -1 for e in range(s.E)], dtype=np.int32)
+    stage = np.array([-1 if e % 2 == 0 else e for e in range(s.E)], dtype=np.int32)
+    return w, s, li, experts, resid, stage
+
+
+def test_tail_skip_output_moves_by_minus_skipped_terms():
+    """The page's identity: y_skip - y_full = -sum over skipped (t, r) of w[t,r] * E_ids[t,r](x_t),
+    with the skipped terms evaluated token by token (no grouping, no scatter)."""
+    w, s, li, experts, resid, stage = _skip_workload()
+    kw = dict(resid=resid, stage=stage, shared=li.shared, I_shared=s.I_shared,
+              w_shared_gate_bits=li.w_shared_gate)
+    full = layer.moe_layer(li.x, li.w_router, li.bias, s.k, experts.__getitem__, s.H, s.I, **kw)
+    R = 3
+    skip = layer.moe_layer(li.x, li.w_router, li.bias, s.k, experts.__getitem__, s.H, s.I, tail_skip=R, **kw)
+    assert np.array_equal(skip.ids, full.ids) and np.array_equal(skip.w, full.w)   # no renormalisation
+    # the skipped experts by the rule, straight from the ids: odd (staged) and never ranked below R
+    chosen = {}
+    for t in range(w.T):
+        for r in range(s.k):
+            chosen.setdefault(int(full.ids[t, r]), []).append(r)
+    skipped = {e for e, rs in chosen.items() if e % 2 == 1 and min(rs) >= R}
+    assert skipped, "the seeded window should skip at least one expert"
+    assert {int(e) for e, sr in zip(skip.groups.experts, skip.src) if sr == layer.SRC_SKIPPED} == skipped
+    x = formats.bf16_value(li.x)
+    for t in range(w.T):
+        delta = np.zeros(s.H)
+        for r in range(s.k):
+            e = int(full.ids[t, r])
+            if e in skipped:
+                de = layer.dequantize_expert(experts[e], s.H, s.I)
+                delta -= full.w[t, r] * layer.swiglu_expert(x[t:t + 1], de)[0]
+        assert np.allclose(skip.y[t] - full.y[t], delta, rtol=1e-12, atol=1e-12)
+
+
+def test_tail_skip_missing_expert_is_dropped_not_an_error():
+    """A missing expert is fine when the rule drops it, an error when a token ranks it high."""
+    w, s, li, experts, resid, stage = _skip_workload()
+    full = layer.moe_layer(li.x, li.w_router, li.bias, s.k, experts.__getitem__, s.H, s.I, resid=resid, stage=stage)
+    R = 3
+    ranks = {}
+    for t in range(w.T):
+        for r in range(s.k):
+            ranks.setdefault(int(full.ids[t, r]), []).append(r)
+    low = [e for e, rs in ranks.items() if e % 2 == 1 and min(rs) >= R]
+    high = [e for e, rs in ranks.items() if e % 2 == 1 and min(rs) < R]
+    assert low and high
+    st2 = stage.copy()
+    st2[low[0]] = -1                      # now missing, but dropped by the rule
+    res = layer.moe_layer(li.x, li.w_router, li.bias, s.k, experts.__getitem__, s.H, s.I, resid=resid, stage=st2,
+                          tail_skip=R)
+    g = int(np.nonzero(res.groups.experts == low[0])[0][0])
+    assert res.src[g] == layer.SRC_SKIPPED and res.slot[g] == layer.MISSING
+    st3 = stage.copy()
+    st3[high[0]] = -1                     # missing and kept: the layer cannot run
+    with pytest.raises(layer.OracleError):
+        layer.moe_layer(li.x, li.w_router, li.bias, s.k, experts.__getitem__, s.H, s.I, resid=resid, stage=st3,
+                        tail_skip=R)
+
+
+def test_tail_skip_all_resident_changes_nothing():
+    w, s, li, experts, resid, stage = _skip_workload()
+    a = layer.moe_layer(li.x, li.w_router, li.bias, s.k, experts.__getitem__, s.H, s.I)
+    b = layer.moe_layer(li.x, li.w_router, li.bias, s.k, experts.__getitem__, s.H, s.I, tail_skip=1)
+    assert np.array_equal(a.y, b.y) and (b.src == layer.SRC_RESIDENT).all()
