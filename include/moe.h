@@ -59,7 +59,7 @@ enum {
 };
 
 /* Source of a group's weights, as resolved by the residency lookup. */
-enum { MOE_SRC_MISSING = -1, MOE_SRC_RESIDENT = 0, MOE_SRC_STAGED = 1 };
+enum { MOE_SRC_MISSING = -1, MOE_SRC_RESIDENT = 0, MOE_SRC_STAGED = 1, MOE_SRC_SKIPPED = 2 };
 
 /* Forward modes. */
 enum { MOE_MODE_AUTO = 0, MOE_MODE_DECODE = 1, MOE_MODE_PREFILL = 2 };
@@ -148,7 +148,8 @@ typedef struct {
 int moe_cache_get_view(const moe_cache* c, moe_cache_view* out);
 
 /* Per-layer counters accumulated on the device: out_host receives
- * int64 [L][4] = {lookups, resident hits, staged, missing}.  Synchronous. */
+ * int64 [L][5] = {lookups, resident hits, staged, missing, skipped by the
+ * tail skip}.  Synchronous. */
 int moe_get_stats(const moe_cache* c, int64_t* out_host);
 
 /* ---------------------------------------------------------- the workspace */
@@ -187,6 +188,20 @@ int moe_ws_get_view(const moe_ws* ws, moe_ws_view* out);
  * elapsed milliseconds (ms_out[i]) and static names (names_out[i], may be
  * NULL); *n_out receives the count (at most `max`).  Off by default. */
 int moe_ws_set_profiling(moe_ws* ws, int enable);
+
+/* Optional tail skip (Strata page, "还有一条会改变输出的路径：跳过尾部专家"):
+ * with min_rank > 0, the grouping of later calls on this workspace drops a
+ * group whose expert is not resident (staged or missing) when every entry has
+ * a zero-based rank (its position r in the token's list) of at least
+ * min_rank.  A dropped group keeps its place in the group arrays with source
+ * MOE_SRC_SKIPPED, slot -1 and no blob; its entries' expert outputs are zero,
+ * so the layer output moves by minus those entries' weighted outputs (the
+ * other weights are not renormalised), and a dropped missing expert records
+ * no MOE_EMISSING.  min_rank = 0 (the default) turns it off; min_rank >= k
+ * drops nothing.  Applies where the grouping looks experts up (moe_group,
+ * moe_layer_forward), not to moe_layer_forward_streamed.  MOE_EINVAL when
+ * min_rank < 0.  Host-side setting, no stream work. */
+int moe_ws_set_tail_skip(moe_ws* ws, int min_rank);
 int moe_ws_kernel_times(moe_ws* ws, int max, float* ms_out, const char** names_out, int* n_out);
 
 /* Synchronise `stream`, return the device error word (MOE_OK if none) and
@@ -215,8 +230,9 @@ int moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, fl
  * (each row distinct ids in [0, E)).  Writes the workspace's group arrays
  * (moe_ws_view): groups by ascending expert id, entries by ascending token,
  * position t*k + r; slot from the residency table, else the staging table,
- * else MOE_SRC_MISSING (also recorded as MOE_EMISSING).  Updates the cache's
- * lookup counters.  Out-of-range ids record MOE_ERANGE. */
+ * else MOE_SRC_MISSING (also recorded as MOE_EMISSING); with the workspace's
+ * tail skip on, MOE_SRC_SKIPPED for the groups it drops (moe_ws_set_tail_skip).
+ * Updates the cache's lookup counters.  Out-of-range ids record MOE_ERANGE. */
 int moe_group(const int32_t* topk_ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws,
               moe_stream_t stream);
 
@@ -224,7 +240,7 @@ int moe_group(const int32_t* topk_ids, int T, int k, int E, int layer, moe_cache
  * the slot blobs -> routing-weighted combine + sigmoid-gated shared expert:
  *   y[t] = sigmoid(x_t . w_sg) * S(x_t) + sum_r w[t,r] * E_{ids[t,r]}(x_t)
  * (Strata page, "路由以后，专家怎样分工？"; FreeToken notes section 3.2: the
- * merge is exact, no expert dropped).  x: bf16 [T, H]; y: bf16 [T, H], or
+ * merge is exact, no expert dropped unless the workspace's tail skip is on).  x: bf16 [T, H]; y: bf16 [T, H], or
  * fp32 [T, H] when y_is_fp32.  T <= the workspace's maxT.  mode selects the
  * decode kernels (CUDA-core router, GEMVs) or the prefill kernels (router and
  * grouped expert GEMMs on the tensor cores); AUTO takes prefill from 128

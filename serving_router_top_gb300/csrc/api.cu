@@ -125,7 +125,7 @@ int moe_cache_create(moe_cache** out, int L, int E, int H, int I, int nslots, in
             cudaMalloc(&c->heat, LE * 4) == cudaSuccess &&
             cudaMalloc(&c->slot_owner, size_t(nslots > 0 ? nslots : 1) * 4) == cudaSuccess &&
             cudaMalloc(&c->staging_owner, size_t(nstaging > 0 ? nstaging : 1) * 4) == cudaSuccess &&
-            cudaMalloc(&c->stats, size_t(L) * 4 * 8) == cudaSuccess &&
+            cudaMalloc(&c->stats, size_t(L) * kStats * 8) == cudaSuccess &&
             cudaMalloc(&c->plan_scratch, c->plan_scratch_bytes) == cudaSuccess;
   if (ok && nslots > 0) ok = cudaMalloc(&c->slots, size_t(nslots) * c->blob_bytes) == cudaSuccess;
   if (ok && nstaging > 0) ok = cudaMalloc(&c->staging, size_t(nstaging) * c->blob_bytes) == cudaSuccess;
@@ -137,7 +137,7 @@ int moe_cache_create(moe_cache** out, int L, int E, int H, int I, int nslots, in
          cudaMemset(c->heat, 0, LE * 4) == cudaSuccess &&
          cudaMemset(c->slot_owner, 0xff, size_t(nslots > 0 ? nslots : 1) * 4) == cudaSuccess &&
          cudaMemset(c->staging_owner, 0xff, size_t(nstaging > 0 ? nstaging : 1) * 4) == cudaSuccess &&
-         cudaMemset(c->stats, 0, size_t(L) * 4 * 8) == cudaSuccess &&
+         cudaMemset(c->stats, 0, size_t(L) * kStats * 8) == cudaSuccess &&
          cudaMemset(c->plan_scratch, 0, c->plan_scratch_bytes) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
@@ -235,7 +235,7 @@ int moe_cache_get_view(const moe_cache* c, moe_cache_view* v) {
 
 int moe_get_stats(const moe_cache* c, int64_t* out_host) {
   if (!c || !out_host) return MOE_EINVAL;
-  MOE_CUDA_TRY(cudaMemcpy(out_host, c->stats, size_t(c->L) * 4 * 8, cudaMemcpyDeviceToHost));
+  MOE_CUDA_TRY(cudaMemcpy(out_host, c->stats, size_t(c->L) * kStats * 8, cudaMemcpyDeviceToHost));
   return MOE_OK;
 }
 
@@ -349,6 +349,12 @@ int moe_ws_get_view(const moe_ws* w, moe_ws_view* v) {
   v->topk_ids = w->topk_ids;
   v->topk_w = w->topk_w;
   v->error = w->error;
+  return MOE_OK;
+}
+
+int moe_ws_set_tail_skip(moe_ws* w, int min_rank) {
+  if (!w || min_rank < 0) return MOE_EINVAL;
+  w->tail_skip = min_rank;
   return MOE_OK;
 }
 

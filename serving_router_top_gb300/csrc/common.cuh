@@ -13,6 +13,7 @@ namespace moe {
 // ---------------------------------------------------------------- limits
 constexpr int kMaxE = 1024;        // experts per layer (top-k keeps E/32 logits per lane)
 constexpr int kMaxK = 32;          // experts per token
+constexpr int kStats = 5;          // lookup counters per layer: groups, hits, staged, missing, skipped
 constexpr int kBlobHeader = 256;   // bytes before the first region of a blob
 constexpr uint32_t kBlobMagic = 0x42454f4du;  // "MOEB"
 
@@ -67,6 +68,15 @@ inline DevBlobLayout dev_layout(int H, int I) {
 // non-zero code written.
 __device__ __forceinline__ void set_error(int32_t* err, int code) {
   if (err) atomicCAS(err, MOE_OK, code);
+}
+
+// Adds one grouping's lookups to a layer's kStats counters.
+__device__ __forceinline__ void add_stats(unsigned long long* st, int groups, int hit, int stg, int miss, int skip) {
+  atomicAdd(st + 0, (unsigned long long)groups);
+  atomicAdd(st + 1, (unsigned long long)hit);
+  atomicAdd(st + 2, (unsigned long long)stg);
+  atomicAdd(st + 3, (unsigned long long)miss);
+  atomicAdd(st + 4, (unsigned long long)skip);
 }
 
 #define MOE_CUDA_TRY(expr)                   \
@@ -208,7 +218,7 @@ struct moe_cache {
   int32_t* staging_owner;     // [nstaging]
   uint8_t* slots;             // nslots * blob_bytes
   uint8_t* staging;           // nstaging * blob_bytes
-  unsigned long long* stats;  // [L][4]
+  unsigned long long* stats;  // [L][kStats]
   int32_t* plan_keys_scratch; // policy scratch (candidates), allocated at creation
   void* plan_scratch;
   size_t plan_scratch_bytes;
@@ -253,6 +263,7 @@ struct moe_ws {
   float* o;             // [maxT*k + maxT, H] routed outputs by position, then shared outputs
   int32_t* grp_scratch; // [(maxT/256 + 1) * E + E] grouping of long windows: per-tile counts, offsets
   int32_t* error;       // [1]
+  int tail_skip;        // groupings drop non-resident experts ranked at or past this by all choosers (0: off)
   // optional per-kernel timing of the most recent call
   int prof_on, prof_n;
   cudaEvent_t prof_ev[2 * 16];

@@ -46,12 +46,15 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int& total
 
 // Group g is expert e with entries from off on: its slot from the residency
 // table, else the staging table, else MISSING; counts resident/staged/missing.
+// tail: every entry of the group ranks at or past the tail-skip threshold
+// (Strata page, "跳过尾部专家"), so a non-resident expert is dropped instead:
+// no staging slot, no blob, no MISSING error.
 __device__ __forceinline__ void resolve_group(int g, int e, int off, int layer, int E, const int32_t* resid,
                                               const int32_t* stage, const uint8_t* slots, const uint8_t* staging,
                                               size_t blob_bytes, int nslots, int nstaging, int32_t* grp_expert,
                                               int32_t* grp_off, int32_t* grp_slot, int32_t* grp_src,
                                               const uint8_t** grp_blob, int32_t* err, int* s_hit, int* s_stg,
-                                              int* s_miss) {
+                                              int* s_miss, bool tail, int* s_skip) {
   grp_expert[g] = e;
   grp_off[g] = off;
   const int flat = layer * E + e;
@@ -71,6 +74,13 @@ __device__ __forceinline__ void resolve_group(int g, int e, int off, int layer, 
     if (slot < nslots) { src = MOE_SRC_RESIDENT; blob = slots + size_t(slot) * blob_bytes; }
     else { set_error(err, MOE_ERANGE); slot = -1; }
   }
+  if (src == MOE_SRC_MISSING && tail) {
+    grp_slot[g] = -1;
+    grp_src[g] = MOE_SRC_SKIPPED;
+    grp_blob[g] = nullptr;
+    atomicAdd(s_skip, 1);
+    return;
+  }
   if (src == MOE_SRC_MISSING) {
     if (st >= 0 && st < nstaging) { slot = st; src = MOE_SRC_STAGED; blob = staging + size_t(st) * blob_bytes; }
     else if (st >= nstaging) set_error(err, MOE_ERANGE);
@@ -83,8 +93,9 @@ __device__ __forceinline__ void resolve_group(int g, int e, int off, int layer, 
 }
 
 // The single-CTA grouping of T*k <= 4096 entries (the CTA's threads, sm: its
-// dynamic shared memory of 3E + E*W ints): counts, scans, group table with
-// the lookup, stable placement in token order.
+// dynamic shared memory of 4E + E*W ints): counts (and, with the tail skip,
+// each expert's lowest rank), scans, group table with the lookup, stable
+// placement in token order.
 __device__ __forceinline__ void group_body(int* sm, const int32_t* __restrict__ ids, int T, int k, int E, int layer,
                                            const int32_t* __restrict__ resid, const int32_t* __restrict__ stage,
                                            const uint8_t* slots, const uint8_t* staging, size_t blob_bytes, int nslots,
@@ -93,29 +104,31 @@ __device__ __forceinline__ void group_body(int* sm, const int32_t* __restrict__ 
                                            int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
                                            const uint8_t** __restrict__ grp_blob, int32_t* __restrict__ ent_tok,
                                            int32_t* __restrict__ ent_pos, unsigned long long* stats, int32_t* err, int W,
-                                           float* __restrict__ hmax, int maxTk) {
+                                           float* __restrict__ hmax, int maxTk, int skip_rank) {
   int* cnt = sm;                                       // [E]
   int* off = cnt + E;                                  // [E]
   int* base = off + E;                                 // [E]
-  uint32_t* bits = reinterpret_cast<uint32_t*>(base + E);  // [E][W]
+  int* minr = base + E;                                // [E] lowest rank choosing each expert
+  uint32_t* bits = reinterpret_cast<uint32_t*>(minr + E);  // [E][W]
   __shared__ int warp_sums[32];
-  __shared__ int s_hit, s_stg, s_miss;
+  __shared__ int s_hit, s_stg, s_miss, s_skip;
   const int n = T * k;
   const int chunk = W * 32;
 
-  for (int e = threadIdx.x; e < E; e += blockDim.x) { cnt[e] = 0; base[e] = 0; }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) { cnt[e] = 0; base[e] = 0; minr[e] = k; }
   // the expert kernels of this call accumulate max|h| per row into hmax
   if (hmax) {
     for (int i = threadIdx.x; i < n; i += blockDim.x) hmax[i] = 0.f;
     for (int i = threadIdx.x; i < T; i += blockDim.x) hmax[maxTk + i] = 0.f;
   }
-  if (threadIdx.x == 0) { s_hit = 0; s_stg = 0; s_miss = 0; }
+  if (threadIdx.x == 0) { s_hit = 0; s_stg = 0; s_miss = 0; s_skip = 0; }
   __syncthreads();
   bool bad = false;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     int e = ids[i];
     if (e < 0 || e >= E) { bad = true; continue; }
     atomicAdd(&cnt[e], 1);
+    if (skip_rank > 0) atomicMin(&minr[e], i % k);
   }
   if (bad) set_error(err, MOE_ERANGE);
   __syncthreads();
@@ -129,18 +142,13 @@ __device__ __forceinline__ void group_body(int* sm, const int32_t* __restrict__ 
   if (e < E) off[e] = ex_c;
   if (e < E && c > 0)
     resolve_group(ex_g, e, ex_c, layer, E, resid, stage, slots, staging, blob_bytes, nslots, nstaging, grp_expert,
-                  grp_off, grp_slot, grp_src, grp_blob, err, &s_hit, &s_stg, &s_miss);
+                  grp_off, grp_slot, grp_src, grp_blob, err, &s_hit, &s_stg, &s_miss,
+                  skip_rank > 0 && minr[e] >= skip_rank, &s_skip);
   __syncthreads();
   if (threadIdx.x == 0) {
     *num_groups = total_groups;
     grp_off[total_groups] = total_entries;
-    if (stats) {
-      unsigned long long* st = stats + size_t(layer) * 4;
-      atomicAdd(st + 0, (unsigned long long)total_groups);
-      atomicAdd(st + 1, (unsigned long long)s_hit);
-      atomicAdd(st + 2, (unsigned long long)s_stg);
-      atomicAdd(st + 3, (unsigned long long)s_miss);
-    }
+    if (stats) add_stats(stats + size_t(layer) * kStats, total_groups, s_hit, s_stg, s_miss, s_skip);
   }
 
   // stable placement, one token chunk at a time
@@ -185,12 +193,12 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t* __restrict__ ids,
                                                 int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
                                                 const uint8_t** __restrict__ grp_blob, int32_t* __restrict__ ent_tok,
                                                 int32_t* __restrict__ ent_pos, unsigned long long* stats, int32_t* err, int W,
-                                                float* __restrict__ hmax, int maxTk) {
+                                                float* __restrict__ hmax, int maxTk, int skip_rank) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ int sm[];
   group_body(sm, ids, T, k, E, layer, resid, stage, slots, staging, blob_bytes, nslots, nstaging, num_groups, grp_expert, grp_off,
-             grp_slot, grp_src, grp_blob, ent_tok, ent_pos, stats, err, W, hmax, maxTk);
+             grp_slot, grp_src, grp_blob, ent_tok, ent_pos, stats, err, W, hmax, maxTk, skip_rank);
 }
 
 // Top-k of every token (G warps per token) and then the grouping, in one CTA:
@@ -205,7 +213,7 @@ __global__ void __launch_bounds__(1024) k_topk_group(int G, const float* __restr
                                                      int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
                                                      const uint8_t** __restrict__ grp_blob, int32_t* __restrict__ ent_tok,
                                                      int32_t* __restrict__ ent_pos, unsigned long long* stats, int32_t* err, int W,
-                                                     float* __restrict__ hmax, int maxTk) {
+                                                     float* __restrict__ hmax, int maxTk, int skip_rank) {
   pdl_wait();
   extern __shared__ int sm[];
   __shared__ unsigned long long cand[32 * 128];  // per token: G*k <= 128 candidates
@@ -213,7 +221,7 @@ __global__ void __launch_bounds__(1024) k_topk_group(int G, const float* __restr
   pdl_trigger();    // the expert kernels launch while the groups are built
   __syncthreads();  // the ids written above are read by other threads of the CTA
   group_body(sm, ids, T, k, E, layer, resid, stage, slots, staging, blob_bytes, nslots, nstaging, num_groups, grp_expert, grp_off,
-             grp_slot, grp_src, grp_blob, ent_tok, ent_pos, stats, err, W, hmax, maxTk);
+             grp_slot, grp_src, grp_blob, ent_tok, ent_pos, stats, err, W, hmax, maxTk, skip_rank);
 }
 
 // ------------------------------------------------------------------
@@ -225,12 +233,18 @@ __global__ void __launch_bounds__(1024) k_topk_group(int G, const float* __restr
 // the tile's token bitmap below the token (ascending tokens, as above).
 constexpr int kGrpTok = 256;
 
+// A tile's count of an expert (at most kGrpTok) in the low 24 bits, the lowest
+// rank choosing it in the tile (kMaxK when none) above them.
+constexpr int kCntBits = 24;
+constexpr int kCntMask = (1 << kCntBits) - 1;
+
 __global__ void __launch_bounds__(256) k_group_count(const int32_t* __restrict__ ids, int T, int k, int E,
                                                      int32_t* __restrict__ cnt, int32_t* err) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ int sc[];  // [E]
-  for (int e = threadIdx.x; e < E; e += blockDim.x) sc[e] = 0;
+  extern __shared__ int sc[];  // [E] counts, then [E] lowest ranks
+  int* smin = sc + E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) { sc[e] = 0; smin[e] = kMaxK; }
   __syncthreads();
   const int t0 = blockIdx.x * kGrpTok, t1 = min(T, t0 + kGrpTok);
   bool bad = false;
@@ -238,10 +252,11 @@ __global__ void __launch_bounds__(256) k_group_count(const int32_t* __restrict__
     const int e = ids[i];
     if (e < 0 || e >= E) { bad = true; continue; }
     atomicAdd(&sc[e], 1);
+    atomicMin(&smin[e], i % k);
   }
   if (bad) set_error(err, MOE_ERANGE);
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[size_t(blockIdx.x) * E + e] = sc[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[size_t(blockIdx.x) * E + e] = sc[e] | (smin[e] << kCntBits);
 }
 
 __global__ void __launch_bounds__(1024) k_group_scan(int ntile, int T, int k, int E, int layer,
@@ -252,20 +267,21 @@ __global__ void __launch_bounds__(1024) k_group_scan(int ntile, int T, int k, in
                                                      int32_t* __restrict__ grp_expert, int32_t* __restrict__ grp_off,
                                                      int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
                                                      const uint8_t** __restrict__ grp_blob, unsigned long long* stats,
-                                                     int32_t* err, float* __restrict__ hmax, int maxTk) {
+                                                     int32_t* err, float* __restrict__ hmax, int maxTk, int skip_rank) {
   pdl_trigger();
   pdl_wait();
   __shared__ int warp_sums[32];
-  __shared__ int s_hit, s_stg, s_miss;
-  if (threadIdx.x == 0) { s_hit = 0; s_stg = 0; s_miss = 0; }
+  __shared__ int s_hit, s_stg, s_miss, s_skip;
+  if (threadIdx.x == 0) { s_hit = 0; s_stg = 0; s_miss = 0; s_skip = 0; }
   const int n = T * k;
   if (hmax) {
     for (int i = threadIdx.x; i < n; i += blockDim.x) hmax[i] = 0.f;
     for (int i = threadIdx.x; i < T; i += blockDim.x) hmax[maxTk + i] = 0.f;
   }
-  // per expert: entries before each tile (in place) and the total, loads eight tiles at a time
+  // per expert: entries before each tile (in place), the total and the lowest
+  // rank; loads eight tiles at a time
   const int e = threadIdx.x;
-  int total = 0;
+  int total = 0, low = kMaxK;
   if (e < E) {
     for (int c0 = 0; c0 < ntile; c0 += 8) {
       int v[8];
@@ -275,7 +291,8 @@ __global__ void __launch_bounds__(1024) k_group_scan(int ntile, int T, int k, in
       for (int j = 0; j < 8; ++j)
         if (c0 + j < ntile) {
           cnt[size_t(c0 + j) * E + e] = total;
-          total += v[j];
+          total += v[j] & kCntMask;
+          low = min(low, v[j] >> kCntBits);
         }
     }
   }
@@ -286,18 +303,13 @@ __global__ void __launch_bounds__(1024) k_group_scan(int ntile, int T, int k, in
   if (e < E) eoff[e] = ex_c;
   if (e < E && total > 0)
     resolve_group(ex_g, e, ex_c, layer, E, resid, stage, slots, staging, blob_bytes, nslots, nstaging, grp_expert,
-                  grp_off, grp_slot, grp_src, grp_blob, err, &s_hit, &s_stg, &s_miss);
+                  grp_off, grp_slot, grp_src, grp_blob, err, &s_hit, &s_stg, &s_miss,
+                  skip_rank > 0 && low >= skip_rank, &s_skip);
   __syncthreads();
   if (threadIdx.x == 0) {
     *num_groups = total_groups;
     grp_off[total_groups] = total_entries;
-    if (stats) {
-      unsigned long long* st = stats + size_t(layer) * 4;
-      atomicAdd(st + 0, (unsigned long long)total_groups);
-      atomicAdd(st + 1, (unsigned long long)s_hit);
-      atomicAdd(st + 2, (unsigned long long)s_stg);
-      atomicAdd(st + 3, (unsigned long long)s_miss);
-    }
+    if (stats) add_stats(stats + size_t(layer) * kStats, total_groups, s_hit, s_stg, s_miss, s_skip);
   }
 }
 
@@ -340,6 +352,7 @@ int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* 
                  bool lookup) {
   const int32_t* resid = c && lookup ? c->resid : nullptr;
   const int32_t* stage = c && lookup ? c->stage : nullptr;
+  const int skip_rank = lookup ? ws->tail_skip : 0;
   if (E > 1024 || E <= 0) return MOE_EINVAL;
   if (T * k > 4096 && ws->grp_scratch) {
     const int ntile = (T + kGrpTok - 1) / kGrpTok;
@@ -352,13 +365,13 @@ int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* 
         return MOE_ECUDA;
       attr3 = true;
     }
-    if (launch_pdl(k_group_count, dim3(ntile), dim3(256), size_t(E) * 4, s, ids, T, k, E, cnt, ws->error) !=
+    if (launch_pdl(k_group_count, dim3(ntile), dim3(256), size_t(2 * E) * 4, s, ids, T, k, E, cnt, ws->error) !=
         cudaSuccess)
       return MOE_ECUDA;
     if (launch_pdl(k_group_scan, dim3(1), dim3(1024), 0, s, ntile, T, k, E, layer, resid, stage, c ? c->slots : nullptr, c ? c->staging : nullptr, c ? c->blob_bytes : 0,
                    c ? c->nslots : 0, c ? c->nstaging : 0, cnt, eoff, ws->num_groups, ws->grp_expert, ws->grp_off,
                    ws->grp_slot, ws->grp_src, ws->grp_blob, c ? c->stats : nullptr, ws->error, ws->hmax,
-                   ws->maxT * ws->s.k) != cudaSuccess)
+                   ws->maxT * ws->s.k, skip_rank) != cudaSuccess)
       return MOE_ECUDA;
     if (launch_pdl(k_group_place, dim3(ntile), dim3(256), smem3, s, ids, T, k, E, cnt, eoff, ws->ent_tok,
                    ws->ent_pos, ws->error) != cudaSuccess)
@@ -371,7 +384,7 @@ int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* 
   if (W < 1) W = 1;
   const int needW = (T + 31) / 32;
   if (W > needW) W = needW > 0 ? needW : 1;
-  size_t smem = size_t(3 * E) * 4 + size_t(E) * W * 4;
+  size_t smem = size_t(4 * E) * 4 + size_t(E) * W * 4;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(k_group, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024) != cudaSuccess)
@@ -382,7 +395,7 @@ int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* 
                                 c ? c->slots : nullptr, c ? c->staging : nullptr, c ? c->blob_bytes : 0,
                                 c ? c->nslots : 0, c ? c->nstaging : 0, ws->num_groups, ws->grp_expert, ws->grp_off,
                                 ws->grp_slot, ws->grp_src, ws->grp_blob, ws->ent_tok, ws->ent_pos,
-                                c ? c->stats : nullptr, ws->error, W, ws->hmax, ws->maxT * ws->s.k);
+                                c ? c->stats : nullptr, ws->error, W, ws->hmax, ws->maxT * ws->s.k, skip_rank);
   if (rc != cudaSuccess) return MOE_ECUDA;
   MOE_LAUNCH_CHECK();
   return MOE_OK;
@@ -402,7 +415,7 @@ int launch_topk_group(const float* logits, int T, int k, int E, int layer, moe_c
   if (W < 1) W = 1;
   const int needW = (T + 31) / 32;
   if (W > needW) W = needW > 0 ? needW : 1;
-  const size_t smem = size_t(3 * E) * 4 + size_t(E) * W * 4;
+  const size_t smem = size_t(4 * E) * 4 + size_t(E) * W * 4;
   // G warps per token: a power of two with T*G <= 32 and G*k <= 128
   int Tp = 1;
   while (Tp < T) Tp <<= 1;
@@ -420,7 +433,8 @@ int launch_topk_group(const float* logits, int T, int k, int E, int layer, moe_c
                       c ? c->resid : nullptr, c ? c->stage : nullptr, c ? c->slots : nullptr,
                       c ? c->staging : nullptr, c ? c->blob_bytes : 0, c ? c->nslots : 0, c ? c->nstaging : 0,
                       ws->num_groups, ws->grp_expert, ws->grp_off, ws->grp_slot, ws->grp_src, ws->grp_blob,
-                      ws->ent_tok, ws->ent_pos, c ? c->stats : nullptr, ws->error, W, ws->hmax, ws->maxT * ws->s.k);
+                      ws->ent_tok, ws->ent_pos, c ? c->stats : nullptr, ws->error, W, ws->hmax, ws->maxT * ws->s.k,
+                      c ? ws->tail_skip : 0);
   };
   cudaError_t rc;
   if (per <= 1) rc = args(k_topk_group<1>);

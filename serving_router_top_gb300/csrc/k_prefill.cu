@@ -692,13 +692,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ar
           failed = __any_sync(0xffffffffu, failed);
           if (failed) break;
           if (lane == 0) {
-            expect_tx(&gfull[gs], kGCodeBytes);
-            uint8_t* dst = sG + gs * kGCodeBytes;
-            if (MODE == kGateUp) {
-              tile_load3(dst, &a.cmaps.m[arena][0], gi * 128, x.mt * 64, slot, &gfull[gs]);
-              tile_load3(dst + 64 * 128, &a.cmaps.m[arena][1], gi * 128, x.mt * 64, slot, &gfull[gs]);
+            if (x.blob) {
+              expect_tx(&gfull[gs], kGCodeBytes);
+              uint8_t* dst = sG + gs * kGCodeBytes;
+              if (MODE == kGateUp) {
+                tile_load3(dst, &a.cmaps.m[arena][0], gi * 128, x.mt * 64, slot, &gfull[gs]);
+                tile_load3(dst + 64 * 128, &a.cmaps.m[arena][1], gi * 128, x.mt * 64, slot, &gfull[gs]);
+              } else {
+                tile_load3(dst, &a.cmaps.m[arena][0], gi * 128, x.mt * 128, slot, &gfull[gs]);
+              }
             } else {
-              tile_load3(dst, &a.cmaps.m[arena][0], gi * 128, x.mt * 128, slot, &gfull[gs]);
+              // a missing or skipped expert: nothing to copy (its arena's map may
+              // not exist), the stage completes on the arrivals alone
+              bar_arrive(&gfull[gs]);
             }
           }
           const int gbytes = min(128, rowbytes - gi * 128);  // 32 per chunk

@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libmoe.so")
 
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_EMISSING, MOE_ERANGE, MOE_ENAN, MOE_ETIMEOUT = range(8)
-MOE_SRC_MISSING, MOE_SRC_RESIDENT, MOE_SRC_STAGED = -1, 0, 1
+MOE_SRC_MISSING, MOE_SRC_RESIDENT, MOE_SRC_STAGED, MOE_SRC_SKIPPED = -1, 0, 1, 2
 MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL = 0, 1, 2
 
 # Every symbol include/moe.h declares.
@@ -26,7 +26,7 @@ EXPORTED = (
     "moe_cache_fill", "moe_cache_get_view", "moe_get_stats", "moe_ws_create", "moe_ws_destroy", "moe_ws_get_view",
     "moe_sync_status", "moe_strerror", "moe_route", "moe_group", "moe_layer_forward", "cache_heat_update",
     "cache_plan_swaps", "moe_cache_apply_swaps", "moe_ws_set_profiling", "moe_ws_kernel_times",
-    "cache_plan_swaps_noalloc", "moe_residual_rmsnorm", "moe_layer_forward_streamed",
+    "cache_plan_swaps_noalloc", "moe_residual_rmsnorm", "moe_layer_forward_streamed", "moe_ws_set_tail_skip",
 )
 
 
@@ -104,6 +104,7 @@ def load() -> C.CDLL:
         "moe_residual_rmsnorm": (I, [P, P, P, I, I, F, P]),
         "moe_cache_apply_swaps": (I, [P, P, P, P, P]),
         "moe_ws_set_profiling": (I, [P, I]),
+        "moe_ws_set_tail_skip": (I, [P, I]),
         "moe_ws_kernel_times": (I, [P, I, P, P, C.POINTER(C.c_int)]),
     }
     for name, (res, args) in sig.items():
@@ -219,7 +220,8 @@ class Cache:
                 device_view(self.view.heat, (LE,), "float32", self))
 
     def stats(self) -> np.ndarray:
-        out = np.zeros((self.L, 4), dtype=np.int64)
+        """int64 [L, 5]: groups looked up, resident hits, staged, missing, skipped by the tail skip."""
+        out = np.zeros((self.L, 5), dtype=np.int64)
         _check(load().moe_get_stats(self.handle, out.ctypes.data), "moe_get_stats")
         return out
 
@@ -265,6 +267,10 @@ class Workspace:
         return (device_view(self.view.logits, (T, E), "float32", self),
                 device_view(self.view.topk_ids, (T, k), "int32", self),
                 device_view(self.view.topk_w, (T, k), "float32", self))
+
+    def set_tail_skip(self, min_rank: int) -> None:
+        """Drop non-resident experts that every choosing token ranks at or past min_rank (0: off)."""
+        _check(load().moe_ws_set_tail_skip(self.handle, int(min_rank)), "moe_ws_set_tail_skip")
 
     def set_profiling(self, enable: bool) -> None:
         _check(load().moe_ws_set_profiling(self.handle, 1 if enable else 0), "moe_ws_set_profiling")

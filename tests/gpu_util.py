@@ -58,7 +58,7 @@ def y_to_numpy(y: torch.Tensor, bf16: bool) -> np.ndarray:
     return y.cpu().numpy().astype(np.float64)
 
 
-def oracle_layer_from_state(st, layer: int, x_bits: np.ndarray, logits: np.ndarray):
+def oracle_layer_from_state(st, layer: int, x_bits: np.ndarray, logits: np.ndarray, tail_skip: int = 0):
     """Oracle forward of one layer of a ModelState, routed on the given fp32 logits."""
     lw = st.layers[layer]
     li = lw.host
@@ -66,4 +66,4 @@ def oracle_layer_from_state(st, layer: int, x_bits: np.ndarray, logits: np.ndarr
     stage = st.stage_table()
     return olayer.moe_layer(x_bits, li.w_router, li.bias, st.k, lambda e: st.expert_host(layer, e), st.H, st.I,
                             layer=layer, resid=resid, stage=stage, shared=li.shared, I_shared=st.I_shared,
-                            w_shared_gate_bits=li.w_shared_gate, logits=logits)
+                            w_shared_gate_bits=li.w_shared_gate, logits=logits, tail_skip=tail_skip)

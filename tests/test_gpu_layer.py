@@ -29,7 +29,7 @@ def run_layer(st, x_bits, T, bf16_out=False, layer=0):
     return U.y_to_numpy(y, bf16_out)
 
 
-def check_layer(st, T, bf16_out=False, step=0, layer=0):
+def check_layer(st, T, bf16_out=False, step=0, layer=0, tail_skip=0):
     x_bits = I.activations(st.w.seed, step, T, st.H)
     y = run_layer(st, x_bits, T, bf16_out, layer)
     logits_t, ids_t, w_t = st.ws.routing(T)
@@ -52,7 +52,7 @@ def check_layer(st, T, bf16_out=False, step=0, layer=0):
         gaps = np.abs(np.diff(srt[: st.k + 1]))
         assert gaps.min() <= 2 * bound[t].max(), t
     # the rest of the layer on identical routing
-    ref = U.oracle_layer_from_state(st, layer, x_bits, logits)
+    ref = U.oracle_layer_from_state(st, layer, x_bits, logits, tail_skip=tail_skip)
     exp_, off, slot, src, ent_tok, ent_pos = st.ws.groups(T)
     assert np.array_equal(exp_, ref.groups.experts)
     assert np.array_equal(off, ref.groups.off)
@@ -97,6 +97,99 @@ def test_layer_decode_t4_h2048_e512_k10():
     check_layer(st, w.T, bf16_out=True, step=1)
     stats = st.cache.stats()
     assert stats[0, 0] == stats[0, 1] + stats[0, 2] and stats[0, 3] == 0
+
+
+# ------------------------------------------------------------ tail skip
+# (Strata page, "跳过尾部专家"): a non-resident expert that every choosing token
+# ranks at or past the threshold is dropped; no renormalisation.
+
+def test_tail_skip_decode_window():
+    """The page's threshold (7, zero-based ranks) on the verify window: groups, sources and
+    slots bit-exact, y within tolerance of the oracle's layer with the same groups dropped,
+    and the drops counted."""
+    from serving_router_top_gb300.model import ModelState
+    w = I.WORKLOADS["decode_t4_h2048_e512_k10"]
+    st = ModelState(w)
+    st.ws.set_tail_skip(7)
+    n_skip = 0
+    for step in range(4):
+        _, ref = check_layer(st, w.T, step=step, tail_skip=7)
+        n_skip += int((ref.src == olayer.SRC_SKIPPED).sum())
+    assert n_skip > 0
+    stats = st.cache.stats()
+    assert stats[0, 4] == n_skip and stats[0, 3] == 0
+    assert stats[0, 0] == stats[0, 1] + stats[0, 2] + stats[0, 4]
+    st.ws.set_tail_skip(0)
+    _, ref = check_layer(st, w.T, step=0)
+    assert not (ref.src == olayer.SRC_SKIPPED).any()
+
+
+@pytest.mark.parametrize("T,R", [(5, 1), (8, 2), (64, 2)])   # GEMV path, and the streaming kernel past 8 tokens
+def test_tail_skip_small_windows(T, R):
+    from serving_router_top_gb300.model import ModelState
+    w = I.small_workload(T=T, H=256, I=128, E=24, k=4, I_shared=128, zipf_s=0.6, resident_frac=0.5, seed=11 + T)
+    st = ModelState(w)
+    st.ws.set_tail_skip(R)
+    n_skip = 0
+    for step in range(3):
+        _, ref = check_layer(st, T, step=step, tail_skip=R)
+        n_skip += int((ref.src == olayer.SRC_SKIPPED).sum())
+    assert n_skip > 0
+
+
+def _split_ids(rng, T, k, R, low, high):
+    """Each token's ranks 0..R-1 from `low`, ranks R..k-1 from `high` (distinct within a row)."""
+    ids = np.zeros((T, k), dtype=np.int32)
+    for t in range(T):
+        ids[t, :R] = rng.choice(low, R, replace=False)
+        ids[t, R:] = rng.choice(high, k - R, replace=False)
+    return ids
+
+
+@pytest.mark.parametrize("T", [100, 600])   # one-CTA grouping, and the three multi-CTA passes (T*k > 4096)
+def test_tail_skip_grouping_missing_experts(T):
+    """Every non-resident expert is missing (no staging) but chosen only at ranks >= R: with the
+    tail skip at R the grouping drops them all and records no error; off, MOE_EMISSING.  Groups
+    and sources bit-exact against the oracle's lookup and drop rule on both grouping paths."""
+    from serving_router_top_gb300.model import ModelState
+    E, k, R = 64, 8, 5
+    w = I.small_workload(T=T, H=128, I=64, E=E, k=k, I_shared=0, resident_frac=0.5, seed=5)
+    st = ModelState(w, stage_rest=False)
+    resid = st.resid_table()
+    res_e = np.flatnonzero(resid[:E] >= 0)
+    non_e = np.flatnonzero(resid[:E] < 0)
+    assert len(res_e) >= R and len(non_e) >= k - R
+    ids = _split_ids(np.random.default_rng(T), T, k, R, res_e, non_e)
+    ids_t = torch.from_numpy(ids).cuda()
+    st.ws.set_tail_skip(R)
+    moe.moe_group(ids_t, T, k, E, 0, st.cache, st.ws)
+    assert moe.moe_sync_status(st.ws) == moe.MOE_OK
+    g = olayer.expert_groups(ids)
+    slot, src = olayer.lookup(g.experts, 0, E, resid, st.stage_table())
+    drop = olayer.tail_skip_mask(g, src, k, R)
+    src[drop] = olayer.SRC_SKIPPED
+    slot[drop] = olayer.MISSING
+    assert drop.sum() == len(set(ids[:, R:].ravel()))
+    exp_, off, gslot, gsrc, ent_tok, ent_pos = st.ws.groups(T)
+    assert np.array_equal(exp_, g.experts) and np.array_equal(off, g.off)
+    assert np.array_equal(ent_tok, g.ent_tok) and np.array_equal(ent_pos, g.ent_pos)
+    assert np.array_equal(gslot, slot) and np.array_equal(gsrc, src)
+    assert st.cache.stats()[0, 4] == drop.sum()
+    # one token ranking a missing expert above R keeps it: an error again
+    ids2 = ids.copy()
+    ids2[0, 0], ids2[0, R] = ids2[0, R], ids2[0, 0]
+    moe.moe_group(torch.from_numpy(ids2).cuda(), T, k, E, 0, st.cache, st.ws)
+    assert moe.moe_sync_status(st.ws) == moe.MOE_EMISSING
+    st.ws.set_tail_skip(0)
+    moe.moe_group(ids_t, T, k, E, 0, st.cache, st.ws)
+    assert moe.moe_sync_status(st.ws) == moe.MOE_EMISSING
+
+
+def test_tail_skip_rejects_negative_rank():
+    from serving_router_top_gb300.model import ModelState
+    st = ModelState(I.small_workload(T=2, H=128, I=64, E=8, k=2, I_shared=0))
+    with pytest.raises(moe.MoeError):
+        st.ws.set_tail_skip(-1)
 
 
 def test_missing_expert_is_reported():

@@ -30,7 +30,7 @@ def run_prefill(st, x_bits, T, bf16_out=False):
     return U.y_to_numpy(y, bf16_out)
 
 
-def check_tokens(st, x_bits, y, tokens):
+def check_tokens(st, x_bits, y, tokens, tail_skip=0):
     logits, ids, _ = st.ws.routing(x_bits.shape[0])
     logits = logits.cpu().numpy()
     li = st.layers[0].host
@@ -39,7 +39,7 @@ def check_tokens(st, x_bits, y, tokens):
     assert np.array_equal(ids.cpu().numpy()[tokens], ref_ids)
     ref = olayer.moe_layer(x_bits[tokens], li.w_router, li.bias, st.k, lambda e: st.expert_host(0, e), st.H, st.I,
                            resid=st.resid_table(), stage=st.stage_table(), shared=li.shared, I_shared=st.I_shared,
-                           w_shared_gate_bits=li.w_shared_gate, logits=logits[tokens])
+                           w_shared_gate_bits=li.w_shared_gate, logits=logits[tokens], tail_skip=tail_skip)
     return ref
 
 
@@ -58,6 +58,26 @@ def test_prefill_small_shapes_full(T, H, I_, E, k, Is, zipf):
     U.assert_close_layer(y, ref.y)
     yb = run_prefill(st, x_bits, T, bf16_out=True)
     U.assert_close_layer(yb, ref.y, bf16_out=True)
+
+
+@pytest.mark.parametrize("T,H,I_,E,k,Is,zipf,R", [
+    (300, 256, 128, 64, 4, 128, 1.2, 2),    # one-CTA grouping
+    (1100, 128, 64, 128, 4, 64, 1.5, 2),    # the multi-CTA grouping passes (T*k > 4096)
+])
+def test_prefill_tail_skip_full(T, H, I_, E, k, Is, zipf, R):
+    """Tail skip (Strata page, "跳过尾部专家") on the prefill path: the dropped groups load no
+    weights and add nothing; y against the oracle's layer with the same drops, whole window."""
+    from serving_router_top_gb300.model import ModelState
+    w = I.small_workload(T=T, H=H, I=I_, E=E, k=k, I_shared=Is, zipf_s=zipf, resident_frac=0.5, seed=T + E)
+    st = ModelState(w)
+    st.ws.set_tail_skip(R)
+    x_bits = I.activations(w.seed, 0, T, H)
+    y = run_prefill(st, x_bits, T)
+    ref = check_tokens(st, x_bits, y, np.arange(T), tail_skip=R)
+    assert (ref.src == olayer.SRC_SKIPPED).any()
+    _, _, slot, src, _, _ = st.ws.groups(T)
+    assert np.array_equal(src, ref.src) and np.array_equal(slot, ref.slot)
+    U.assert_close_layer(y, ref.y)
 
 
 def test_prefill_chunk_t8192_h2048_e512_k10_sampled():
