@@ -202,6 +202,16 @@ int moe_ws_set_profiling(moe_ws* ws, int enable);
  * moe_layer_forward), not to moe_layer_forward_streamed.  MOE_EINVAL when
  * min_rank < 0.  Host-side setting, no stream work. */
 int moe_ws_set_tail_skip(moe_ws* ws, int min_rank);
+
+/* Heat update inside the grouping (Strata page, "哪些专家能长期留在显存？":
+ * heat counts how often the router picks an expert).  With enable != 0, the
+ * grouping of later moe_layer_forward and moe_group calls on this workspace
+ * with a cache also adds the window's selection counts to the cache's heat
+ * row of the call's layer, with the arithmetic of cache_heat_update
+ * (heat = fl32(heat + (float)count), each selected expert once per call); the
+ * caller then leaves cache_heat_update out.  Off by default.  Host-side
+ * setting, no stream work. */
+int moe_ws_set_fused_heat(moe_ws* ws, int enable);
 int moe_ws_kernel_times(moe_ws* ws, int max, float* ms_out, const char** names_out, int* n_out);
 
 /* Synchronise `stream`, return the device error word (MOE_OK if none) and
@@ -232,7 +242,9 @@ int moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, fl
  * position t*k + r; slot from the residency table, else the staging table,
  * else MOE_SRC_MISSING (also recorded as MOE_EMISSING); with the workspace's
  * tail skip on, MOE_SRC_SKIPPED for the groups it drops (moe_ws_set_tail_skip).
- * Updates the cache's lookup counters.  Out-of-range ids record MOE_ERANGE. */
+ * Updates the cache's lookup counters.  Out-of-range ids record MOE_ERANGE.
+ * MOE_EINVAL when T exceeds the workspace's maxT, k or E differ from the
+ * workspace's shape, or E from the cache's. */
 int moe_group(const int32_t* topk_ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws,
               moe_stream_t stream);
 

@@ -352,6 +352,12 @@ int moe_ws_get_view(const moe_ws* w, moe_ws_view* v) {
   return MOE_OK;
 }
 
+int moe_ws_set_fused_heat(moe_ws* w, int enable) {
+  if (!w) return MOE_EINVAL;
+  w->fused_heat = enable ? 1 : 0;
+  return MOE_OK;
+}
+
 int moe_ws_set_tail_skip(moe_ws* w, int min_rank) {
   if (!w || min_rank < 0) return MOE_EINVAL;
   w->tail_skip = min_rank;
@@ -405,8 +411,8 @@ int moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, fl
 }
 
 int moe_group(const int32_t* topk_ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws, moe_stream_t stream) {
-  if (!topk_ids || !c || !ws || T < 0 || T > ws->maxT || k != ws->s.k || E != c->E || E > kMaxE || layer < 0 ||
-      layer >= c->L)
+  if (!topk_ids || !c || !ws || T < 0 || T > ws->maxT || k != ws->s.k || E != c->E || E != ws->s.E || E > kMaxE ||
+      layer < 0 || layer >= c->L)
     return MOE_EINVAL;
   if (T == 0) return MOE_OK;
   return launch_group(topk_ids, T, k, E, layer, c, ws, reinterpret_cast<cudaStream_t>(stream));

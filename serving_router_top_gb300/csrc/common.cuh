@@ -70,6 +70,11 @@ __device__ __forceinline__ void set_error(int32_t* err, int code) {
   if (err) atomicCAS(err, MOE_OK, code);
 }
 
+// An L2 prefetch of the 128-byte line holding p (a hint: no data returns).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Adds one grouping's lookups to a layer's kStats counters.
 __device__ __forceinline__ void add_stats(unsigned long long* st, int groups, int hit, int stg, int miss, int skip) {
   atomicAdd(st + 0, (unsigned long long)groups);
@@ -263,6 +268,7 @@ struct moe_ws {
   float* o;             // [maxT*k + maxT, H] routed outputs by position, then shared outputs
   int32_t* grp_scratch; // [(maxT/256 + 1) * E + E] grouping of long windows: per-tile counts, offsets
   int32_t* error;       // [1]
+  int fused_heat;       // groupings with a cache also add the window's counts to the layer's heat
   int tail_skip;        // groupings drop non-resident experts ranked at or past this by all choosers (0: off)
   // optional per-kernel timing of the most recent call
   int prof_on, prof_n;

@@ -94,8 +94,8 @@ __device__ __forceinline__ void resolve_group(int g, int e, int off, int layer, 
 
 // The single-CTA grouping of T*k <= 4096 entries (the CTA's threads, sm: its
 // dynamic shared memory of 4E + E*W ints): counts (and, with the tail skip,
-// each expert's lowest rank), scans, group table with the lookup, stable
-// placement in token order.
+// each expert's lowest rank; with heat_row, the heat update of the window),
+// scans, group table with the lookup, stable placement in token order.
 __device__ __forceinline__ void group_body(int* sm, const int32_t* __restrict__ ids, int T, int k, int E, int layer,
                                            const int32_t* __restrict__ resid, const int32_t* __restrict__ stage,
                                            const uint8_t* slots, const uint8_t* staging, size_t blob_bytes, int nslots,
@@ -104,7 +104,8 @@ __device__ __forceinline__ void group_body(int* sm, const int32_t* __restrict__ 
                                            int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
                                            const uint8_t** __restrict__ grp_blob, int32_t* __restrict__ ent_tok,
                                            int32_t* __restrict__ ent_pos, unsigned long long* stats, int32_t* err, int W,
-                                           float* __restrict__ hmax, int maxTk, int skip_rank) {
+                                           float* __restrict__ hmax, int maxTk, int skip_rank,
+                                           float* __restrict__ heat_row) {
   int* cnt = sm;                                       // [E]
   int* off = cnt + E;                                  // [E]
   int* base = off + E;                                 // [E]
@@ -136,6 +137,7 @@ __device__ __forceinline__ void group_body(int* sm, const int32_t* __restrict__ 
   // scan counts and presence (E <= blockDim.x)
   const int e = threadIdx.x;
   const int c = e < E ? cnt[e] : 0;
+  if (heat_row && c > 0) heat_row[e] = __fadd_rn(heat_row[e], float(c));  // as the heat-update kernel
   int total_entries, total_groups;
   const int ex_c = block_excl_scan(c, warp_sums, total_entries);
   const int ex_g = block_excl_scan(c > 0 ? 1 : 0, warp_sums, total_groups);
@@ -193,12 +195,13 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t* __restrict__ ids,
                                                 int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
                                                 const uint8_t** __restrict__ grp_blob, int32_t* __restrict__ ent_tok,
                                                 int32_t* __restrict__ ent_pos, unsigned long long* stats, int32_t* err, int W,
-                                                float* __restrict__ hmax, int maxTk, int skip_rank) {
+                                                float* __restrict__ hmax, int maxTk, int skip_rank,
+                                                float* __restrict__ heat_row) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ int sm[];
   group_body(sm, ids, T, k, E, layer, resid, stage, slots, staging, blob_bytes, nslots, nstaging, num_groups, grp_expert, grp_off,
-             grp_slot, grp_src, grp_blob, ent_tok, ent_pos, stats, err, W, hmax, maxTk, skip_rank);
+             grp_slot, grp_src, grp_blob, ent_tok, ent_pos, stats, err, W, hmax, maxTk, skip_rank, heat_row);
 }
 
 // Top-k of every token (G warps per token) and then the grouping, in one CTA:
@@ -213,7 +216,16 @@ __global__ void __launch_bounds__(1024) k_topk_group(int G, const float* __restr
                                                      int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
                                                      const uint8_t** __restrict__ grp_blob, int32_t* __restrict__ ent_tok,
                                                      int32_t* __restrict__ ent_pos, unsigned long long* stats, int32_t* err, int W,
-                                                     float* __restrict__ hmax, int maxTk, int skip_rank) {
+                                                     float* __restrict__ hmax, int maxTk, int skip_rank,
+                                                     float* __restrict__ heat_row) {
+  // the layer's residency, staging and heat rows do not depend on the previous
+  // kernel: they travel to L2 while it finishes
+  {
+    const int lines = (E + 31) / 32, i = threadIdx.x;
+    if (resid && i < lines) prefetch_l2(resid + size_t(layer) * E + 32 * i);
+    else if (stage && i >= 32 && i - 32 < lines) prefetch_l2(stage + size_t(layer) * E + 32 * (i - 32));
+    else if (heat_row && i >= 64 && i - 64 < lines) prefetch_l2(heat_row + 32 * (i - 64));
+  }
   pdl_wait();
   extern __shared__ int sm[];
   __shared__ unsigned long long cand[32 * 128];  // per token: G*k <= 128 candidates
@@ -221,7 +233,7 @@ __global__ void __launch_bounds__(1024) k_topk_group(int G, const float* __restr
   pdl_trigger();    // the expert kernels launch while the groups are built
   __syncthreads();  // the ids written above are read by other threads of the CTA
   group_body(sm, ids, T, k, E, layer, resid, stage, slots, staging, blob_bytes, nslots, nstaging, num_groups, grp_expert, grp_off,
-             grp_slot, grp_src, grp_blob, ent_tok, ent_pos, stats, err, W, hmax, maxTk, skip_rank);
+             grp_slot, grp_src, grp_blob, ent_tok, ent_pos, stats, err, W, hmax, maxTk, skip_rank, heat_row);
 }
 
 // ------------------------------------------------------------------
@@ -267,7 +279,8 @@ __global__ void __launch_bounds__(1024) k_group_scan(int ntile, int T, int k, in
                                                      int32_t* __restrict__ grp_expert, int32_t* __restrict__ grp_off,
                                                      int32_t* __restrict__ grp_slot, int32_t* __restrict__ grp_src,
                                                      const uint8_t** __restrict__ grp_blob, unsigned long long* stats,
-                                                     int32_t* err, float* __restrict__ hmax, int maxTk, int skip_rank) {
+                                                     int32_t* err, float* __restrict__ hmax, int maxTk, int skip_rank,
+                                                     float* __restrict__ heat_row) {
   pdl_trigger();
   pdl_wait();
   __shared__ int warp_sums[32];
@@ -296,6 +309,7 @@ __global__ void __launch_bounds__(1024) k_group_scan(int ntile, int T, int k, in
         }
     }
   }
+  if (heat_row && total > 0) heat_row[e] = __fadd_rn(heat_row[e], float(total));  // as the heat-update kernel
   __syncthreads();
   int total_entries, total_groups;
   const int ex_c = block_excl_scan(total, warp_sums, total_entries);
@@ -353,6 +367,7 @@ int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* 
   const int32_t* resid = c && lookup ? c->resid : nullptr;
   const int32_t* stage = c && lookup ? c->stage : nullptr;
   const int skip_rank = lookup ? ws->tail_skip : 0;
+  float* heat_row = c && ws->fused_heat ? c->heat + size_t(layer) * E : nullptr;
   if (E > 1024 || E <= 0) return MOE_EINVAL;
   if (T * k > 4096 && ws->grp_scratch) {
     const int ntile = (T + kGrpTok - 1) / kGrpTok;
@@ -371,7 +386,7 @@ int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* 
     if (launch_pdl(k_group_scan, dim3(1), dim3(1024), 0, s, ntile, T, k, E, layer, resid, stage, c ? c->slots : nullptr, c ? c->staging : nullptr, c ? c->blob_bytes : 0,
                    c ? c->nslots : 0, c ? c->nstaging : 0, cnt, eoff, ws->num_groups, ws->grp_expert, ws->grp_off,
                    ws->grp_slot, ws->grp_src, ws->grp_blob, c ? c->stats : nullptr, ws->error, ws->hmax,
-                   ws->maxT * ws->s.k, skip_rank) != cudaSuccess)
+                   ws->maxT * ws->s.k, skip_rank, heat_row) != cudaSuccess)
       return MOE_ECUDA;
     if (launch_pdl(k_group_place, dim3(ntile), dim3(256), smem3, s, ids, T, k, E, cnt, eoff, ws->ent_tok,
                    ws->ent_pos, ws->error) != cudaSuccess)
@@ -395,7 +410,8 @@ int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* 
                                 c ? c->slots : nullptr, c ? c->staging : nullptr, c ? c->blob_bytes : 0,
                                 c ? c->nslots : 0, c ? c->nstaging : 0, ws->num_groups, ws->grp_expert, ws->grp_off,
                                 ws->grp_slot, ws->grp_src, ws->grp_blob, ws->ent_tok, ws->ent_pos,
-                                c ? c->stats : nullptr, ws->error, W, ws->hmax, ws->maxT * ws->s.k, skip_rank);
+                                c ? c->stats : nullptr, ws->error, W, ws->hmax, ws->maxT * ws->s.k, skip_rank,
+                                heat_row);
   if (rc != cudaSuccess) return MOE_ECUDA;
   MOE_LAUNCH_CHECK();
   return MOE_OK;
@@ -434,7 +450,7 @@ int launch_topk_group(const float* logits, int T, int k, int E, int layer, moe_c
                       c ? c->staging : nullptr, c ? c->blob_bytes : 0, c ? c->nslots : 0, c ? c->nstaging : 0,
                       ws->num_groups, ws->grp_expert, ws->grp_off, ws->grp_slot, ws->grp_src, ws->grp_blob,
                       ws->ent_tok, ws->ent_pos, c ? c->stats : nullptr, ws->error, W, ws->hmax, ws->maxT * ws->s.k,
-                      c ? ws->tail_skip : 0);
+                      c ? ws->tail_skip : 0, c && ws->fused_heat ? c->heat + size_t(layer) * E : nullptr);
   };
   cudaError_t rc;
   if (per <= 1) rc = args(k_topk_group<1>);

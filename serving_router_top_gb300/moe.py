@@ -27,6 +27,7 @@ EXPORTED = (
     "moe_sync_status", "moe_strerror", "moe_route", "moe_group", "moe_layer_forward", "cache_heat_update",
     "cache_plan_swaps", "moe_cache_apply_swaps", "moe_ws_set_profiling", "moe_ws_kernel_times",
     "cache_plan_swaps_noalloc", "moe_residual_rmsnorm", "moe_layer_forward_streamed", "moe_ws_set_tail_skip",
+    "moe_ws_set_fused_heat",
 )
 
 
@@ -105,6 +106,7 @@ def load() -> C.CDLL:
         "moe_cache_apply_swaps": (I, [P, P, P, P, P]),
         "moe_ws_set_profiling": (I, [P, I]),
         "moe_ws_set_tail_skip": (I, [P, I]),
+        "moe_ws_set_fused_heat": (I, [P, I]),
         "moe_ws_kernel_times": (I, [P, I, P, P, C.POINTER(C.c_int)]),
     }
     for name, (res, args) in sig.items():
@@ -271,6 +273,10 @@ class Workspace:
     def set_tail_skip(self, min_rank: int) -> None:
         """Drop non-resident experts that every choosing token ranks at or past min_rank (0: off)."""
         _check(load().moe_ws_set_tail_skip(self.handle, int(min_rank)), "moe_ws_set_tail_skip")
+
+    def set_fused_heat(self, enable: bool) -> None:
+        """Let the grouping of later calls with a cache also add the window's counts to the layer's heat."""
+        _check(load().moe_ws_set_fused_heat(self.handle, 1 if enable else 0), "moe_ws_set_fused_heat")
 
     def set_profiling(self, enable: bool) -> None:
         _check(load().moe_ws_set_profiling(self.handle, 1 if enable else 0), "moe_ws_set_profiling")

@@ -67,6 +67,57 @@ def test_heat_update_bit_exact():
     assert np.array_equal(c.tables()[2].cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("T", [17, 600])   # one-CTA grouping, and the multi-CTA passes (T*k > 4096)
+def test_fused_heat_in_grouping_bit_exact(T):
+    """moe_group with the workspace's fused heat on adds exactly the oracle's heat update;
+    off, the heats stay as they were."""
+    L, E, k = 3, 40, 8
+    resident = np.zeros((L, E), dtype=bool)
+    resident[:, ::3] = True
+    c, _, _ = make_cache(L, E, resident)
+    ws = moe.Workspace(T, 64, 64, E, k, 0)
+    g = np.random.default_rng(T)
+    heat = (g.random(L * E) * 50).astype(F32)
+    set_heat(c, heat)
+    ref = heat.copy()
+    ws.set_fused_heat(True)
+    for step in range(6):
+        layer = step % L
+        ids = np.stack([g.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        moe.moe_group(torch.from_numpy(ids).cuda(), T, k, E, layer, c, ws)
+        opol.heat_update(ref, ids, layer, E)
+    torch.cuda.synchronize()
+    assert moe.moe_sync_status(ws) in (moe.MOE_OK, moe.MOE_EMISSING)
+    assert np.array_equal(c.tables()[2].cpu().numpy(), ref)
+    ws.set_fused_heat(False)
+    moe.moe_group(torch.from_numpy(ids).cuda(), T, k, E, 0, c, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(c.tables()[2].cpu().numpy(), ref)
+
+
+def test_fused_heat_in_layer_forward_bit_exact():
+    """The decode window's fused top-k + grouping kernel adds the heat update of its ids."""
+    from serving_router_top_gb300 import inputs as I
+    from serving_router_top_gb300.model import ModelState
+    w = I.WORKLOADS["decode_t4_h2048_e512_k10"]
+    st = ModelState(w, layers=2)
+    E = w.shape.E
+    g = np.random.default_rng(7)
+    heat = (g.random(2 * E) * 20).astype(F32)
+    set_heat(st.cache, heat)
+    ref = heat.copy()
+    st.ws.set_fused_heat(True)
+    y = torch.zeros((w.T, w.shape.H), dtype=torch.float32, device="cuda")
+    for step in range(4):
+        layer = step % 2
+        x = torch.from_numpy(I.activations(w.seed, step, w.T, w.shape.H).view(np.int16)).cuda()
+        st.forward(layer, x, y, w.T)
+        ids = st.ws.routing(w.T)[1].cpu().numpy()
+        opol.heat_update(ref, ids, layer, E)
+    assert moe.moe_sync_status(st.ws) == moe.MOE_OK
+    assert np.array_equal(st.cache.tables()[2].cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("L,E,seed", [(1, 4, 0), (3, 37, 1), (8, 256, 2), (48, 512, 3)])
 def test_plan_swaps_bit_exact(L, E, seed):
     g = np.random.default_rng(seed)
