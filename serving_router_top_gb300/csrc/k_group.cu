@@ -438,12 +438,14 @@ int launch_topk_group(const float* logits, int T, int k, int E, int layer, moe_c
   int G = 32 / Tp;
   while (G > 1 && G * k > 128) G >>= 1;
   const int per = ((E + G - 1) / G + 31) / 32;  // logits per lane of a warp's slice
-  auto args = [&](auto kern) {
-    static bool attr = false;
-    if (!attr) {
+  // one shared-memory opt-in per instantiation: the instantiations share one
+  // function-pointer type, so a flag in this lambda would be set by the first alone
+  static bool attr[6] = {false, false, false, false, false, false};
+  auto args = [&](auto kern, int which) {
+    if (!attr[which]) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024) != cudaSuccess)
         return cudaErrorInvalidValue;
-      attr = true;
+      attr[which] = true;
     }
     return launch_pdl(kern, dim3(1), dim3(1024), smem, s, G, logits, ws->topk_w, ws->topk_ids, T, k, E, layer,
                       c ? c->resid : nullptr, c ? c->stage : nullptr, c ? c->slots : nullptr,
@@ -453,12 +455,12 @@ int launch_topk_group(const float* logits, int T, int k, int E, int layer, moe_c
                       c ? ws->tail_skip : 0, c && ws->fused_heat ? c->heat + size_t(layer) * E : nullptr);
   };
   cudaError_t rc;
-  if (per <= 1) rc = args(k_topk_group<1>);
-  else if (per <= 2) rc = args(k_topk_group<2>);
-  else if (per <= 4) rc = args(k_topk_group<4>);
-  else if (per <= 8) rc = args(k_topk_group<8>);
-  else if (per <= 16) rc = args(k_topk_group<16>);
-  else rc = args(k_topk_group<32>);
+  if (per <= 1) rc = args(k_topk_group<1>, 0);
+  else if (per <= 2) rc = args(k_topk_group<2>, 1);
+  else if (per <= 4) rc = args(k_topk_group<4>, 2);
+  else if (per <= 8) rc = args(k_topk_group<8>, 3);
+  else if (per <= 16) rc = args(k_topk_group<16>, 4);
+  else rc = args(k_topk_group<32>, 5);
   return rc == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
 

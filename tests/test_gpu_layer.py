@@ -192,6 +192,27 @@ def test_tail_skip_rejects_negative_rank():
         st.ws.set_tail_skip(-1)
 
 
+@pytest.mark.parametrize("T,E,k", [(4, 512, 10), (12, 64, 10), (32, 64, 6)])
+def test_fused_topk_group_all_ties(T, E, k):
+    """Router weights zeroed and no bias: every logit is 0, so each token takes experts
+    0..k-1 with weights 1/k (ties to the lower id), through the fused top-k + grouping."""
+    from serving_router_top_gb300.model import ModelState
+    w = I.small_workload(T=T, H=128, I=64, E=E, k=k, I_shared=0, zipf_s=0.0, resident_frac=1.0, seed=2)
+    st = ModelState(w)
+    st.layers[0].w_router.zero_()
+    st.layers[0].bias.zero_()
+    x = torch.from_numpy(I.activations(w.seed, 0, T, 128).view(np.int16)).cuda()
+    y = torch.zeros((T, 128), dtype=torch.float32, device="cuda")
+    st.forward(0, x, y, T, mode=moe.MOE_MODE_DECODE)
+    assert moe.moe_sync_status(st.ws) == moe.MOE_OK
+    _, ids_t, w_t = st.ws.routing(T)
+    assert np.array_equal(ids_t.cpu().numpy(), np.tile(np.arange(k, dtype=np.int32), (T, 1)))
+    assert np.all(w_t.cpu().numpy() == np.float32(1.0) / np.float32(k))
+    exp_, off, _, _, ent_tok, _ = st.ws.groups(T)
+    assert exp_.tolist() == list(range(k)) and off.tolist() == [T * r for r in range(k + 1)]
+    assert ent_tok.tolist() == list(range(T)) * k
+
+
 def test_missing_expert_is_reported():
     from serving_router_top_gb300.model import ModelState
     w = I.small_workload(T=6, H=128, I=64, E=12, k=3, I_shared=0, resident_frac=0.25, seed=3)
@@ -255,7 +276,11 @@ def test_large_expert_layer_decode_batch64_sampled():
 @pytest.mark.parametrize("T,H,I_,E,k,frac", [
     (1, 2048, 512, 512, 10, 0.5),   # eight warps per token
     (4, 2048, 512, 512, 10, 0.5),   # the decode window: eight warps per token
+    (8, 256, 128, 40, 7, 0.5),      # four warps per token, E not a multiple of the slices
+    (12, 256, 128, 1000, 10, 0.5),  # two warps per token, 32 logits per lane, 120 entries
+    (3, 128, 64, 16, 16, 1.0),      # k = E = 16: every expert
     (16, 256, 128, 64, 6, 0.4),     # two warps per token
+    (16, 256, 128, 64, 8, 0.5),     # 128 entries
     (32, 256, 128, 40, 7, 0.6),     # one warp per token, E not a multiple of the slices
 ])
 def test_fused_topk_group_equals_separate_kernels(T, H, I_, E, k, frac):
