@@ -476,3 +476,79 @@ def test_tail_skip_all_resident_changes_nothing():
     a = layer.moe_layer(li.x, li.w_router, li.bias, s.k, experts.__getitem__, s.H, s.I)
     b = layer.moe_layer(li.x, li.w_router, li.bias, s.k, experts.__getitem__, s.H, s.I, tail_skip=1)
     assert np.array_equal(a.y, b.y) and (b.src == layer.SRC_RESIDENT).all()
+
+
+# ---------------------------------------------------------------- global LRU (FreeToken notes, 3.3 and 4)
+
+def _lru_run(calls, nslots, K, E, resid=None, owner=None):
+    """Drive the oracle LRU through calls of (layer, [experts]); returns the hit/miss flags per
+    call and the final tables.  The lookup is the oracle's (resident or not)."""
+    from oracle import lru
+    L = 1 + max(l for l, _ in calls)
+    resid = np.full(L * E, -1, dtype=np.int32) if resid is None else resid
+    owner = np.full(nslots, -1, dtype=np.int32) if owner is None else owner
+    st = lru.new_state(nslots)
+    flags = []
+    for layer, exps in calls:
+        exps = sorted(set(exps))
+        slot, src = layer_mod.lookup(np.array(exps), layer, E, resid)
+        src = np.where(src == layer_mod.SRC_MISSING, layer_mod.SRC_STAGED, src)   # misses come from staging
+        flags.append([bool(s == layer_mod.SRC_RESIDENT) for s in src])
+        plan = lru.plan_call(st, owner, layer, exps, src, slot, K, E)
+        lru.apply(resid, owner, plan, E)
+    return flags, resid, owner
+
+
+layer_mod = layer
+
+
+def test_lru_single_accesses_match_textbook_lru():
+    """One expert per call: the hit sequence is that of a textbook LRU of the same capacity
+    (an ordered dict: a hit moves the key to the back, a miss evicts the front when full)."""
+    import collections
+    g = np.random.default_rng(3)
+    E, L, C = 20, 2, 6
+    calls = [(int(g.integers(L)), [int(min(E - 1, g.zipf(1.3) - 1))]) for _ in range(400)]
+    flags, _, _ = _lru_run(calls, C, K=4, E=E)
+    od = collections.OrderedDict()
+    ref = []
+    for layer, (e,) in calls:
+        key = (layer, e)
+        if key in od:
+            od.move_to_end(key)
+            ref.append(True)
+        else:
+            ref.append(False)
+            if len(od) == C:
+                od.popitem(last=False)
+            od[key] = True
+    assert [f[0] for f in flags] == ref
+
+
+def test_lru_batch_worked_by_hand():
+    """Three slots, one layer, E = 8.  Call 1 {1,2}: both miss, fill empty slots 0, 1.
+    Call 2 {2,3}: 2 hits; 3 fills empty slot 2.  Call 3 {4,5}: the victims are slots the call
+    did not use, oldest first: slot 0 (expert 1, last used in call 1) then slot 1 (expert 2,
+    call 2); 4 takes slot 0, 5 takes slot 1.  Call 4 {1}: slot 2 (expert 3, call 2) is the
+    oldest; 1 takes it."""
+    flags, resid, owner = _lru_run([(0, [1, 2]), (0, [2, 3]), (0, [4, 5]), (0, [1])], 3, K=4, E=8)
+    assert flags == [[False, False], [True, False], [False, False], [False]]
+    assert owner.tolist() == [4, 5, 1]
+    assert [int(resid[e]) for e in range(8)] == [-1, 2, -1, -1, 0, 1, -1, -1]
+
+
+def test_lru_admits_at_most_k_and_keeps_the_call_hits():
+    """Five misses with K = 2: only the first two (ascending expert id) are admitted; a
+    slot the call hit is never a victim."""
+    from oracle import lru
+    E, nslots = 16, 4
+    resid = np.full(E, -1, dtype=np.int32)
+    owner = np.array([0, 1, 2, 3], dtype=np.int32)
+    resid[:4] = [0, 1, 2, 3]
+    st = lru.new_state(nslots)
+    exps = [0, 9, 10, 11, 12, 13]
+    slot, src = layer_mod.lookup(np.array(exps), 0, E, resid)
+    src = np.where(src == layer_mod.SRC_MISSING, layer_mod.SRC_STAGED, src)
+    plan = lru.plan_call(st, owner, 0, exps, src, slot, 2, E)
+    assert [(p.hot_expert, p.cold_flat, p.slot) for p in plan] == [(9, 1, 1), (10, 2, 2)]
+    assert st.tick.tolist() == [1, 1, 1, 0]
