@@ -134,7 +134,9 @@ int moe_cache_fill(moe_cache* c, const uint8_t* mask_host, int staging);
 
 /* Device pointers to the cache's tables (valid for the cache's lifetime):
  * resid / stage int32 [L*E] (slot or -1), heat fp32 [L*E], slot_owner int32
- * [nslots] (l*E+e or -1), slot and staging pool bases. */
+ * [nslots] (l*E+e or -1), slot and staging pool bases; the global LRU's
+ * lru_tick uint32 [nslots] (the LRU clock at each slot's last use, 0: never)
+ * and lru_clock uint32 [1] (layer calls planned so far). */
 typedef struct {
   int32_t* resid;
   int32_t* stage;
@@ -144,6 +146,8 @@ typedef struct {
   void* staging;
   size_t blob_bytes;
   int L, E, nslots, nstaging;
+  uint32_t* lru_tick;
+  uint32_t* lru_clock;
 } moe_cache_view;
 int moe_cache_get_view(const moe_cache* c, moe_cache_view* out);
 
@@ -361,6 +365,35 @@ int cache_plan_swaps_noalloc(float* heat_dev, const int32_t* resid_dev, int L, i
  *   No host synchronisation; n_dev is read on the device. */
 int moe_cache_apply_swaps(moe_cache* c, const moe_swap* plan_dev, const int32_t* n_dev, moe_stream_t compute,
                           moe_stream_t copy);
+
+/* Global LRU over the slots (FreeToken reading notes, section 3.3: one LRU for
+ * every layer's (layer, expert) -- a hit refreshes its recency, a fill admits
+ * the newly chosen expert, the least recently used is evicted; section 4: one
+ * pass finds K victim candidates and the misses take the first q <= K).  Call
+ * after a layer call's grouping on ws (moe_group, moe_layer_forward) for layer
+ * `layer`: advances the cache's LRU clock, marks the slots of the call's
+ * resident groups as used now, then writes into plan_dev (device moe_swap[K])
+ * and *n_dev (device int32) the admissions: the call's i-th miss (a group that
+ * is staged or missing, in group order) into the i-th victim, the victims
+ * being the slots this call did not use, empty slots first, then least
+ * recently used first, ties to the lower slot.  In an entry, `layer` and
+ * hot_expert name the admitted expert, cold_expert the evicted one as
+ * layer * E + expert (-1: the slot was empty), slot the slot, diff is 0; the
+ * slots taken count as used now.  1 <= K <= 32, else MOE_EINVAL.  The clock
+ * is 32-bit: past 2^32 - 2 calls the device records MOE_ERANGE.  Async on
+ * `stream`; execute the plan with moe_cache_apply_lru. */
+int cache_lru_plan(moe_cache* c, const moe_ws* ws, int layer, int K, moe_swap* plan_dev, int32_t* n_dev,
+                   moe_stream_t stream);
+
+/* Executes an LRU plan with the publish-after-copy order of
+ * moe_cache_apply_swaps (evicted entries cleared on `compute`; blobs copied
+ * from the backing store on `copy` after that; admitted entries published on
+ * `compute` after the copies), the evicted expert given by its flat id.  An
+ * entry whose evicted expert does not own its slot (or whose slot is not
+ * empty when no expert is named) is skipped, as moe_cache_apply_swaps skips
+ * an inconsistent entry. */
+int moe_cache_apply_lru(moe_cache* c, const moe_swap* plan_dev, const int32_t* n_dev, moe_stream_t compute,
+                        moe_stream_t copy);
 
 #ifdef __cplusplus
 }

@@ -16,9 +16,9 @@ Readings (listed in the design notes):
   * one call: the clock advances, the call's hits are refreshed, then its
     misses -- groups neither resident nor dropped by the tail skip, in group
     order (ascending expert id) -- are admitted into the victims, which are the
-    K slots the call did not use, empty slots first, then by (tick, slot)
-    ascending; q = min(misses, victims) admissions, the i-th miss taking the
-    i-th victim;
+    K slots the call did not use, empty slots first (in slot order), then by
+    (tick, slot) ascending; q = min(misses, victims) admissions, the i-th miss
+    taking the i-th victim;
   * an admitted expert takes the slot (tick = the call's clock); the expert it
     evicts, if any, loses its residency; a miss beyond the first K stays out
     until a later call admits it.
@@ -52,9 +52,9 @@ def new_state(nslots: int) -> LruState:
 
 
 def victims(state: LruState, slot_owner: np.ndarray, K: int) -> List[int]:
-    """The K slots not used by the current call, empty first, then oldest (tick, slot)."""
+    """The K slots not used by the current call: empty ones by slot, then the others by (tick, slot)."""
     cand = [s for s in range(state.tick.size) if state.tick[s] < state.clock]
-    cand.sort(key=lambda s: (0 if slot_owner[s] < 0 else 1, int(state.tick[s]), s))
+    cand.sort(key=lambda s: (0, 0, s) if slot_owner[s] < 0 else (1, int(state.tick[s]), s))
     return cand[:K]
 
 

@@ -126,7 +126,9 @@ int moe_cache_create(moe_cache** out, int L, int E, int H, int I, int nslots, in
             cudaMalloc(&c->slot_owner, size_t(nslots > 0 ? nslots : 1) * 4) == cudaSuccess &&
             cudaMalloc(&c->staging_owner, size_t(nstaging > 0 ? nstaging : 1) * 4) == cudaSuccess &&
             cudaMalloc(&c->stats, size_t(L) * kStats * 8) == cudaSuccess &&
+            cudaMalloc(&c->lru_tick, size_t(nslots > 0 ? nslots : 1) * 4 + 4) == cudaSuccess &&
             cudaMalloc(&c->plan_scratch, c->plan_scratch_bytes) == cudaSuccess;
+  if (ok) c->lru_clock = c->lru_tick + (nslots > 0 ? nslots : 1);
   if (ok && nslots > 0) ok = cudaMalloc(&c->slots, size_t(nslots) * c->blob_bytes) == cudaSuccess;
   if (ok && nstaging > 0) ok = cudaMalloc(&c->staging, size_t(nstaging) * c->blob_bytes) == cudaSuccess;
   if (ok) ok = cudaEventCreateWithFlags(&c->ev_unmapped, cudaEventDisableTiming) == cudaSuccess &&
@@ -138,6 +140,7 @@ int moe_cache_create(moe_cache** out, int L, int E, int H, int I, int nslots, in
          cudaMemset(c->slot_owner, 0xff, size_t(nslots > 0 ? nslots : 1) * 4) == cudaSuccess &&
          cudaMemset(c->staging_owner, 0xff, size_t(nstaging > 0 ? nstaging : 1) * 4) == cudaSuccess &&
          cudaMemset(c->stats, 0, size_t(L) * kStats * 8) == cudaSuccess &&
+         cudaMemset(c->lru_tick, 0, size_t(nslots > 0 ? nslots : 1) * 4 + 4) == cudaSuccess &&
          cudaMemset(c->plan_scratch, 0, c->plan_scratch_bytes) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
@@ -156,6 +159,7 @@ int moe_cache_destroy(moe_cache* c) {
   cudaFree(c->slot_owner);
   cudaFree(c->staging_owner);
   cudaFree(c->stats);
+  cudaFree(c->lru_tick);
   cudaFree(c->plan_scratch);
   cudaFree(c->slots);
   cudaFree(c->staging);
@@ -230,6 +234,8 @@ int moe_cache_get_view(const moe_cache* c, moe_cache_view* v) {
   v->E = c->E;
   v->nslots = c->nslots;
   v->nstaging = c->nstaging;
+  v->lru_tick = c->lru_tick;
+  v->lru_clock = c->lru_clock;
   return MOE_OK;
 }
 
@@ -533,6 +539,21 @@ int moe_cache_apply_swaps(moe_cache* c, const moe_swap* plan_dev, const int32_t*
   // each planned swap reuses a distinct slot, so at most min(nslots, 4096) swaps exist
   return launch_apply_swaps(c, plan_dev, n_dev, c->nslots < 4096 ? c->nslots : 4096,
                             reinterpret_cast<cudaStream_t>(compute), reinterpret_cast<cudaStream_t>(copy));
+}
+
+int cache_lru_plan(moe_cache* c, const moe_ws* ws, int layer, int K, moe_swap* plan_dev, int32_t* n_dev,
+                   moe_stream_t stream) {
+  if (!c || !ws || !plan_dev || !n_dev || layer < 0 || layer >= c->L || K < 1 || K > kLruMaxK || c->nslots < 1 ||
+      c->nslots >= (1 << 24))
+    return MOE_EINVAL;
+  return launch_lru_plan(c, ws, layer, K, plan_dev, n_dev, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_cache_apply_lru(moe_cache* c, const moe_swap* plan_dev, const int32_t* n_dev, moe_stream_t compute,
+                        moe_stream_t copy) {
+  if (!c || !plan_dev || !n_dev || !c->backing) return MOE_EINVAL;
+  return launch_apply_swaps(c, plan_dev, n_dev, kLruMaxK, reinterpret_cast<cudaStream_t>(compute),
+                            reinterpret_cast<cudaStream_t>(copy), /*flat_cold=*/true);
 }
 
 }  // extern "C"

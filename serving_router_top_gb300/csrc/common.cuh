@@ -224,6 +224,8 @@ struct moe_cache {
   uint8_t* slots;             // nslots * blob_bytes
   uint8_t* staging;           // nstaging * blob_bytes
   unsigned long long* stats;  // [L][kStats]
+  uint32_t* lru_tick;         // [nslots] global LRU: the clock value of each slot's last use (0: never)
+  uint32_t* lru_clock;        // [1] global LRU: layer calls planned so far
   int32_t* plan_keys_scratch; // policy scratch (candidates), allocated at creation
   void* plan_scratch;
   size_t plan_scratch_bytes;

@@ -35,8 +35,13 @@ int launch_prefill_streamed(const moe_layer_desc* d, moe_cache* c, const uint16_
 // Policy.
 int launch_heat_update(moe_cache* c, const int32_t* ids, int T, int k, int layer, int32_t* err, cudaStream_t s);
 int launch_plan_swaps(moe_cache* c, const moe_policy_cfg* p, moe_swap* plan, int32_t* n, cudaStream_t s);
+// flat_cold: the plan's cold_expert is the evicted expert's layer * E + expert
+// (-1: an empty slot), as global LRU plans write it.
 int launch_apply_swaps(moe_cache* c, const moe_swap* plan, const int32_t* n, int max_swaps, cudaStream_t compute,
-                       cudaStream_t copy);
+                       cudaStream_t copy, bool flat_cold = false);
+// Global LRU: refresh the last call's hits and plan its admissions (k_lru.cu).
+constexpr int kLruMaxK = 32;
+int launch_lru_plan(moe_cache* c, const moe_ws* ws, int layer, int K, moe_swap* plan, int32_t* n, cudaStream_t s);
 // Planner kernels (defined with the policy), also launched on caller tables.
 __global__ void __launch_bounds__(1024) k_plan_layer(float* __restrict__ heat, const int32_t* __restrict__ resid, int E,
                                                      int P, float threshold, float decay,

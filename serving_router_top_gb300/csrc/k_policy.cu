@@ -187,13 +187,26 @@ int launch_plan_swaps(moe_cache* c, const moe_policy_cfg* p, moe_swap* plan, int
 }
 
 // ----------------------------------------------------------- apply swaps
+// flat_cold: cold_expert is layer * E + expert of the evicted expert, or -1
+// when the slot is empty (global LRU plans, whose victims may be in any layer).
 __global__ void k_swap_unmap(const moe_swap* __restrict__ plan, const int32_t* __restrict__ n, int32_t* resid,
-                             int32_t* slot_owner, int E, int L, int nslots, int32_t* err) {
+                             int32_t* slot_owner, int E, int L, int nslots, int32_t* err, int flat_cold) {
   const int cnt = *n;
   for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
     const moe_swap sw = plan[i];
-    if (sw.layer < 0 || sw.layer >= L || sw.cold_expert < 0 || sw.cold_expert >= E || sw.slot < 0 ||
-        sw.slot >= nslots) { set_error(err, MOE_ERANGE); continue; }
+    if (sw.layer < 0 || sw.layer >= L || sw.slot < 0 || sw.slot >= nslots) { set_error(err, MOE_ERANGE); continue; }
+    if (flat_cold) {
+      if (sw.cold_expert < -1 || sw.cold_expert >= L * E) { set_error(err, MOE_ERANGE); continue; }
+      if (sw.cold_expert < 0) {  // an empty slot: nothing to unmap
+        if (slot_owner[sw.slot] != -1) set_error(err, MOE_ERANGE);
+        continue;
+      }
+      if (resid[sw.cold_expert] != sw.slot) { set_error(err, MOE_ERANGE); continue; }
+      resid[sw.cold_expert] = -1;
+      slot_owner[sw.slot] = -1;
+      continue;
+    }
+    if (sw.cold_expert < 0 || sw.cold_expert >= E) { set_error(err, MOE_ERANGE); continue; }
     const size_t f = size_t(sw.layer) * E + sw.cold_expert;
     if (resid[f] != sw.slot) { set_error(err, MOE_ERANGE); continue; }
     resid[f] = -1;
@@ -233,8 +246,9 @@ __global__ void k_swap_publish(const moe_swap* __restrict__ plan, const int32_t*
 }
 
 int launch_apply_swaps(moe_cache* c, const moe_swap* plan, const int32_t* n, int max_swaps, cudaStream_t compute,
-                       cudaStream_t copy) {
-  k_swap_unmap<<<1, 256, 0, compute>>>(plan, n, c->resid, c->slot_owner, c->E, c->L, c->nslots, nullptr);
+                       cudaStream_t copy, bool flat_cold) {
+  k_swap_unmap<<<1, 256, 0, compute>>>(plan, n, c->resid, c->slot_owner, c->E, c->L, c->nslots, nullptr,
+                                       flat_cold ? 1 : 0);
   MOE_LAUNCH_CHECK();
   MOE_CUDA_TRY(cudaEventRecord(c->ev_unmapped, compute));
   MOE_CUDA_TRY(cudaStreamWaitEvent(copy, c->ev_unmapped, 0));

@@ -27,7 +27,7 @@ EXPORTED = (
     "moe_sync_status", "moe_strerror", "moe_route", "moe_group", "moe_layer_forward", "cache_heat_update",
     "cache_plan_swaps", "moe_cache_apply_swaps", "moe_ws_set_profiling", "moe_ws_kernel_times",
     "cache_plan_swaps_noalloc", "moe_residual_rmsnorm", "moe_layer_forward_streamed", "moe_ws_set_tail_skip",
-    "moe_ws_set_fused_heat",
+    "moe_ws_set_fused_heat", "cache_lru_plan", "moe_cache_apply_lru",
 )
 
 
@@ -49,7 +49,8 @@ class moe_layer_desc(C.Structure):
 class moe_cache_view(C.Structure):
     _fields_ = [("resid", C.c_void_p), ("stage", C.c_void_p), ("heat", C.c_void_p), ("slot_owner", C.c_void_p),
                 ("slots", C.c_void_p), ("staging", C.c_void_p), ("blob_bytes", C.c_size_t), ("L", C.c_int),
-                ("E", C.c_int), ("nslots", C.c_int), ("nstaging", C.c_int)]
+                ("E", C.c_int), ("nslots", C.c_int), ("nstaging", C.c_int), ("lru_tick", C.c_void_p),
+                ("lru_clock", C.c_void_p)]
 
 
 class moe_ws_view(C.Structure):
@@ -107,6 +108,8 @@ def load() -> C.CDLL:
         "moe_ws_set_profiling": (I, [P, I]),
         "moe_ws_set_tail_skip": (I, [P, I]),
         "moe_ws_set_fused_heat": (I, [P, I]),
+        "cache_lru_plan": (I, [P, P, I, I, P, P, P]),
+        "moe_cache_apply_lru": (I, [P, P, P, P, P]),
         "moe_ws_kernel_times": (I, [P, I, P, P, C.POINTER(C.c_int)]),
     }
     for name, (res, args) in sig.items():
@@ -220,6 +223,11 @@ class Cache:
         LE = self.L * self.E
         return (device_view(self.view.resid, (LE,), "int32", self), device_view(self.view.stage, (LE,), "int32", self),
                 device_view(self.view.heat, (LE,), "float32", self))
+
+    def lru_tables(self):
+        """Torch views of the global LRU's slot ticks (uint32 as int32 [nslots]) and clock (int32 [1])."""
+        return (device_view(self.view.lru_tick, (max(1, self.view.nslots),), "int32", self),
+                device_view(self.view.lru_clock, (1,), "int32", self))
 
     def stats(self) -> np.ndarray:
         """int64 [L, 5]: groups looked up, resident hits, staged, missing, skipped by the tail skip."""
@@ -361,6 +369,17 @@ def cache_plan_swaps_noalloc(heat_dev, resid_dev, L: int, E: int, threshold: flo
     cfg = moe_policy_cfg(threshold, max_swaps, decay)
     _check(load().cache_plan_swaps_noalloc(_ptr(heat_dev), _ptr(resid_dev), L, E, C.byref(cfg), _ptr(plan_dev),
                                            _ptr(n_dev), _stream(stream)), "cache_plan_swaps_noalloc")
+
+
+def cache_lru_plan(cache: Cache, ws: Workspace, layer: int, K: int, plan_dev, n_dev, stream=None) -> None:
+    """After a layer call's grouping on ws: refresh its hits, plan its admissions into the K LRU victims."""
+    _check(load().cache_lru_plan(cache.handle, ws.handle, layer, K, _ptr(plan_dev), _ptr(n_dev), _stream(stream)),
+           "cache_lru_plan")
+
+
+def moe_cache_apply_lru(cache: Cache, plan_dev, n_dev, compute=None, copy=None) -> None:
+    _check(load().moe_cache_apply_lru(cache.handle, _ptr(plan_dev), _ptr(n_dev), _stream(compute), _stream(copy)),
+           "moe_cache_apply_lru")
 
 
 def moe_cache_apply_swaps(cache: Cache, plan_dev, n_dev, compute=None, copy=None) -> None:

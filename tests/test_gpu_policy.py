@@ -188,3 +188,79 @@ def test_apply_swaps_publishes_after_copy():
     for f in np.flatnonzero(resid >= 0):
         s = int(resid[f])
         assert torch.equal(pool[s * nb:(s + 1) * nb], backing[f * nb:(f + 1) * nb]), f
+
+
+# ------------------------------------------------------------ global LRU
+# (FreeToken reading notes, 3.3 and 4: one LRU for all layers; K victims per pass)
+
+def _zipf_ids(g, T, k, E, perm, s=1.1):
+    p = 1.0 / np.arange(1, E + 1) ** s
+    p = p[np.argsort(perm)]
+    p /= p.sum()
+    return np.stack([g.choice(E, k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("L,E,nslots,T,k,K,calls", [
+    (3, 24, 10, 2, 3, 4, 60),       # a small pool, K below the misses of many calls
+    (4, 64, 40, 4, 6, 32, 80),      # empty slots at the start, admissions across layers
+    (2, 512, 300, 4, 10, 32, 40),   # the decode window's routing shape
+])
+def test_lru_plans_and_residency_bit_exact(L, E, nslots, T, k, K, calls):
+    from oracle import layer as olayer, lru
+    H, I_ = 64, 64
+    nb = moe.moe_blob_bytes(H, I_)
+    g = np.random.default_rng(nslots)
+    backing = torch.from_numpy(g.integers(0, 256, size=L * E * nb, dtype=np.uint8)).cuda()
+    c = moe.Cache(L, E, H, I_, nslots, 0, backing, True)
+    resident = np.zeros((L, E), dtype=bool)
+    resident[0, : nslots // 2] = True             # half the slots filled, the rest empty
+    c.fill(resident.astype(np.uint8))
+    ws = moe.Workspace(T, H, I_, E, k, 0)
+    plan = torch.zeros(K * 5, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    resid_o = c.tables()[0].cpu().numpy().copy()
+    view = moe.device_view(c.view.slot_owner, (nslots,), "int32", c)
+    owner_o = view.cpu().numpy().copy()
+    st = lru.new_state(nslots)
+    tick_t, clock_t = c.lru_tables()
+    perm = g.permutation(E)
+    for i in range(calls):
+        layer = i % L
+        if i % 20 == 0:
+            perm = g.permutation(E)                  # the hot set drifts
+        ids = _zipf_ids(g, T, k, E, perm)
+        moe.moe_group(torch.from_numpy(ids).cuda(), T, k, E, layer, c, ws)
+        moe.cache_lru_plan(c, ws, layer, K, plan, n)
+        moe.moe_cache_apply_lru(c, plan, n)
+        torch.cuda.synchronize()
+        assert moe.moe_sync_status(ws) in (moe.MOE_OK, moe.MOE_EMISSING)   # misses have no staging copy here
+        grp = olayer.expert_groups(ids)
+        slot, src = olayer.lookup(grp.experts, layer, E, resid_o)
+        ref = lru.plan_call(st, owner_o, layer, grp.experts, src, slot, K, E)
+        lru.apply(resid_o, owner_o, ref, E)
+        cnt = int(n.item())
+        got = plan.cpu().numpy().view(moe.SWAP_DTYPE)[:cnt]
+        assert cnt == len(ref), (i, cnt, len(ref))
+        for a, b in zip(got, ref):
+            assert (int(a["layer"]), int(a["hot_expert"]), int(a["cold_expert"]), int(a["slot"])) == \
+                   (b.layer, b.hot_expert, b.cold_flat, b.slot), i
+        assert np.array_equal(tick_t.cpu().numpy().astype(np.int64), st.tick), i
+        assert int(clock_t.item()) == st.clock
+        assert np.array_equal(c.tables()[0].cpu().numpy(), resid_o), i
+        assert np.array_equal(view.cpu().numpy(), owner_o), i
+    # the admitted blobs are the backing store's
+    slots_t = moe.device_view(c.view.slots, (nslots * nb,), "uint8", c)
+    for s in g.choice(nslots, 5, replace=False):
+        f = int(owner_o[s])
+        if f >= 0:
+            assert torch.equal(slots_t[s * nb:(s + 1) * nb], backing[f * nb:(f + 1) * nb])
+
+
+def test_lru_plan_rejects_bad_k():
+    c, _, _ = make_cache(1, 8, np.ones((1, 8), dtype=bool))
+    ws = moe.Workspace(2, 64, 64, 8, 2, 0)
+    plan = torch.zeros(40 * 5, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for K in (0, 33):
+        with pytest.raises(moe.MoeError):
+            moe.cache_lru_plan(c, ws, 0, K, plan, n)
