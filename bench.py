@@ -294,6 +294,56 @@ def kernel_time_pass(st, step, set_input, flusher, steps: int, stream):
     return {n: v / steps for n, v in sums.items()}, per_step
 
 
+def measure_policy(st, xs, ys, T, stream, n=16):
+    """The cache policies' device costs on the bench's cache (CUDA events on the launching
+    stream, medians over n calls): the heat policy's planning round over all layers, and the
+    global LRU's per-call plan (K = 32 victims) and its execution (unmap, blob copies from the
+    backing pool on a copy stream, publish), each after a real layer call whose groups it
+    uses.  Run after the timed region: the LRU admissions change the residency."""
+    import torch
+    from serving_router_top_gb300 import moe
+    K = 32
+    plan = torch.zeros(96 * 5, dtype=torch.int32, device="cuda")
+    n_dev = torch.zeros(1, dtype=torch.int32, device="cuda")
+    copy_stream = torch.cuda.Stream()
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    heat_ms, plan_ms, apply_ms, admitted = [], [], [], 0
+    with torch.cuda.stream(stream):
+        for _ in range(n):
+            a, b = ev(), ev()
+            a.record(stream)
+            moe.cache_plan_swaps(st.cache, 1.5, 96, 0.7, plan, n_dev, stream=stream)
+            b.record(stream)
+            b.synchronize()
+            heat_ms.append(a.elapsed_time(b))
+        for i in range(n):
+            layer = i % st.L
+            st.forward(layer, xs[i % len(xs)], ys[layer], T, y_is_fp32=False, stream=stream)
+            a, b, c = ev(), ev(), ev()
+            a.record(stream)
+            moe.cache_lru_plan(st.cache, st.ws, layer, K, plan, n_dev, stream=stream)
+            b.record(stream)
+            moe.moe_cache_apply_lru(st.cache, plan, n_dev, compute=stream, copy=copy_stream)
+            c.record(stream)
+            c.synchronize()
+            plan_ms.append(a.elapsed_time(b))
+            apply_ms.append(b.elapsed_time(c))
+            admitted += int(n_dev.item())
+    rc = moe.moe_sync_status(st.ws)
+    if rc != moe.MOE_OK:
+        raise RuntimeError(f"device error in the policy pass: {moe.strerror(rc)}")
+    return {"heat_plan_round_us": 1e3 * statistics.median(heat_ms),
+            "heat_plan_scope": f"{st.L} layers x {st.E} experts, threshold 1.5, at most 96 swaps, decay 0.7",
+            "lru_plan_us": 1e3 * statistics.median(plan_ms),
+            "lru_apply_us": 1e3 * statistics.median(apply_ms),
+            "lru_admitted_per_call": admitted / n, "lru_K": K, "slots": st.cache.view.nslots,
+            "note": "CUDA events on the launching stream; the LRU's apply includes the blob copies of its "
+                    "admissions (the decode window's misses)"}
+
+
 def measure_prefill(args, peaks):
     """A short measurement of the prefill chunk (8192 tokens through one layer)."""
     import torch
@@ -557,6 +607,8 @@ def run_ours(args, w):
                 "d2h_bytes_per_step": T * s.H * 2},
         "gpu_launches": launches,
     }
+    with torch.cuda.stream(stream):
+        out["policy"] = measure_policy(st, xs, ys, T, stream)
     if not args.no_prefill:
         out["prefill"] = measure_prefill(args, peaks)
     if not args.no_cpu_baseline:

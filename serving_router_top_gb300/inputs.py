@@ -39,7 +39,7 @@ from typing import Dict, Optional, Tuple
 import numpy as np
 
 # Tensor tags keep the sub-streams of one seed apart.
-TAG_X, TAG_WR, TAG_BIAS, TAG_WSG, TAG_GATE, TAG_UP, TAG_DOWN, TAG_RESID, TAG_SHARED = range(1, 10)
+TAG_X, TAG_WR, TAG_BIAS, TAG_WSG, TAG_GATE, TAG_UP, TAG_DOWN, TAG_RESID, TAG_SHARED, TAG_TRACE = range(1, 11)
 SHARED_EXPERT_ID = 1 << 20  # expert id used for the shared expert's sub-stream
 
 
@@ -140,6 +140,19 @@ def resident_mask(seed: int, layer: int, E: int, frac: float) -> np.ndarray:
     mask = np.zeros(E, dtype=bool)
     mask[rng(seed, TAG_RESID, layer).permutation(E)[:n]] = True
     return mask
+
+
+def routing_trace(seed: int, L: int, E: int, k: int, T: int, steps: int, drift_every: int, s: float):
+    """Synthetic decode routing: for each step and layer (in that order), int32 ``[T, k]``
+    distinct expert ids per token, drawn without replacement with probability proportional
+    to ``rank^-s`` (Gumbel keys on ``zipf_bias``); the ranks are re-drawn every
+    ``drift_every`` steps, so the hot set drifts.  Yields ``(step, layer, ids)``."""
+    for step in range(steps):
+        epoch = step // drift_every
+        for layer in range(L):
+            bias = zipf_bias(seed, layer, E, s, epoch).astype(np.float64)
+            g = rng(seed, TAG_TRACE, step, layer).gumbel(size=(T, E))
+            yield step, layer, np.argsort(-(bias[None, :] + g), axis=1)[:, :k].astype(np.int32)
 
 
 @dataclasses.dataclass(frozen=True)
