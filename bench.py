@@ -400,8 +400,8 @@ def measure_prefill(args, peaks):
     total = sum(fl.values())
     del st
     torch.cuda.empty_cache()
-    streamed = {src: measure_prefill_streamed(w, xs, on_device) for src, on_device in (("device", True),
-                                                                                     ("pinned_host", False))}
+    streamed = {f"{src}_{nb}buf": measure_prefill_streamed(w, xs, on_device, buffers=nb)
+                for src, on_device in (("device", True), ("pinned_host", False)) for nb in (2, 1)}
     return {"workload": w.name, "tokens_per_s": T / (ms / 1e3), "ms_per_layer": ms,
             "tflops_dense_equiv": total / (ms / 1e3) / 1e12, "peak_tflops": peak,
             "peak_source": "measured bf16_tflops (burst); the GEMMs run kind::f16 on bf16/f16 operands",
@@ -409,10 +409,11 @@ def measure_prefill(args, peaks):
             "timing": f"{n} steps, CUDA graph, L2 flushed before each", "streamed": streamed}
 
 
-def measure_prefill_streamed(w, xs, on_device: bool, U: int = 64, n: int = 8):
+def measure_prefill_streamed(w, xs, on_device: bool, U: int = 64, n: int = 8, buffers: int = 2):
     """The same chunk with every expert of the layer streamed from the backing pool (HBM, or
-    pinned host memory over the host link) through two halves of the staging pool, units of U
-    experts: copies on a second stream overlap the grouped GEMMs of the previous unit."""
+    pinned host memory over the host link) through the staging pool in units of U experts:
+    with two buffers the copies on a second stream overlap the grouped GEMMs of the previous
+    unit; with one, each copy waits for them (the second buffer off)."""
     import torch
     from serving_router_top_gb300 import moe
     from serving_router_top_gb300.model import ModelState
@@ -424,12 +425,12 @@ def measure_prefill_streamed(w, xs, on_device: bool, U: int = 64, n: int = 8):
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for _ in range(2):
-            st.forward_streamed(0, x_in, y, T, U, y_is_fp32=False, stream=stream)
+            st.forward_streamed(0, x_in, y, T, U, y_is_fp32=False, stream=stream, buffers=buffers)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for i in range(n):
-            st.forward_streamed(0, xs[i % 2], y, T, U, y_is_fp32=False, stream=stream)
+            st.forward_streamed(0, xs[i % 2], y, T, U, y_is_fp32=False, stream=stream, buffers=buffers)
         e1.record(stream)
         torch.cuda.synchronize()
     rc = moe.moe_sync_status(st.ws)
@@ -438,6 +439,7 @@ def measure_prefill_streamed(w, xs, on_device: bool, U: int = 64, n: int = 8):
     ms = e0.elapsed_time(e1) / n
     nbytes = s.E * moe.moe_blob_bytes(s.H, s.I)
     out = {"backing": "device" if on_device else "pinned host", "units": f"{(s.E + U - 1) // U} of {U} experts",
+           "buffers": buffers,
            "ms_per_layer": ms, "tokens_per_s": T / (ms / 1e3), "weight_GBps": nbytes / (ms / 1e3) / 1e9,
            "timing": f"{n} calls back to back, events on the compute stream (its last wait covers the copies)"}
     del st

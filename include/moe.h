@@ -276,14 +276,18 @@ int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y
  * (one cudaMemcpyAsync of n*blob_bytes per unit, n <= U, from the cache's
  * backing pool, device or pinned host) into staging slots (u % 2)*U ..; stream
  * runs the grouped GEMMs of that unit's groups once they have landed.  The
- * shared expert runs with unit 0.  Same arguments, layout and result as
- * moe_layer_forward in prefill mode, plus: U >= 1 with 2*U <= the cache's
- * staging slots, a backing pool, and copy_stream a stream other than stream,
- * else MOE_EINVAL.  Both streams may be used again as soon as the call
- * returns; the staging slots' contents and table entries are left undefined
- * for lookups (the staging table itself is not changed). */
+ * shared expert runs with unit 0.  buffers = 2 double-buffers the units
+ * (unit u + 1 copies while unit u computes); buffers = 1 keeps one half, so
+ * each copy waits for the previous unit's GEMMs (the FreeToken notes'
+ * "second buffer off" ablation, section 5.3).  Same arguments, layout and
+ * result as moe_layer_forward in prefill mode, plus: U >= 1 with buffers*U <=
+ * the cache's staging slots, buffers 1 or 2, a backing pool, and copy_stream
+ * a stream other than stream, else MOE_EINVAL.  Both streams may be used again
+ * as soon as the call returns; the staging slots' contents and table entries
+ * are left undefined for lookups (the staging table itself is not changed). */
 int moe_layer_forward_streamed(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T,
-                               moe_cache* c, moe_ws* ws, int U, moe_stream_t stream, moe_stream_t copy_stream);
+                               moe_cache* c, moe_ws* ws, int U, int buffers, moe_stream_t stream,
+                               moe_stream_t copy_stream);
 
 /* Heat update (Strata page, "哪些专家能长期留在显存？": accumulate how often
  * each expert is routed to): heat[layer*E+e] = fl32(heat + (float)count_e)

@@ -442,10 +442,13 @@ static int forward_args_ok(const moe_layer_desc* d, const uint16_t* x, void* y, 
 }
 
 int moe_layer_forward_streamed(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T,
-                               moe_cache* c, moe_ws* ws, int U, moe_stream_t stream, moe_stream_t copy_stream) {
+                               moe_cache* c, moe_ws* ws, int U, int buffers, moe_stream_t stream,
+                               moe_stream_t copy_stream) {
   int rc;
   if ((rc = forward_args_ok(d, x, y, T, c, ws, true))) return rc;
-  if (U < 1 || 2 * U > c->nstaging || !c->backing || !copy_stream || copy_stream == stream) return MOE_EINVAL;
+  if (U < 1 || (buffers != 1 && buffers != 2) || buffers * U > c->nstaging || !c->backing || !copy_stream ||
+      copy_stream == stream)
+    return MOE_EINVAL;
   if (T == 0) return MOE_OK;
   const moe_layer_shape& s = d->s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -462,7 +465,8 @@ int moe_layer_forward_streamed(const moe_layer_desc* d, const uint16_t* x, void*
     ProfScope p(ws, "group", st);
     if ((rc = launch_group(ws->topk_ids, T, s.k, s.E, d->layer, c, ws, st, false))) return rc;
   }
-  return launch_prefill_streamed(d, c, x, y, y_is_fp32, T, U, ws, st, reinterpret_cast<cudaStream_t>(copy_stream));
+  return launch_prefill_streamed(d, c, x, y, y_is_fp32, T, U, buffers, ws, st,
+                                 reinterpret_cast<cudaStream_t>(copy_stream));
 }
 
 int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T, moe_cache* c,

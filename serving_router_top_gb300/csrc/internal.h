@@ -30,7 +30,7 @@ int launch_prefill_router(const moe_layer_desc* d, const uint16_t* x, int T, moe
 int launch_prefill_experts(const moe_layer_desc* d, const moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
                            moe_ws* ws, cudaStream_t s);
 int launch_prefill_streamed(const moe_layer_desc* d, moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
-                            int U, moe_ws* ws, cudaStream_t s, cudaStream_t cs);
+                            int U, int buffers, moe_ws* ws, cudaStream_t s, cudaStream_t cs);
 
 // Policy.
 int launch_heat_update(moe_cache* c, const int32_t* ids, int T, int k, int layer, int32_t* err, cudaStream_t s);

@@ -1310,7 +1310,7 @@ int launch_prefill_experts(const moe_layer_desc* d, const moe_cache* c, const ui
 // the staging pool; the unit's groups are bound to those slots and only they
 // run.  The shared expert runs with the first unit.
 int launch_prefill_streamed(const moe_layer_desc* d, moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
-                            int U, moe_ws* ws, cudaStream_t s, cudaStream_t cs) {
+                            int U, int buffers, moe_ws* ws, cudaStream_t s, cudaStream_t cs) {
   using namespace prefill;
   const moe_layer_shape& sh = d->s;
   prefill::Args a = base_args(d, T, ws);
@@ -1323,9 +1323,11 @@ int launch_prefill_streamed(const moe_layer_desc* d, moe_cache* c, const uint16_
   const int nunits = (sh.E + U - 1) / U;
   const uint8_t* pool = static_cast<const uint8_t*>(c->backing) + size_t(d->layer) * sh.E * c->blob_bytes;
   for (int u = 0; u < nunits; ++u) {
-    const int half = u & 1, n = sh.E - u * U < U ? sh.E - u * U : U;
+    // two buffers: unit u + 1 copies into the other half while unit u computes;
+    // one buffer: each copy waits for the previous unit's GEMMs
+    const int half = buffers == 2 ? (u & 1) : 0, n = sh.E - u * U < U ? sh.E - u * U : U;
     cudaEvent_t copied = c->ev_ring[half], used = c->ev_ring[2 + half];
-    if (u >= 2) MOE_CUDA_TRY(cudaStreamWaitEvent(cs, used, 0));
+    if (u >= buffers) MOE_CUDA_TRY(cudaStreamWaitEvent(cs, used, 0));
     MOE_CUDA_TRY(cudaMemcpyAsync(c->staging + size_t(half) * U * c->blob_bytes, pool + size_t(u) * U * c->blob_bytes,
                                  size_t(n) * c->blob_bytes, cudaMemcpyDefault, cs));
     MOE_CUDA_TRY(cudaEventRecord(copied, cs));

@@ -121,10 +121,11 @@ class ModelState:
         moe.moe_layer_forward(self.layers[layer].desc, x, y, y_is_fp32, T, self.cache, self.ws, mode, stream)
 
     def forward_streamed(self, layer: int, x: torch.Tensor, y: torch.Tensor, T: int, U: int,
-                         y_is_fp32: bool = True, stream=None) -> None:
+                         y_is_fp32: bool = True, stream=None, buffers: int = 2) -> None:
         """Prefill forward with the layer's experts streamed from the backing pool through the
-        staging pool in units of U (needs at least 2*U staging slots)."""
+        staging pool in units of U (needs at least buffers*U staging slots; buffers = 1 lets
+        each copy wait for the previous unit's GEMMs)."""
         if getattr(self, "_copy_stream", None) is None:
             self._copy_stream = torch.cuda.Stream()
         moe.moe_layer_forward_streamed(self.layers[layer].desc, x, y, y_is_fp32, T, self.cache, self.ws, U,
-                                       stream, self._copy_stream)
+                                       stream, self._copy_stream, buffers=buffers)

@@ -99,7 +99,7 @@ def load() -> C.CDLL:
         "moe_route": (I, [P, P, P, P, I, I, I, I, P, P, P, P]),
         "moe_group": (I, [P, I, I, I, I, P, P, P]),
         "moe_layer_forward": (I, [C.POINTER(moe_layer_desc), P, P, I, I, P, P, I, P]),
-        "moe_layer_forward_streamed": (I, [C.POINTER(moe_layer_desc), P, P, I, I, P, P, I, P, P]),
+        "moe_layer_forward_streamed": (I, [C.POINTER(moe_layer_desc), P, P, I, I, P, P, I, I, P, P]),
         "cache_heat_update": (I, [P, P, I, I, I, P, P]),
         "cache_plan_swaps": (I, [P, C.POINTER(moe_policy_cfg), P, P, P]),
         "cache_plan_swaps_noalloc": (I, [P, P, I, I, C.POINTER(moe_policy_cfg), P, P, P]),
@@ -331,9 +331,9 @@ def moe_layer_forward(desc: moe_layer_desc, x, y, y_is_fp32: bool, T: int, cache
 
 
 def moe_layer_forward_streamed(desc: moe_layer_desc, x, y, y_is_fp32: bool, T: int, cache: Cache, ws: Workspace,
-                               U: int, stream=None, copy_stream=None) -> None:
+                               U: int, stream=None, copy_stream=None, buffers: int = 2) -> None:
     _check(load().moe_layer_forward_streamed(C.byref(desc), _ptr(x), _ptr(y), 1 if y_is_fp32 else 0, T, cache.handle,
-                                             ws.handle, U, _stream(stream), _stream(copy_stream)),
+                                             ws.handle, U, buffers, _stream(stream), _stream(copy_stream)),
            "moe_layer_forward_streamed")
 
 

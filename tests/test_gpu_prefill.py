@@ -111,10 +111,10 @@ def test_prefill_large_expert_layer_sampled():
     U.assert_close_layer(y[tokens], ref.y, what="sampled y")
 
 
-def run_streamed(st, x_bits, T, U_, bf16_out=False):
+def run_streamed(st, x_bits, T, U_, bf16_out=False, buffers=2):
     x = torch.from_numpy(x_bits.view(np.int16)).cuda()
     y = torch.zeros((T, st.H), dtype=torch.int16 if bf16_out else torch.float32, device="cuda")
-    st.forward_streamed(0, x, y, T, U_, y_is_fp32=not bf16_out)
+    st.forward_streamed(0, x, y, T, U_, y_is_fp32=not bf16_out, buffers=buffers)
     torch.cuda.synchronize()
     rc = moe.moe_sync_status(st.ws)
     assert rc == moe.MOE_OK, moe.strerror(rc)
@@ -151,6 +151,8 @@ def test_prefill_streamed_small_shapes_full(T, H, I_, E, k, Is, U_):
     U.assert_close_layer(y, ref.y)
     yb = run_streamed(st, x_bits, T, U_, bf16_out=True)
     U.assert_close_layer(yb, ref.y, bf16_out=True)
+    y1 = run_streamed(st, x_bits, T, U_, buffers=1)   # one staging half: each copy waits for the GEMMs before it
+    U.assert_close_layer(y1, ref.y)
 
 
 def test_prefill_streamed_chunk_t8192_sampled():
@@ -174,3 +176,8 @@ def test_prefill_streamed_rejects_bad_units():
     for bad in (0, 3):  # 2*U must fit the four staging slots
         with pytest.raises(moe.MoeError):
             st.forward_streamed(0, x, y, 64, bad)
+    for bad_buffers in (0, 3):
+        with pytest.raises(moe.MoeError):
+            st.forward_streamed(0, x, y, 64, 2, buffers=bad_buffers)
+    with pytest.raises(moe.MoeError):  # one buffer of 5 does not fit four slots either
+        st.forward_streamed(0, x, y, 64, 5, buffers=1)
