@@ -50,6 +50,9 @@ def parse():
     p.add_argument("--layers", type=int, default=8,
                    help="layers of the workload's shape stepped through in turn (1 for small profiling runs)")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget for cpu_baseline")
+    p.add_argument("--large", action="store_true",
+                   help="also time the 4096-hidden, 256-expert top-6 model: its 4096-token prefill chunk and "
+                        "batch-64 decode")
     return p.parse_args()
 
 
@@ -344,15 +347,12 @@ def measure_policy(st, xs, ys, T, stream, n=16):
                     "admissions (the decode window's misses)"}
 
 
-def measure_prefill(args, peaks):
-    """A short measurement of the prefill chunk (8192 tokens through one layer)."""
+def prefill_timing(st, w, T, peaks, xs):
+    """One prefill chunk of T tokens through layer 0 of st: CUDA graph, L2 flushed before each of
+    20 replays, events on the launching stream; per-kernel times from a separate pass."""
     import torch
-    from serving_router_top_gb300 import inputs as I, moe
-    from serving_router_top_gb300.model import ModelState
-    w = I.WORKLOADS["prefill_t8192_h2048_e512_k10"]
-    s, T = w.shape, w.T
-    st = ModelState(w)
-    xs = [torch.from_numpy(I.activations(w.seed, 20_000 + i, T, s.H).view(np.int16)).cuda() for i in range(2)]
+    from serving_router_top_gb300 import moe
+    s = w.shape
     x_in = torch.empty_like(xs[0])
     y = torch.zeros((T, s.H), dtype=torch.int16, device="cuda")
     flusher = L2Flush()
@@ -398,15 +398,84 @@ def measure_prefill(args, peaks):
             tf = fl[name] / (kt[name] / 1e3) / 1e12
             gemms[name] = {"us": 1e3 * kt[name], "tflops": tf, "frac": tf / peak}
     total = sum(fl.values())
-    del st
-    torch.cuda.empty_cache()
-    streamed = {f"{src}_{nb}buf": measure_prefill_streamed(w, xs, on_device, buffers=nb)
-                for src, on_device in (("device", True), ("pinned_host", False)) for nb in (2, 1)}
-    return {"workload": w.name, "tokens_per_s": T / (ms / 1e3), "ms_per_layer": ms,
+    return {"workload": w.name, "tokens": T, "tokens_per_s": T / (ms / 1e3), "ms_per_layer": ms,
             "tflops_dense_equiv": total / (ms / 1e3) / 1e12, "peak_tflops": peak,
             "peak_source": "measured bf16_tflops (burst); the GEMMs run kind::f16 on bf16/f16 operands",
             "kernels_us": {n: 1e3 * v for n, v in kt.items()}, "gemms": gemms,
-            "timing": f"{n} steps, CUDA graph, L2 flushed before each", "streamed": streamed}
+            "timing": f"{n} steps, CUDA graph, L2 flushed before each"}
+
+
+def measure_prefill(args, peaks):
+    """A short measurement of the prefill chunk (8192 tokens through one layer), then the
+    same chunk with the layer's experts streamed through the staging pool."""
+    import torch
+    from serving_router_top_gb300 import inputs as I
+    from serving_router_top_gb300.model import ModelState
+    w = I.WORKLOADS["prefill_t8192_h2048_e512_k10"]
+    s, T = w.shape, w.T
+    st = ModelState(w)
+    xs = [torch.from_numpy(I.activations(w.seed, 20_000 + i, T, s.H).view(np.int16)).cuda() for i in range(2)]
+    out = prefill_timing(st, w, T, peaks, xs)
+    del st
+    torch.cuda.empty_cache()
+    out["streamed"] = {f"{src}_{nb}buf": measure_prefill_streamed(w, xs, on_device, buffers=nb)
+                       for src, on_device in (("device", True), ("pinned_host", False)) for nb in (2, 1)}
+    return out
+
+
+def measure_large(peaks, layers: int = 2, T_decode: int = 64, steps: int = 200):
+    """The 4096-hidden, 256-expert top-6 model (I = I_shared = 2048), all experts resident:
+    its 4096-token prefill chunk through one layer, and batch-64 decode stepping through
+    `layers` layers in turn (their weights, 3.6 GB per layer, exceed the L2), captured as
+    graphs of `layers` steps and timed back to back with one event pair."""
+    import torch
+    from serving_router_top_gb300 import inputs as I, moe
+    from serving_router_top_gb300.model import ModelState
+    w = I.WORKLOADS["large_h4096_e256_k6"]
+    s = w.shape
+    st = ModelState(w, layers=layers)
+    xs = [torch.from_numpy(I.activations(w.seed, 30_000 + i, w.T, s.H).view(np.int16)).cuda() for i in range(2)]
+    pre = prefill_timing(st, w, w.T, peaks, xs)
+    wins = [torch.from_numpy(I.activations(w.seed, 40_000 + i, T_decode, s.H).view(np.int16)).cuda()
+            for i in range(4 * layers)]
+    ys = [torch.zeros((T_decode, s.H), dtype=torch.int16, device="cuda") for _ in range(layers)]
+    stream = torch.cuda.Stream()
+
+    def steps_of(j):
+        for l in range(layers):
+            st.forward(l, wins[(j * layers + l) % len(wins)], ys[l], T_decode, y_is_fp32=False,
+                       mode=moe.MOE_MODE_DECODE, stream=stream)
+
+    with torch.cuda.stream(stream):
+        steps_of(0)
+        torch.cuda.synchronize()
+        graphs = []
+        for j in range(4):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                steps_of(j)
+            graphs.append(g)
+        for j in range(8):
+            graphs[j % 4].replay()
+        torch.cuda.synchronize()
+        reps = max(1, steps // layers)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for j in range(reps):
+            graphs[j % 4].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    rc = moe.moe_sync_status(st.ws)
+    if rc != moe.MOE_OK:
+        raise RuntimeError(f"device error in the large-model measurement: {moe.strerror(rc)}")
+    us = 1e3 * e0.elapsed_time(e1) / (reps * layers)
+    out = {"workload": w.name, "prefill": pre,
+           "decode": {"tokens_per_window": T_decode, "us_per_layer_step": us,
+                      "tokens_per_s": T_decode / (us / 1e6), "layers_stepped": layers,
+                      "timing": f"{reps * layers} layer steps in graphs of {layers}, back to back, one event pair"}}
+    del st
+    torch.cuda.empty_cache()
+    return out
 
 
 def measure_prefill_streamed(w, xs, on_device: bool, U: int = 64, n: int = 8, buffers: int = 2):
@@ -613,6 +682,8 @@ def run_ours(args, w):
         out["policy"] = measure_policy(st, xs, ys, T, stream)
     if not args.no_prefill:
         out["prefill"] = measure_prefill(args, peaks)
+    if args.large:
+        out["large"] = measure_large(peaks)
     if not args.no_cpu_baseline:
         v, tok, calls, el = oracle_sample(w, args.cpu_seconds)
         out["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
