@@ -56,6 +56,10 @@ __device__ __forceinline__ void ld_stream32(const void* p, uint32_t (&r)[8]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                : "l"(p));
 }
+// An L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned address.
+__device__ __forceinline__ void prefetch_bulk_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
   uint32_t v;
   asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
@@ -257,6 +261,19 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_gemv(Args a) {
   Unit<NM> ring[D];
 #pragma unroll
   for (int d = 0; d < D; ++d) load_unit(d, ring[d]);
+  // the codes of the tasks beyond the ring's first D units go to L2 now, so
+  // that their loads, issued when the ring turns over, find them there
+  {
+    const int t_first = (D + g.CPW - 1) >> g.l_cpw, ntl = t_end - t_begin;
+    if (t_first < ntl && tid < (ntl - t_first) * NM) {
+      const int tl = t_first + tid / NM, m = tid - (tid / NM) * NM;
+      const int task = t_begin + tl, gi = task >> g.l_tpg, tb = task & (g.TPG - 1);
+      const uint8_t* blob = S.blob[gi];
+      if (blob)
+        prefetch_bulk_l2(blob + a.lay.code_off[GATEUP ? m : 2] + size_t(tb * g.RB * 16) * (g.K / 2),
+                         uint32_t(g.RB * 16) * uint32_t(g.K / 2));
+    }
+  }
   if (GATEUP) {
     if (tid < a.T) S.vinv[tid] = 1.0f / S.vinv[tid];
     __syncthreads();
