@@ -83,3 +83,29 @@ def test_blob_roundtrip_dequantises_like_canonical(lib):
     scales = blob[sc_off:sc_off + I * H // 16].reshape(I, H // 16)
     rows = np.concatenate([codes, scales], axis=1)
     assert np.array_equal(formats.dequantize(rows, H), formats.dequantize(ex.gate, H))
+
+
+def test_null_handles_are_rejected_without_a_device(lib):
+    """Every entry point that takes a cache or workspace handle checks it before any CUDA call,
+    so these run on a machine without a GPU."""
+    P = None
+    assert lib.moe_ws_set_tail_skip(P, 7) == moe.MOE_EINVAL
+    assert lib.moe_ws_set_fused_heat(P, 1) == moe.MOE_EINVAL
+    assert lib.moe_ws_set_profiling(P, 1) == moe.MOE_EINVAL
+    assert lib.cache_lru_plan(P, P, 0, 8, P, P, P) == moe.MOE_EINVAL
+    assert lib.moe_cache_apply_lru(P, P, P, P, P) == moe.MOE_EINVAL
+    assert lib.moe_cache_apply_swaps(P, P, P, P, P) == moe.MOE_EINVAL
+    assert lib.moe_group(P, 4, 2, 8, 0, P, P, P) == moe.MOE_EINVAL
+    assert lib.moe_cache_destroy(P) == moe.MOE_OK
+    assert lib.moe_ws_destroy(P) == moe.MOE_OK
+
+
+def test_shape_limits_stated_in_the_header_are_enforced(lib):
+    """moe_ws_create rejects rows outside powers of two in [64, 4096] and k outside [1, min(E, 32)]
+    before allocating (MOE_EINVAL, no CUDA call)."""
+    import ctypes as C
+    h = C.c_void_p()
+    for H, I, E, k in ((96, 64, 8, 2), (64, 8192, 8, 2), (64, 64, 8, 9), (64, 64, 2048, 2), (64, 64, 64, 33),
+                       (64, 64, 8, 0)):
+        assert lib.moe_ws_create(C.byref(h), 4, moe.moe_layer_shape(H, I, E, k, 0)) == moe.MOE_EINVAL
+    assert lib.moe_ws_create(C.byref(h), 0, moe.moe_layer_shape(64, 64, 8, 2, 0)) == moe.MOE_EINVAL
