@@ -79,6 +79,9 @@ def test_layer_t8_h256_e16_k2():
     (33, 64, 64, 9, 9, 0, 1.0),        # k == E, no shared expert, narrowest rows
     (64, 1024, 256, 64, 6, 256, 0.5),
     (3, 4096, 2048, 16, 2, 2048, 1.0),  # the large-expert row widths
+    (2, 128, 64, 1, 1, 64, 1.0),        # a single routed expert (weight 1) and the shared one
+    (8, 256, 128, 40, 7, 64, 0.5),      # the largest window of the decode GEMVs
+    (9, 256, 128, 40, 7, 64, 0.5),      # the smallest window of the streaming kernels
 ])
 def test_layer_small_shapes(T, H, I_, E, k, Is, frac):
     from serving_router_top_gb300.model import ModelState
@@ -211,6 +214,24 @@ def test_fused_topk_group_all_ties(T, E, k):
     exp_, off, _, _, ent_tok, _ = st.ws.groups(T)
     assert exp_.tolist() == list(range(k)) and off.tolist() == [T * r for r in range(k + 1)]
     assert ent_tok.tolist() == list(range(T)) * k
+
+
+def test_empty_window_is_a_no_op():
+    """T = 0 through every call: MOE_OK, nothing written."""
+    from serving_router_top_gb300.model import ModelState
+    w = I.small_workload(T=4, H=128, I=64, E=8, k=2, I_shared=64, resident_frac=0.5, seed=4)
+    st = ModelState(w)
+    x = torch.zeros((4, 128), dtype=torch.int16, device="cuda")
+    y = torch.full((4, 128), 7.0, dtype=torch.float32, device="cuda")
+    for mode in (moe.MOE_MODE_DECODE, moe.MOE_MODE_PREFILL, moe.MOE_MODE_AUTO):
+        st.forward(0, x, y, 0, mode=mode)
+    ids = torch.zeros((4, 2), dtype=torch.int32, device="cuda")
+    moe.moe_group(ids, 0, 2, 8, 0, st.cache, st.ws)
+    moe.cache_heat_update(st.cache, ids, 0, 2, 0)
+    torch.cuda.synchronize()
+    assert moe.moe_sync_status(st.ws) == moe.MOE_OK
+    assert bool((y == 7.0).all())
+    assert float(st.cache.tables()[2].abs().sum()) == 0.0   # no heat added
 
 
 def test_missing_expert_is_reported():
