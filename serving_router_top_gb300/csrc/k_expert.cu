@@ -127,9 +127,12 @@ struct StageGeo {
 
 // GATEUP: input x (f16 [T,H]) -> h[entry row][r] = SiLU(gs_g*<Wg_r,x>) * gs_u*<Wu_r,x>, and max|h| per row
 // !GATEUP: input h (fp32 rows, to f16 with a per-row power-of-two scale) -> o[position][r] = gs_d*<Wd_r,h>
-// Task index = ((g * NRB + rb) * KS + ks) * NBP + nbk with power-of-two NRB,
-// KS, NBP, so it decodes with shifts; the shared expert's tasks follow the
-// routed ones.  A task covers C/KS columns in units of UC.
+// Task index = ((nbk * G + g) * NRB + rb) * KS + ks with power-of-two NRB and
+// KS: the vector block outermost, so that the tasks of the first block -- the
+// only non-empty one of a group of at most 8 vectors -- are consecutive and
+// spread over every warp (warps take every nw-th task).  The shared expert's
+// tasks, ((nbk * NRB_s + rb) * KS_s + ks), follow the routed ones.  A task
+// covers C/KS columns in units of UC.
 template <bool GATEUP, int UC>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, 1) k_expert_stream(DecodeArgs a) {
   pdl_trigger();
@@ -142,10 +145,10 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 1) k_expert_stream(DecodeAr
   uint8_t* wbase = smem + size_t(wib) * (kStages * (SG::BYTES + sizeof(UnitMeta)));
   UnitMeta* meta = reinterpret_cast<UnitMeta*>(wbase + kStages * SG::BYTES);
   const int G = *a.num_groups;
-  const int lbits_r = a.l_nrb_r + a.l_ks_r + a.l_nbp, lbits_s = a.l_nrb_s + a.l_ks_s + a.l_nbp;
-  const int routed = G << lbits_r;
-  const int ntask = routed + (a.shared_blob ? (1 << lbits_s) : 0);
-  const int nbmask = (1 << a.l_nbp) - 1;
+  const int lgs_r = a.l_nrb_r + a.l_ks_r, lgs_s = a.l_nrb_s + a.l_ks_s;  // tasks per (block, group)
+  const int per_block = G << lgs_r;                                     // routed tasks per vector block
+  const int routed = per_block << a.l_nbp;
+  const int ntask = routed + (a.shared_blob ? (1 << (lgs_s + a.l_nbp)) : 0);
 
   // ---- issue side: the warp's cursor over (task, unit); tasks without vectors are skipped
   int cur = gw, cu = 0;
@@ -155,13 +158,14 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 1) k_expert_stream(DecodeAr
     for (; cur < ntask; cur += nw) {
       int n, r;
       if (cur < routed) {
-        r = cur;
+        const int nbk = cur / per_block;
+        r = cur - nbk * per_block;
         i_shared = 0;
-        i_g = r >> lbits_r;
-        const int rest = r & ((1 << lbits_r) - 1);
-        i_rb = rest >> (a.l_ks_r + a.l_nbp);
-        i_ks = (rest >> a.l_nbp) & ((1 << a.l_ks_r) - 1);
-        i_jbase = (rest & nbmask) * 8;
+        i_g = r >> lgs_r;
+        const int rest = r & ((1 << lgs_r) - 1);
+        i_rb = rest >> a.l_ks_r;
+        i_ks = rest & ((1 << a.l_ks_r) - 1);
+        i_jbase = nbk * 8;
         i_e0 = a.grp_off[i_g];
         n = a.grp_off[i_g + 1] - i_e0;
         i_C = GATEUP ? a.H : a.I;
@@ -170,9 +174,10 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 1) k_expert_stream(DecodeAr
         r = cur - routed;
         i_shared = 1;
         i_g = G;
-        i_rb = r >> (a.l_ks_s + a.l_nbp);
-        i_ks = (r >> a.l_nbp) & ((1 << a.l_ks_s) - 1);
-        i_jbase = (r & nbmask) * 8;
+        const int rest = r & ((1 << lgs_s) - 1);
+        i_rb = rest >> a.l_ks_s;
+        i_ks = rest & ((1 << a.l_ks_s) - 1);
+        i_jbase = (r >> lgs_s) * 8;
         i_e0 = 0;
         n = a.T;
         i_C = GATEUP ? a.H : a.I_s;
