@@ -19,7 +19,7 @@ int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* 
 int launch_gateup_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s);
 int launch_down_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s);
 int launch_combine(const moe_layer_desc* d, void* y, int y_is_fp32, int T, moe_ws* ws, cudaStream_t s);
-// Row-block-streaming GEMVs for windows of at most 8 tokens (bulk copies).
+// Decode GEMVs for windows of at most 8 tokens (every warp streams weight rows into registers).
 constexpr int kGemvNotApplicable = -1;
 int launch_gemv_decode(bool gateup, const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s);
 
