@@ -15,7 +15,7 @@ int launch_topk_group(const float* logits, int T, int k, int E, int layer, moe_c
 int launch_group(const int32_t* ids, int T, int k, int E, int layer, moe_cache* c, moe_ws* ws, cudaStream_t s,
                  bool lookup = true);
 
-// Decode expert path (CUDA-core GEMVs over the slot blobs).
+// Decode expert path (GEMVs over the slot blobs, mma.sync on the tensor cores).
 int launch_gateup_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s);
 int launch_down_decode(const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s);
 int launch_combine(const moe_layer_desc* d, void* y, int y_is_fp32, int T, moe_ws* ws, cudaStream_t s);
