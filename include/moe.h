@@ -383,7 +383,8 @@ int moe_cache_apply_swaps(moe_cache* c, const moe_swap* plan_dev, const int32_t*
  * recently used first, ties to the lower slot.  In an entry, `layer` and
  * hot_expert name the admitted expert, cold_expert the evicted one as
  * layer * E + expert (-1: the slot was empty), slot the slot, diff is 0; the
- * slots taken count as used now.  1 <= K <= 32, else MOE_EINVAL.  The clock
+ * slots taken count as used now.  1 <= K <= 32 and a cache of 1 to 2^24 - 1
+ * slots, else MOE_EINVAL.  The clock
  * is 32-bit: past 2^32 - 2 calls the device records MOE_ERANGE.  Async on
  * `stream`; execute the plan with moe_cache_apply_lru. */
 int cache_lru_plan(moe_cache* c, const moe_ws* ws, int layer, int K, moe_swap* plan_dev, int32_t* n_dev,
