@@ -38,6 +38,24 @@ import numpy as np  # noqa: E402
 DEFAULT_WORKLOAD = "decode_t4_h2048_e512_k10"
 
 
+# ------------------------------------------------------------------ replicas
+def max_over_ranks(values, world: int, device: str = "cuda"):
+    """Each value's maximum over the ranks: a job's time is its slowest replica's.  Needs the
+    process group initialised when world > 1 (its backend must handle `device`)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_tokens_per_s(tokens_per_step: int, steps: int, world: int, job_ms: float) -> float:
+    """Whole-job throughput: every replica's tokens over the slowest replica's time."""
+    return tokens_per_step * steps * world / (job_ms / 1e3)
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -639,13 +657,9 @@ def run_ours(args, w):
             e2e_ms += a.elapsed_time(b)
     torch.cuda.synchronize()
 
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
-    tokens = T * args.steps * world
-    value = tokens / (total_ms / 1e3)
-    e2e_value = tokens / (e2e_ms / 1e3)
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], world)
+    value = job_tokens_per_s(T, args.steps, world, total_ms)
+    e2e_value = job_tokens_per_s(T, args.steps, world, e2e_ms)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
