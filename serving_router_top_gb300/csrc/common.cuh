@@ -144,41 +144,39 @@ __device__ __forceinline__ float pow2_scale_for(float amax) {
   return ldexpf(1.0f, 13 - e);  // amax * 2^(13-e) in [2^12, 2^13)
 }
 
-// y[t] cols 4c4..4c4+3 = sum_r w[t,r] * o[t*k + r] (rank order) + sigmoid(g_t) * o[shared t],
-// with the rows' loads issued eight at a time so their latencies overlap.
+// y[t] cols 4c4..4c4+3 = sum_r w[t,r] * o[t*k + r] (rank order) + sigmoid(g_t) * o[shared t].
+// The shared row counts as row k; the rows' loads (and their coefficients) are issued
+// sixteen at a time before any is used, so up to 15 routed rows and the shared one take a
+// single round trip.  The multiply-adds keep the rank order, the shared term last.
 template <bool LDCG>
 __device__ __forceinline__ float4 combine4(const float* o, const float* w, const float* gate_logit, bool has_shared,
                                            int t, int c4, int H, int k, int maxTk) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int r0 = 0; r0 < k; r0 += 8) {
-    float4 v[8];
-    float wr[8];
+  const int nrow = k + (has_shared ? 1 : 0);
+  for (int r0 = 0; r0 < nrow; r0 += 16) {
+    float4 v[16];
+    float c[16];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (r0 + j < k) {
-        const float4* p = reinterpret_cast<const float4*>(o + size_t(t * k + r0 + j) * H) + c4;
+    for (int j = 0; j < 16; ++j) {
+      const int r = r0 + j;
+      if (r < nrow) {
+        const size_t row = r < k ? size_t(t * k + r) : size_t(maxTk + t);
+        const float4* p = reinterpret_cast<const float4*>(o + row * H) + c4;
         v[j] = LDCG ? __ldcg(p) : *p;
-        wr[j] = w[t * k + r0 + j];
+        c[j] = r < k ? w[t * k + r] : gate_logit[t];
       }
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (r0 + j < k) {
-        acc.x = fmaf(wr[j], v[j].x, acc.x);
-        acc.y = fmaf(wr[j], v[j].y, acc.y);
-        acc.z = fmaf(wr[j], v[j].z, acc.z);
-        acc.w = fmaf(wr[j], v[j].w, acc.w);
+    for (int j = 0; j < 16; ++j) {
+      const int r = r0 + j;
+      if (r < nrow) {
+        const float cf = r < k ? c[j] : sigmoid_f32(c[j]);
+        acc.x = fmaf(cf, v[j].x, acc.x);
+        acc.y = fmaf(cf, v[j].y, acc.y);
+        acc.z = fmaf(cf, v[j].z, acc.z);
+        acc.w = fmaf(cf, v[j].w, acc.w);
       }
     }
-  }
-  if (has_shared) {
-    const float gm = sigmoid_f32(gate_logit[t]);
-    const float4* p = reinterpret_cast<const float4*>(o + size_t(maxTk + t) * H) + c4;
-    const float4 sv = LDCG ? __ldcg(p) : *p;
-    acc.x = fmaf(gm, sv.x, acc.x);
-    acc.y = fmaf(gm, sv.y, acc.y);
-    acc.z = fmaf(gm, sv.z, acc.z);
-    acc.w = fmaf(gm, sv.w, acc.w);
   }
   return acc;
 }
