@@ -154,7 +154,7 @@ class OracleRunner:
         self.w, self.I = w, I
         s = w.shape
         self.li = I.layer_inputs(w)
-        self.experts = [I.expert_weights(w.seed, 0, e, s.H, s.I) for e in range(s.E)]
+        self.experts = [I.expert_of(w, 0, e) for e in range(s.E)]
         mask = I.resident_mask(w.seed, 0, s.E, w.resident_frac)
         self.resid = np.where(mask, np.cumsum(mask) - 1, -1).astype(np.int32)
         self.stage = np.where(~mask, np.cumsum(~mask) - 1, -1).astype(np.int32)
@@ -288,11 +288,15 @@ def profiled_traffic(workload: str, kernel: str):
     return None
 
 
-def kernel_time_pass(st, step, set_input, flusher, steps: int, stream):
+def kernel_time_pass(st, step, set_input, flusher, steps: int, stream, groups_out=None):
     """Per-kernel durations (CUDA events recorded on the launching stream around each
     kernel, captured into a graph of the step) averaged over `steps` flushed steps.
-    Kept out of the timed region: the event nodes lengthen the step."""
+    Kept out of the timed region: the event nodes lengthen the step.  When `groups_out`
+    is a list, the routed-group count of every one of those steps is appended to it
+    (the algorithmic bytes behind the durations are those of the same windows)."""
     import torch
+    from serving_router_top_gb300 import moe
+    ngroups = moe.device_view(st.ws.view.num_groups, (1,), "int32", st.ws)
     st.ws.set_profiling(True)
     set_input(0)
     step()
@@ -307,6 +311,8 @@ def kernel_time_pass(st, step, set_input, flusher, steps: int, stream):
         g.replay()
         times = st.ws.kernel_times()
         per_step = len(times)
+        if groups_out is not None:
+            groups_out.append(int(ngroups.item()))
         for name, ms in times:
             sums[name] = sums.get(name, 0.0) + ms
     torch.cuda.synchronize()
@@ -566,7 +572,6 @@ def run_ours(args, w):
                for i in range(P)]
     xs = [x.cuda() for x in xs_host]
     ys = [torch.zeros((T, s.H), dtype=torch.int16, device="cuda") for _ in range(NL)]  # bf16 output bits
-    ngroups = moe.device_view(st.ws.view.num_groups, (1,), "int32", st.ws)
     stream = torch.cuda.Stream()
 
     def layer_step(l, x):
@@ -630,10 +635,11 @@ def run_ours(args, w):
     # ---- per-kernel durations for the roofline (separate pass: layer 0, L2 evicted before each step)
     flusher = L2Flush()
     x_in = torch.empty_like(xs[0])
+    G_steps = []
     with torch.cuda.stream(stream):
         kt, per_step = kernel_time_pass(st, lambda: layer_step(0, x_in), lambda i: x_in.copy_(xs[i % P]), flusher,
-                                        min(K, 300), stream)
-    G = int(ngroups.item())
+                                        min(K, 300), stream, groups_out=G_steps)
+    G = statistics.mean(G_steps)  # the mean over the same windows whose durations are averaged
     launches = per_step * K  # the forward's kernels (the heat update inside the grouping), every step
 
     # ---- end to end through the C ABI with host buffers: each step's window is
@@ -687,6 +693,10 @@ def run_ours(args, w):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": f"{src} hbm_gbs",
                      "algorithmic_bytes_per_launch": by[dom], "avg_launch_us": avg_ms * 1e3,
+                     "mean_routed_groups": G,
+                     "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum of the committed ncu summary "
+                                       "of this kernel (profiles/), used only while the kernel's source file "
+                                       "matches the SHA-1 recorded there; not measured in this run",
                      "duration": "CUDA events around the kernel on its stream, separate pass of "
                                  f"{min(args.steps, 300)} flushed steps"},
         "kernels_us_per_step": {n: 1e3 * v for n, v in kt.items()},

@@ -315,7 +315,9 @@ typedef struct {
  *   threshold; candidates of all layers ordered by (diff desc, layer asc,
  *   hot id asc); the first max_swaps written to plan_dev (moe_swap[max_swaps],
  *   device) and their number to n_dev (int32[1], device); then every heat
- *   becomes fl32(heat * decay).  Requires L*E <= 32768 and max_swaps <= 4096. */
+ *   becomes fl32(heat * decay).  A NaN difference (a NaN heat, or infinite
+ *   heats on both sides) fails the test, so it ends its layer's pairing there.
+ *   Requires L*E <= 32768 and max_swaps <= 4096. */
 int cache_plan_swaps(moe_cache* c, const moe_policy_cfg* p, moe_swap* plan_dev, int32_t* n_dev, moe_stream_t stream);
 
 /* Residual stream and RMS normalisation between the layers of a decode stack.
@@ -352,9 +354,13 @@ int moe_residual_rmsnorm(float* x_res, const uint16_t* y_prev, uint16_t* xn_out,
  * start at zero.  The scratch's address is looked up on the first call on
  * each device (with that device current); the lookup may load the module,
  * which a stream capture does not allow, so make the first call on each
- * device before any capture.  All calls on one device share the scratch:
- * calls that overlap in time (other streams, other threads) race and must
- * be serialised by the caller. */
+ * device before any capture.  The looked-up address is kept for the life of
+ * the process: after a cudaDeviceReset (or any teardown of the device's
+ * primary context) it is stale, so do not call this function again in that
+ * process.  All calls on one device share the scratch: calls that overlap in
+ * time (other streams, other threads) race and must be serialised by the
+ * caller.  Heats may be NaN or infinite: a layer's pairing stops at the first
+ * pair whose difference fails the threshold test, as in cache_plan_swaps. */
 int cache_plan_swaps_noalloc(float* heat_dev, const int32_t* resid_dev, int L, int E, const moe_policy_cfg* p,
                              moe_swap* plan_dev, int32_t* n_dev, moe_stream_t stream);
 

@@ -100,21 +100,28 @@ __global__ void __launch_bounds__(1024) k_plan_layer(float* __restrict__ heat, c
   __syncthreads();
   bitonic_sort(hot, P);
   bitonic_sort(cold, P);
+  // Pairing stops at the first pair whose difference fails the test: with finite heats
+  // the differences never increase along i, but a NaN (or inf - inf) fails the test
+  // wherever it sits, so the candidates are the prefix before the first failure.
   const int npair = min(s_nhot, s_ncold);
+  if (threadIdx.x == 0) s_ncand = npair;
+  __syncthreads();
   for (int i = threadIdx.x; i < npair; i += blockDim.x) {
     const int a = int(hot[i] & 0xffffffffu), b = int(cold[i] & 0xffffffffu);
-    const float d = __fsub_rn(hrow[a], hrow[b]);
-    if (d >= threshold) {
-      atomicAdd(&s_ncand, 1);
-      // global order: diff desc, layer asc, hot id asc (d > 0, so its bits order like d)
-      cand[size_t(l) * cand_stride + i] =
-          (static_cast<unsigned long long>(0xffffffffu - __float_as_uint(d)) << 32) |
-          (static_cast<unsigned long long>(l) << 16) | uint32_t(a);
-      cold_of[size_t(l) * E + a] = b;
-    }
+    if (!(__fsub_rn(hrow[a], hrow[b]) >= threshold)) atomicMin(&s_ncand, i);
   }
   __syncthreads();
-  if (threadIdx.x == 0) cand_count[l] = s_ncand;
+  const int ncand = s_ncand;
+  for (int i = threadIdx.x; i < ncand; i += blockDim.x) {
+    const int a = int(hot[i] & 0xffffffffu), b = int(cold[i] & 0xffffffffu);
+    const float d = __fsub_rn(hrow[a], hrow[b]);
+    // global order: diff desc, layer asc, hot id asc (d >= threshold > 0, so its bits order like d)
+    cand[size_t(l) * cand_stride + i] = (static_cast<unsigned long long>(0xffffffffu - __float_as_uint(d)) << 32) |
+                                        (static_cast<unsigned long long>(l) << 16) | uint32_t(a);
+    cold_of[size_t(l) * E + a] = b;
+  }
+  if (threadIdx.x == 0) cand_count[l] = ncand;
+  __syncthreads();  // every thread has read the heats it compared before any is decayed
   for (int e = threadIdx.x; e < E; e += blockDim.x) hrow[e] = __fmul_rn(hrow[e], decay);
 }
 
@@ -145,13 +152,20 @@ __global__ void __launch_bounds__(1024) k_plan_merge(const unsigned long long* _
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const unsigned long long key = keys[i];
     const int l = int((key >> 16) & 0xffffu), a = int(key & 0xffffu);
-    const int b = cold_of[size_t(l) * E + a];
     moe_swap sw;
-    sw.layer = l;
+    sw.layer = -1;  // an entry that fails the checks below is one the swap execution rejects
     sw.hot_expert = a;
-    sw.cold_expert = b;
-    sw.slot = resid[size_t(l) * E + b];
+    sw.cold_expert = -1;
+    sw.slot = -1;
     sw.diff = __uint_as_float(0xffffffffu - uint32_t(key >> 32));
+    if (l < L && a < E) {  // every key read was written by this round (a guard, not a path)
+      const int b = cold_of[size_t(l) * E + a];
+      if (b >= 0 && b < E) {
+        sw.layer = l;
+        sw.cold_expert = b;
+        sw.slot = resid[size_t(l) * E + b];
+      }
+    }
     plan[i] = sw;
   }
   if (threadIdx.x == 0) *n_out = n;

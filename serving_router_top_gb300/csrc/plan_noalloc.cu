@@ -12,7 +12,10 @@
 // The scratch's address is looked up once per device (cudaGetSymbolAddress,
 // on the first call made while that device is current).  The lookup may load
 // the module, which is not allowed while a stream is being captured, so the
-// first call on each device should come before any capture.
+// first call on each device should come before any capture.  The address is
+// kept for the life of the process; a device reset (cudaDeviceReset, or any
+// teardown of the primary context) leaves it stale, so the library must not be
+// called again in that process after one.
 #include <mutex>
 
 #include "internal.h"

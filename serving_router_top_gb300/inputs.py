@@ -21,7 +21,8 @@ Input recipe (stated once here; the design notes repeat it):
   * block scales: E4M3 bytes ``(e<<3)|m`` with ``e`` uniform in 3..6 and ``m``
     uniform in 0..7, i.e. values ``2^(e-7)*(1+m/8)`` spread over
     ``[2^-4, 2^0)`` one octave at a time (log-uniform at octave grain);
-  * global scales: 1.0;
+  * global scales: 1.0 (the edge-case workload: 0.375, 2.0, 1.25 for gate, up, down,
+    and block scales over the whole non-negative E4M3 range, see ``packed_matrix``);
   * activations x: N(0,1) rounded to bf16 (round-to-nearest-even);
   * router weights W_r: N(0, std) in bf16, std 0.02 (or 1/sqrt(H) where a
     workload asks for unit-variance logits);
@@ -70,17 +71,34 @@ def random_bytes(g: np.random.Generator, n: int) -> np.ndarray:
     return words.view(np.uint8)[:n]
 
 
-def packed_matrix(g: np.random.Generator, rows: int, cols: int) -> np.ndarray:
+# Scale-byte recipes.  "octaves": exponent field 3..6, any mantissa (the default).
+# "edge": the whole non-negative E4M3 range with its ends over-represented -- zero
+# (0x00), subnormals (0x01..0x07), the largest normal 448 (0x7E) and the rest of
+# the normal range (0x08..0x7D) -- to reach the ends of the format's value range.
+SCALE_RECIPES = ("octaves", "edge")
+
+
+def packed_matrix(g: np.random.Generator, rows: int, cols: int, scales: str = "octaves") -> np.ndarray:
     """One matrix in the canonical packed-row format, uint8 ``[rows, 9*cols/16]``.
 
-    Codes are raw random bytes.  Each scale byte takes 5 random bits: two pick
-    the exponent field e in 3..6, three the mantissa field m in 0..7.
+    Codes are raw random bytes.  "octaves" scales: each scale byte takes 5 random
+    bits, two picking the exponent field e in 3..6 and three the mantissa field m in
+    0..7.  "edge" scales: a random byte picks 0x00 (1 in 16), a subnormal 0x01..0x07
+    (2 in 16), 0x7E (1 in 16), else a uniform byte of 0x08..0x7D; the sign bit stays 0.
     """
     assert cols % 16 == 0, cols
+    assert scales in SCALE_RECIPES, scales
     codes = random_bytes(g, rows * cols // 2).reshape(rows, cols // 2)
     r = random_bytes(g, rows * cols // 16).reshape(rows, cols // 16)
-    scales = (((r & 3) + 3) << 3) | ((r >> 2) & 7)
-    return np.concatenate([codes, scales], axis=1)
+    if scales == "octaves":
+        sc = (((r & 3) + 3) << 3) | ((r >> 2) & 7)
+    else:
+        kind = r & 15
+        rest = random_bytes(g, rows * cols // 16).reshape(rows, cols // 16)
+        sc = np.where(kind == 0, 0,
+             np.where(kind <= 2, 1 + rest % 7,
+             np.where(kind == 3, 0x7E, 0x08 + rest % (0x7E - 0x08)))).astype(np.uint8)
+    return np.concatenate([codes, sc.astype(np.uint8)], axis=1)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -101,16 +119,19 @@ class Expert:
     gscale: Tuple[float, float, float] = (1.0, 1.0, 1.0)
 
 
-def expert_weights(seed: int, layer: int, expert: int, H: int, I: int) -> Expert:
+def expert_weights(seed: int, layer: int, expert: int, H: int, I: int, scales: str = "octaves",
+                   gscale: Tuple[float, float, float] = (1.0, 1.0, 1.0)) -> Expert:
     return Expert(
-        gate=packed_matrix(rng(seed, TAG_GATE, layer, expert), I, H),
-        up=packed_matrix(rng(seed, TAG_UP, layer, expert), I, H),
-        down=packed_matrix(rng(seed, TAG_DOWN, layer, expert), H, I),
+        gate=packed_matrix(rng(seed, TAG_GATE, layer, expert), I, H, scales),
+        up=packed_matrix(rng(seed, TAG_UP, layer, expert), I, H, scales),
+        down=packed_matrix(rng(seed, TAG_DOWN, layer, expert), H, I, scales),
+        gscale=tuple(float(np.float32(v)) for v in gscale),
     )
 
 
-def shared_expert_weights(seed: int, layer: int, H: int, I_shared: int) -> Expert:
-    return expert_weights(seed, layer, SHARED_EXPERT_ID, H, I_shared)
+def shared_expert_weights(seed: int, layer: int, H: int, I_shared: int, scales: str = "octaves",
+                          gscale: Tuple[float, float, float] = (1.0, 1.0, 1.0)) -> Expert:
+    return expert_weights(seed, layer, SHARED_EXPERT_ID, H, I_shared, scales, gscale)
 
 
 def activations(seed: int, step: int, T: int, H: int) -> np.ndarray:
@@ -166,6 +187,8 @@ class Workload:
     resident_frac: float = 1.0
     seed: int = 0
     description: str = ""
+    scales: str = "octaves"                                  # block-scale recipe (SCALE_RECIPES)
+    gscale: Tuple[float, float, float] = (1.0, 1.0, 1.0)     # FP32 global scales of gate, up, down
 
 
 # The five workload shapes of the method's evaluation, plus small variants
@@ -196,10 +219,24 @@ WORKLOADS: Dict[str, Workload] = {
 }
 
 
-def small_workload(T=5, H=128, I=64, E=12, k=3, I_shared=64, zipf_s=0.5, resident_frac=1.0, seed=1, layers=1) -> Workload:
+def small_workload(T=5, H=128, I=64, E=12, k=3, I_shared=64, zipf_s=0.5, resident_frac=1.0, seed=1, layers=1,
+                   scales="octaves", gscale=(1.0, 1.0, 1.0)) -> Workload:
     """Ragged small shapes for exhaustive oracle checks."""
     return Workload(f"small_t{T}_h{H}_e{E}_k{k}", LayerShape(H=H, I=I, E=E, k=k, I_shared=I_shared), T=T,
-                    layers=layers, zipf_s=zipf_s, resident_frac=resident_frac, seed=seed)
+                    layers=layers, zipf_s=zipf_s, resident_frac=resident_frac, seed=seed, scales=scales,
+                    gscale=tuple(gscale))
+
+
+def edge_workload(T=6, H=256, I=128, E=24, k=4, I_shared=128, seed=11, resident_frac=0.5) -> Workload:
+    """The format's edge cases on a small layer: block scales over the whole non-negative
+    E4M3 range (zero, subnormals, 448) and distinct non-unit global scales per matrix."""
+    return small_workload(T=T, H=H, I=I, E=E, k=k, I_shared=I_shared, zipf_s=0.7, resident_frac=resident_frac,
+                          seed=seed, scales="edge", gscale=(0.375, 2.0, 1.25))
+
+
+def expert_of(w: Workload, layer: int, e: int) -> Expert:
+    """Routed expert e of a layer of workload w, with the workload's scale recipe."""
+    return expert_weights(w.seed, layer, e, w.shape.H, w.shape.I, w.scales, w.gscale)
 
 
 @dataclasses.dataclass
@@ -222,7 +259,7 @@ def layer_inputs(w: Workload, layer: int = 0, step: int = 0, epoch: int = 0, T: 
         w_router=router_weights(w.seed, layer, s.E, s.H, w.router_std),
         bias=zipf_bias(w.seed, layer, s.E, w.zipf_s, epoch),
         w_shared_gate=shared_gate_weights(w.seed, layer, s.H) if has_shared else None,
-        shared=shared_expert_weights(w.seed, layer, s.H, s.I_shared) if has_shared else None,
+        shared=shared_expert_weights(w.seed, layer, s.H, s.I_shared, w.scales, w.gscale) if has_shared else None,
         layer=layer,
     )
 
@@ -230,4 +267,4 @@ def layer_inputs(w: Workload, layer: int = 0, step: int = 0, epoch: int = 0, T: 
 def experts_of_layer(w: Workload, layer: int):
     """Generator over ``(expert id, Expert)`` of one layer."""
     for e in range(w.shape.E):
-        yield e, expert_weights(w.seed, layer, e, w.shape.H, w.shape.I)
+        yield e, expert_of(w, layer, e)

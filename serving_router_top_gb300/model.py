@@ -114,7 +114,7 @@ class ModelState:
         return st.cpu().numpy()
 
     def expert_host(self, layer: int, e: int) -> I.Expert:
-        return I.expert_weights(self.w.seed, layer, e, self.H, self.I)
+        return I.expert_of(self.w, layer, e)
 
     def forward(self, layer: int, x: torch.Tensor, y: torch.Tensor, T: int, y_is_fp32: bool = True,
                 mode: int = moe.MOE_MODE_AUTO, stream=None) -> None:

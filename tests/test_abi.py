@@ -109,3 +109,25 @@ def test_shape_limits_stated_in_the_header_are_enforced(lib):
                        (64, 64, 8, 0)):
         assert lib.moe_ws_create(C.byref(h), 4, moe.moe_layer_shape(H, I, E, k, 0)) == moe.MOE_EINVAL
     assert lib.moe_ws_create(C.byref(h), 0, moe.moe_layer_shape(64, 64, 8, 2, 0)) == moe.MOE_EINVAL
+
+
+def test_edge_recipe_reaches_the_ends_of_the_format(lib):
+    """The edge-case workload's weights hold zero, subnormal and 448 block scales, keep the scale
+    sign bit clear, and carry their non-unit global scales into the blob header; the oracle's
+    values then reach 6 * 448 = 2688 and 0.5 * 2^-9 = 2^-10 (times the global scale)."""
+    w = inputs.edge_workload()
+    ex = inputs.expert_of(w, 0, 3)
+    sc = np.concatenate([m[:, c // 2:].ravel() for m, c in ((ex.gate, w.shape.H), (ex.up, w.shape.H),
+                                                              (ex.down, w.shape.I))])
+    assert (sc == 0).any() and ((sc >= 1) & (sc <= 7)).any() and (sc == 0x7E).any()
+    assert (sc < 0x7F).all()   # no NaN scale, sign bit clear
+    vals = np.abs(formats.dequantize(ex.gate, w.shape.H, ex.gscale[0]))
+    nz = vals[vals > 0]
+    assert vals.max() == 2688.0 * 0.375
+    assert nz.min() == 2.0 ** -10 * 0.375
+    blob = moe.moe_pack_expert(ex.gate, ex.up, ex.down, w.shape.H, w.shape.I, ex.gscale)
+    assert blob[16:28].view(np.float32).tolist() == [0.375, 2.0, 1.25]
+    # the default recipe is unchanged by the edge option: exponent fields 3..6 only
+    d = inputs.expert_weights(0, 0, 1, 128, 64)
+    e = (d.gate[:, 64:] >> 3) & 15
+    assert e.min() == 3 and e.max() == 6

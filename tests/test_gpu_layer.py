@@ -275,23 +275,24 @@ def test_group_rejects_out_of_range_ids():
     assert moe.moe_sync_status(st.ws) == moe.MOE_ERANGE
 
 
-def test_large_expert_layer_decode_batch64_sampled():
-    """One layer of the 4096-hidden, 256-expert top-6 model (I = I_shared = 2048) decoding a batch of 64
-    tokens; sampled tokens against the oracle on the GPU's own logits."""
+def test_large_expert_layer_decode_batch64_all_tokens():
+    """One layer of the 4096-hidden, 256-expert top-6 model (I = I_shared = 2048) decoding a batch of
+    64 tokens: every token against the oracle, plus the router, routing and groups as check_layer."""
     from serving_router_top_gb300.model import ModelState
     w = I.WORKLOADS["large_h4096_e256_k6"]
     st = ModelState(w, layers=1, maxT=64)
-    T = 64
-    x_bits = I.activations(w.seed, 7, T, st.H)
-    y = run_layer(st, x_bits, T, bf16_out=False)
-    logits_t, ids_t, w_t = st.ws.routing(T)
-    logits = logits_t.cpu().numpy()
-    ids = ids_t.cpu().numpy()
-    ref_ids, ref_w = olayer.top_k(logits, st.k)
-    assert np.array_equal(ids, ref_ids)
-    toks = np.random.default_rng(11).choice(T, 8, replace=False)
-    ref = U.oracle_layer_from_state(st, 0, x_bits[toks], logits[toks])
-    U.assert_close_layer(y[toks], ref.y, what="sampled y")
+    check_layer(st, 64, step=7)
+
+
+@pytest.mark.parametrize("T", [6, 20])   # the decode GEMVs; the streaming kernel past 8 tokens
+def test_layer_edge_format(T):
+    """Zero, subnormal and 448 block scales and global scales 0.375 / 2.0 / 1.25 (gate, up, down)
+    through the decode path, fp32 and bf16 output."""
+    from serving_router_top_gb300.model import ModelState
+    w = I.edge_workload(T=T)
+    st = ModelState(w)
+    check_layer(st, T)
+    check_layer(st, T, bf16_out=True, step=1)
 
 
 @pytest.mark.parametrize("T,H,I_,E,k,frac", [

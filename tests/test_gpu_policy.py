@@ -264,3 +264,53 @@ def test_lru_plan_rejects_bad_k():
     for K in (0, 33):
         with pytest.raises(moe.MoeError):
             moe.cache_lru_plan(c, ws, 0, K, plan, n)
+
+
+def test_publish_after_copy_race_with_layer_calls():
+    """Publish-after-copy under a delayed copy (Strata page, "哪些专家能长期留在显存？": new weights
+    become visible only after their copy completes).  The copy stream first runs a timed spin
+    (about 0.1 s), so the swap's blob copy lands long after the compute stream could otherwise
+    run the layer calls queued behind moe_cache_apply_swaps.  Those calls route every token to
+    the swapped-in expert; each output must equal the oracle's, and the last call's lookup must
+    find that expert resident in the reused slot: the calls ran after the publish, which waited
+    for the copy, so none of them read the slot while it still held the evicted expert."""
+    from oracle import layer as olayer
+    from serving_router_top_gb300 import inputs as I
+    from serving_router_top_gb300.model import ModelState
+    T, E = 4, 16
+    w = I.small_workload(T=T, H=256, I=128, E=E, k=3, I_shared=128, zipf_s=0.0, resident_frac=0.5, seed=21)
+    st = ModelState(w, stage_all=True)   # every expert also staged: the evicted one stays reachable
+    resid0 = st.resid_table()[:E]
+    A = int(np.flatnonzero(resid0 < 0)[0])    # hot, not resident
+    B = int(np.flatnonzero(resid0 >= 0)[0])   # cold, resident
+    heat = np.where(resid0 >= 0, F32(100.0), F32(0.0)).astype(F32)
+    heat[A], heat[B] = F32(10.0), F32(8.0)    # the page's worked example: 10 - 8 = 2 >= 1.5
+    set_heat(st.cache, heat)
+    bias = st.layers[0].bias
+    bias[A] = 50.0                            # every token's first choice is A
+    got, plan, n = run_plan(st.cache)
+    assert [(int(s["hot_expert"]), int(s["cold_expert"]), int(s["slot"])) for s in got] == [(A, B, int(resid0[B]))]
+    compute = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    with torch.cuda.stream(copy):
+        torch.cuda._sleep(200_000_000)        # ~0.1 s at 2 GHz, bounded: a delay, not a wait
+    moe.moe_cache_apply_swaps(st.cache, plan, n, compute, copy)
+    xs = [I.activations(w.seed, 50 + i, T, w.shape.H) for i in range(6)]
+    ys = [torch.zeros((T, w.shape.H), dtype=torch.float32, device="cuda") for _ in xs]
+    for xb, y in zip(xs, ys):
+        st.forward(0, torch.from_numpy(xb.view(np.int16)).cuda(), y, T, mode=moe.MOE_MODE_DECODE)
+    torch.cuda.synchronize()
+    assert moe.moe_sync_status(st.ws) == moe.MOE_OK
+    exp_, _, slot, src, _, _ = st.ws.groups(T)
+    gi = int(np.flatnonzero(exp_ == A)[0])
+    assert src[gi] == moe.MOE_SRC_RESIDENT and slot[gi] == int(resid0[B])
+    li = st.layers[0].host
+    bias_h = li.bias.copy()
+    bias_h[A] = np.float32(50.0)
+    for xb, y in zip(xs, ys):
+        logits = olayer.router_logits(xb, li.w_router, bias_h)
+        ref = olayer.moe_layer(xb, li.w_router, bias_h, st.k, lambda e: st.expert_host(0, e), st.H, st.I,
+                               resid=st.resid_table(), stage=st.stage_table(), shared=li.shared,
+                               I_shared=st.I_shared, w_shared_gate_bits=li.w_shared_gate, logits=logits)
+        assert (ref.ids[:, 0] == A).all()
+        U.assert_close_layer(y.cpu().numpy(), ref.y)

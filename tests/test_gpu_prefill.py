@@ -1,9 +1,8 @@
 """GPU parity of the prefill path (tcgen05 grouped GEMMs) against the oracle, through the C ABI.
 
-Small ragged shapes are compared in full; the full-size workloads are compared
-on sampled tokens (a token's output depends only on its own experts and the
-shared expert, so the oracle evaluates just those tokens, routed on the GPU's
-fp32 logits)."""
+Every token is compared, at small ragged shapes and at the full-size chunks,
+routed on the GPU's fp32 logits; those logits are held against the oracle's
+within the fp32 accumulation bound."""
 import numpy as np
 import pytest
 import torch
@@ -30,13 +29,31 @@ def run_prefill(st, x_bits, T, bf16_out=False):
     return U.y_to_numpy(y, bf16_out)
 
 
+def check_router(st, x_bits, logits, ids, tokens):
+    """The prefill router GEMM's logits against the oracle's fp64 logits, within the fp32
+    accumulation bound; ids chosen on the GPU logits against the oracle's top-k of the
+    oracle's own logits, where they may differ only at a near-tie within that bound."""
+    li = st.layers[0].host
+    ref_logits = olayer.router_logits(x_bits[tokens], li.w_router, li.bias)
+    bound = U.logits_bound(x_bits[tokens], li.w_router, li.bias)
+    err = np.abs(logits[tokens].astype(np.float64) - ref_logits)
+    assert np.all(err <= bound), f"router logits: {int((err > bound).sum())} beyond the bound, max {err.max():.3g}"
+    o_ids, _ = olayer.top_k(ref_logits, st.k)
+    for i in np.flatnonzero((o_ids != ids[tokens]).any(axis=1)):
+        srt = np.sort(ref_logits[i].astype(np.float64))[::-1]
+        gaps = np.abs(np.diff(srt[: st.k + 1]))
+        assert gaps.min() <= 2 * bound[i].max(), tokens[i]
+
+
 def check_tokens(st, x_bits, y, tokens, tail_skip=0):
     logits, ids, _ = st.ws.routing(x_bits.shape[0])
     logits = logits.cpu().numpy()
+    ids = ids.cpu().numpy()
     li = st.layers[0].host
+    check_router(st, x_bits, logits, ids, tokens)
     # routing on the GPU's own logits matches the oracle's top-k bit for bit
     ref_ids, _ = olayer.top_k(logits[tokens], st.k)
-    assert np.array_equal(ids.cpu().numpy()[tokens], ref_ids)
+    assert np.array_equal(ids[tokens], ref_ids)
     ref = olayer.moe_layer(x_bits[tokens], li.w_router, li.bias, st.k, lambda e: st.expert_host(0, e), st.H, st.I,
                            resid=st.resid_table(), stage=st.stage_table(), shared=li.shared, I_shared=st.I_shared,
                            w_shared_gate_bits=li.w_shared_gate, logits=logits[tokens], tail_skip=tail_skip)
@@ -45,6 +62,8 @@ def check_tokens(st, x_bits, y, tokens, tail_skip=0):
 
 @pytest.mark.parametrize("T,H,I_,E,k,Is,zipf", [
     (300, 256, 128, 16, 2, 128, 0.8),   # ragged token count, groups of many sizes
+    (160, 2048, 512, 64, 4, 512, 1.1),  # the chunk's row widths, router K = 2048
+    (200, 512, 128, 300, 5, 128, 0.0),  # router N of 300 experts (a ragged last N tile)
     (1024, 128, 64, 8, 2, 64, 0.0),     # narrowest rows; groups above 256 tokens (several N tiles)
     (129, 512, 256, 40, 7, 0, 1.2),     # no shared expert, small groups
 ])
@@ -80,16 +99,17 @@ def test_prefill_tail_skip_full(T, H, I_, E, k, Is, zipf, R):
     U.assert_close_layer(y, ref.y)
 
 
-def test_prefill_chunk_t8192_h2048_e512_k10_sampled():
+def test_prefill_chunk_t8192_h2048_e512_k10_all_tokens():
+    """The 8192-token chunk: every token of y against the oracle (512 groups of about 160
+    tokens, so every work item, tile and split point of the persistent GEMMs is compared)."""
     from serving_router_top_gb300.model import ModelState
     w = I.WORKLOADS["prefill_t8192_h2048_e512_k10"]
     st = ModelState(w)
     x_bits = I.activations(w.seed, 0, w.T, w.shape.H)
     y = run_prefill(st, x_bits, w.T)
-    tokens = np.random.default_rng(4).choice(w.T, 12, replace=False)
-    tokens = np.concatenate([tokens, [0, w.T - 1]])
+    tokens = np.arange(w.T)
     ref = check_tokens(st, x_bits, y, tokens)
-    U.assert_close_layer(y[tokens], ref.y, what="sampled y")
+    U.assert_close_layer(y, ref.y, what="y, all tokens")
     # decode and prefill paths agree on a window both can run
     yd = torch.zeros((64, w.shape.H), dtype=torch.float32, device="cuda")
     st.forward(0, torch.from_numpy(x_bits[:64].view(np.int16)).cuda(), yd, 64, mode=moe.MOE_MODE_DECODE)
@@ -99,16 +119,33 @@ def test_prefill_chunk_t8192_h2048_e512_k10_sampled():
     U.assert_close_layer(yd, ref64.y, what="decode window")
 
 
-def test_prefill_large_expert_layer_sampled():
-    """One layer of the 4096-hidden, 256-expert top-6 model (I = I_shared = 2048), 4096-token chunk."""
+def test_prefill_large_expert_layer_all_tokens():
+    """One layer of the 4096-hidden, 256-expert top-6 model (I = I_shared = 2048), 4096-token
+    chunk, every token against the oracle."""
     from serving_router_top_gb300.model import ModelState
     w = I.WORKLOADS["large_h4096_e256_k6"]
     st = ModelState(w, layers=1)
     x_bits = I.activations(w.seed, 0, w.T, w.shape.H)
     y = run_prefill(st, x_bits, w.T)
-    tokens = np.random.default_rng(5).choice(w.T, 6, replace=False)
-    ref = check_tokens(st, x_bits, y, tokens)
-    U.assert_close_layer(y[tokens], ref.y, what="sampled y")
+    ref = check_tokens(st, x_bits, y, np.arange(w.T))
+    U.assert_close_layer(y, ref.y, what="y, all tokens")
+
+
+@pytest.mark.parametrize("T", [300, 1100])   # one-CTA grouping; the multi-CTA grouping passes
+def test_prefill_edge_format(T):
+    """Zero, subnormal and 448 block scales and global scales 0.375 / 2.0 / 1.25 (gate, up,
+    down) through the prefill GEMMs, resident and streamed, every token."""
+    from serving_router_top_gb300.model import ModelState
+    w = I.edge_workload(T=T, resident_frac=0.5)
+    st = ModelState(w)
+    x_bits = I.activations(w.seed, 0, T, w.shape.H)
+    y = run_prefill(st, x_bits, T)
+    ref = check_tokens(st, x_bits, y, np.arange(T))
+    U.assert_close_layer(y, ref.y)
+    st2 = ModelState(w, stage_rest=False, nstaging=16)
+    y2 = run_streamed(st2, x_bits, T, 8)
+    ref2 = check_tokens_streamed(st2, x_bits, np.arange(T))
+    U.assert_close_layer(y2, ref2.y, what="streamed y")
 
 
 def run_streamed(st, x_bits, T, U_, bf16_out=False, buffers=2):
@@ -125,9 +162,11 @@ def check_tokens_streamed(st, x_bits, tokens):
     """Reference for a streamed call: every expert of the layer is available (no residency tables)."""
     logits, ids, _ = st.ws.routing(x_bits.shape[0])
     logits = logits.cpu().numpy()
+    ids = ids.cpu().numpy()
     li = st.layers[0].host
+    check_router(st, x_bits, logits, ids, tokens)
     ref_ids, _ = olayer.top_k(logits[tokens], st.k)
-    assert np.array_equal(ids.cpu().numpy()[tokens], ref_ids)
+    assert np.array_equal(ids[tokens], ref_ids)
     return olayer.moe_layer(x_bits[tokens], li.w_router, li.bias, st.k, lambda e: st.expert_host(0, e), st.H, st.I,
                             shared=li.shared, I_shared=st.I_shared, w_shared_gate_bits=li.w_shared_gate,
                             logits=logits[tokens])
@@ -155,16 +194,16 @@ def test_prefill_streamed_small_shapes_full(T, H, I_, E, k, Is, U_):
     U.assert_close_layer(y1, ref.y)
 
 
-def test_prefill_streamed_chunk_t8192_sampled():
-    """The 8192-token chunk with all 512 experts streamed in eight units of 64 (113 MB each)."""
+def test_prefill_streamed_chunk_t8192_all_tokens():
+    """The 8192-token chunk with all 512 experts streamed in eight units of 64 (113 MB each),
+    every token against the oracle."""
     from serving_router_top_gb300.model import ModelState
     w = I.WORKLOADS["prefill_t8192_h2048_e512_k10"]
     st = ModelState(w, resident=np.zeros((1, w.shape.E), dtype=bool), stage_rest=False, nslots=1, nstaging=128)
     x_bits = I.activations(w.seed, 2, w.T, w.shape.H)
     y = run_streamed(st, x_bits, w.T, 64)
-    tokens = np.concatenate([np.random.default_rng(6).choice(w.T, 10, replace=False), [0, w.T - 1]])
-    ref = check_tokens_streamed(st, x_bits, tokens)
-    U.assert_close_layer(y[tokens], ref.y, what="sampled y")
+    ref = check_tokens_streamed(st, x_bits, np.arange(w.T))
+    U.assert_close_layer(y, ref.y, what="y, all tokens")
 
 
 def test_prefill_streamed_rejects_bad_units():
