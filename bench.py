@@ -246,7 +246,9 @@ def algorithmic_bytes(st, G: int, T: int) -> dict:
     dn = G * H * (I_ // 2 + I_ // 16) + (H * (Is // 2 + Is // 16) if Is else 0)
     dn += (T * k + (T if Is else 0)) * (I_ * 4 + H * 4)               # h in, o out
     router = E * H * 2 + T * H * 2 + T * E * 4
-    return {"gateup_decode": gu, "down_decode": dn, "router": router}
+    # the single-kernel decode moves all of it (h stays on chip between its phases only
+    # through L2, so its h traffic is counted as for the separate kernels)
+    return {"gateup_decode": gu, "down_decode": dn, "router": router, "decode_fused": gu + dn + router}
 
 
 def prefill_flops(st, T: int) -> dict:
@@ -258,6 +260,7 @@ def prefill_flops(st, T: int) -> dict:
 
 
 KERNEL_SOURCES = {"gateup_decode": "k_gemv.cu", "down_decode": "k_gemv.cu", "router": "k_route.cu",
+                  "decode_fused": "k_decode.cu",
                   "gateup_gemm": "k_prefill.cu", "down_gemm": "k_prefill.cu"}
 
 

@@ -64,6 +64,9 @@ enum { MOE_SRC_MISSING = -1, MOE_SRC_RESIDENT = 0, MOE_SRC_STAGED = 1, MOE_SRC_S
 /* Forward modes. */
 enum { MOE_MODE_AUTO = 0, MOE_MODE_DECODE = 1, MOE_MODE_PREFILL = 2 };
 
+/* Decode paths (moe_ws_set_decode_path). */
+enum { MOE_DECODE_FUSED = 0, MOE_DECODE_CHAIN = 1 };
+
 typedef struct moe_cache moe_cache; /* residency + staging tables, slot pools, heats, backing store */
 typedef struct moe_ws moe_ws;       /* per-call scratch: logits, ids, groups, h, o, error word */
 
@@ -218,8 +221,38 @@ int moe_ws_set_tail_skip(moe_ws* ws, int min_rank);
 int moe_ws_set_fused_heat(moe_ws* ws, int enable);
 int moe_ws_kernel_times(moe_ws* ws, int max, float* ms_out, const char** names_out, int* n_out);
 
+/* Decode path of later moe_layer_forward calls on this workspace (the same
+ * layer in either case: Strata page, "路由以后，专家怎样分工？").
+ * MOE_DECODE_FUSED (the default) runs a decode call as ONE cooperative kernel
+ * -- router, top-k, groups and lookup (with the heat update and the tail skip
+ * when set), gate/up, down, combine, separated by grid barriers -- whenever the
+ * shapes fit it: T <= 8, T*k <= 256, E <= 256 * (16 / T rounded down to a power
+ * of two, at most 128 / k rounded likewise) and <= 1024, H a power of two in
+ * [512, 2048], I a power of two in [256, 1024], I_shared 0 or I, x, y and
+ * w_router 16-byte aligned, the shared blob 32-byte aligned; other calls run
+ * the chain.  MOE_DECODE_CHAIN always runs the chain of kernels (router,
+ * top-k + groups, gate/up, down, combine).  The single kernel needs every
+ * SM of the device for its CTAs (a cooperative launch: MOE_ECUDA if the device
+ * cannot hold them at once).  Results agree within the layer's tolerance, not
+ * bit for bit (the fp32 sums run in another order); ids, groups and lookups
+ * are decided on each path's own logits.  MOE_EINVAL for another value.
+ * Host-side setting, no stream work. */
+int moe_ws_set_decode_path(moe_ws* ws, int path);
+
+/* Fault-injection hook for tests of the bounded waits: the grid barriers of
+ * the single-kernel decode give up after wait_ns nanoseconds (default one
+ * second) and, with phantom_arrivals > 0, wait for that many arrivals beyond
+ * the grid, which never come -- so the wait expires, MOE_ETIMEOUT is recorded
+ * in the device error word, the CTAs skip the rest of the call (its outputs
+ * are undefined) and the context stays usable.  moe_sync_status() resets the
+ * barrier when it returns MOE_ETIMEOUT.  phantom_arrivals 0 restores normal
+ * operation; wait_ns 0, phantom_arrivals < 0 or > 1024 is MOE_EINVAL.
+ * Host-side setting, no stream work. */
+int moe_ws_set_wait_test(moe_ws* ws, unsigned long long wait_ns, int phantom_arrivals);
+
 /* Synchronise `stream`, return the device error word (MOE_OK if none) and
- * reset it to MOE_OK. */
+ * reset it to MOE_OK (after MOE_ETIMEOUT also the single-kernel decode's grid
+ * barrier). */
 int moe_sync_status(moe_ws* ws, moe_stream_t stream);
 const char* moe_strerror(int code);
 

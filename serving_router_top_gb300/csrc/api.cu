@@ -288,6 +288,7 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   const size_t o_o = cv.take<float>((Tk + maxT) * s.H);
   const size_t o_gscr = cv.take<int32_t>((size_t(maxT) / 256 + 2) * s.E);
   const size_t o_err = cv.take<int32_t>(1);
+  const size_t o_bar = cv.take<unsigned long long>(kBarWords);
   uint8_t* base = nullptr;
   if (cudaMalloc(&base, cv.off) != cudaSuccess) {
     cudaGetLastError();
@@ -323,6 +324,10 @@ int moe_ws_create(moe_ws** out, int maxT, moe_layer_shape s) {
   w->o = reinterpret_cast<float*>(base + o_o);
   w->grp_scratch = reinterpret_cast<int32_t*>(base + o_gscr);
   w->error = reinterpret_cast<int32_t*>(base + o_err);
+  w->bar = reinterpret_cast<unsigned long long*>(base + o_bar);
+  w->bar_extra = 0;
+  w->wait_ns = 1000000000ull;  // one second
+  w->decode_path = MOE_DECODE_FUSED;
   if (cudaMemset(base, 0, cv.off) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
     cudaFree(base);
@@ -364,6 +369,19 @@ int moe_ws_set_fused_heat(moe_ws* w, int enable) {
   return MOE_OK;
 }
 
+int moe_ws_set_decode_path(moe_ws* w, int path) {
+  if (!w || (path != MOE_DECODE_FUSED && path != MOE_DECODE_CHAIN)) return MOE_EINVAL;
+  w->decode_path = path;
+  return MOE_OK;
+}
+
+int moe_ws_set_wait_test(moe_ws* w, unsigned long long wait_ns, int phantom_arrivals) {
+  if (!w || wait_ns == 0 || phantom_arrivals < 0 || phantom_arrivals > 1024) return MOE_EINVAL;
+  w->wait_ns = wait_ns;
+  w->bar_extra = unsigned(phantom_arrivals);
+  return MOE_OK;
+}
+
 int moe_ws_set_tail_skip(moe_ws* w, int min_rank) {
   if (!w || min_rank < 0) return MOE_EINVAL;
   w->tail_skip = min_rank;
@@ -400,6 +418,8 @@ int moe_sync_status(moe_ws* w, moe_stream_t stream) {
   int32_t e = 0;
   MOE_CUDA_TRY(cudaMemcpy(&e, w->error, 4, cudaMemcpyDeviceToHost));
   MOE_CUDA_TRY(cudaMemset(w->error, 0, 4));
+  // a grid-barrier wait that gave up leaves the barrier's count behind: start it afresh
+  if (e == MOE_ETIMEOUT) MOE_CUDA_TRY(cudaMemset(w->bar, 0, kBarWords * sizeof(unsigned long long)));
   return e;
 }
 
@@ -489,6 +509,12 @@ int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y
                   (s.I_shared > 0 && (reinterpret_cast<uintptr_t>(d->w_shared_gate) & 15))))
     return MOE_EINVAL;
   ws->prof_n = 0;
+  if (!prefill && ws->decode_path == MOE_DECODE_FUSED) {  // one cooperative kernel where the shapes fit
+    ProfScope p(ws, "decode_fused", st);
+    rc = launch_decode_fused(d, c, x, y, y_is_fp32, T, ws, st);
+    if (rc != kNotFused) return rc;
+    ws->prof_n = 0;
+  }
   {
     ProfScope p(ws, "router", st);
     if (prefill)

@@ -13,6 +13,7 @@ namespace moe {
 // ---------------------------------------------------------------- limits
 constexpr int kMaxE = 1024;        // experts per layer (top-k keeps E/32 logits per lane)
 constexpr int kMaxK = 32;          // experts per token
+constexpr int kBarWords = 16;      // grid-barrier counter of the single-kernel decode (one 128-byte line)
 constexpr int kStats = 5;          // lookup counters per layer: groups, hits, staged, missing, skipped
 constexpr int kBlobHeader = 256;   // bytes before the first region of a blob
 constexpr uint32_t kBlobMagic = 0x42454f4du;  // "MOEB"
@@ -268,6 +269,10 @@ struct moe_ws {
   float* o;             // [maxT*k + maxT, H] routed outputs by position, then shared outputs
   int32_t* grp_scratch; // [(maxT/256 + 1) * E + E] grouping of long windows: per-tile counts, offsets
   int32_t* error;       // [1]
+  unsigned long long* bar;  // [kBarWords] grid-barrier arrivals of the single-kernel decode (zero at creation)
+  unsigned bar_extra;   // arrivals that barrier waits for beyond the grid (0; a fault-injection hook for tests)
+  unsigned long long wait_ns;  // bound of each grid-barrier wait
+  int decode_path;      // MOE_DECODE_FUSED or MOE_DECODE_CHAIN
   int fused_heat;       // groupings with a cache also add the window's counts to the layer's heat
   int tail_skip;        // groupings drop non-resident experts ranked at or past this by all choosers (0: off)
   // optional per-kernel timing of the most recent call

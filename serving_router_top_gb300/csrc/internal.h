@@ -23,6 +23,11 @@ int launch_combine(const moe_layer_desc* d, void* y, int y_is_fp32, int T, moe_w
 constexpr int kGemvNotApplicable = -1;
 int launch_gemv_decode(bool gateup, const moe_layer_desc* d, int T, moe_ws* ws, cudaStream_t s);
 
+// The whole decode forward as one cooperative kernel (router, top-k, groups and
+// lookup, gate/up, down, combine); kNotFused when the shapes call for the chain.
+int launch_decode_fused(const moe_layer_desc* d, moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
+                        moe_ws* ws, cudaStream_t s);
+
 // Prefill path (tcgen05 GEMMs): router logits and gate logit, then the
 // experts, which write y directly.  x rows must be 16-byte aligned.
 bool prefill_supported(const moe_layer_shape& s);

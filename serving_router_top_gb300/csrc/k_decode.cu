@@ -1,0 +1,952 @@
+// The decode forward of one MoE layer in a single cooperative kernel.
+//
+// Strata expert paths: "显存里缓存的是什么？" (the router picks each token's
+// experts and merge weights), "路由以后，专家怎样分工？" (repeated experts of a
+// window form one group with input and output positions; outputs are weighted,
+// summed, and the gated shared expert is added), "哪些专家能长期留在显存？"
+// (the residency table maps (layer, expert) to a slot), "CPU 怎样把剩下的专家
+// 算完？" (gate/up, the activation, then the down projection).
+//
+// A decode window of a few tokens touches tens of experts but moves only a few
+// tens of megabytes, so a chain of dependent launches spends more time between
+// and inside the prologues of its kernels than streaming weights.  Here one CTA
+// per SM runs every step, the CTAs meeting at two grid barriers:
+//
+//   A  router logits and the shared-gate logit: CTA c owns rows c, c + ncta, ...
+//      (row E is the gate vector), each row cut into 512-element slices, one
+//      slice per warp, fp32 sums of exact bf16 products; the CTA meanwhile
+//      prefetches its slice of the shared expert's blob into L2 and stages x,
+//      then x as f16 times a per-token power of two (exact for bf16 values).
+//   -- grid barrier --
+//   B  every CTA reads all T x E logits and runs the same top-k and the same
+//      grouping on them, so every CTA holds the same groups without another
+//      barrier; CTA 0 writes them, with the top-k, lookups, statistics and the
+//      heat update, to the workspace.  Each CTA then issues bulk L2 prefetches
+//      of every weight byte it will read in C and D: the step's expert bytes
+//      stream from HBM at once instead of behind each consumer's own loads.
+//   C  gate/up: tasks are (group, 16-row block of I), CTA c owns a contiguous
+//      range of them, and the (task, 256-column chunk) units go round-robin to
+//      the 16 warps; mma.sync m16n8k16 f16 -> f32 with the weights dequantised
+//      exactly into f16 (E2M1 code x E4M3 scale) as A and up to 8 of the
+//      group's token rows as B; partial tiles are summed in chunk order and the
+//      epilogue writes h = SiLU(gs_g g) * gs_u u (fp32) and max|h| per row.
+//   -- grid barrier --
+//   D  down and combine: CTA c owns 16-row blocks c, c + ncta, ... of the
+//      output.  It reads every entry's h row (f16 times a per-row power of two,
+//      exact to 11 bits), runs the (group, 256-column chunk) units of its row
+//      block and then, per token, y = sum_r w[t,r] o[t,r] + sigmoid(gl_t) s_t
+//      in rank order with the shared term last -- deterministic, no atomics.
+//
+// Every wait is bounded (the grid barriers give up after the workspace's wait
+// limit, record MOE_ETIMEOUT and the CTAs skip the remaining phases).
+#include "dequant.cuh"
+#include "topk.cuh"
+
+namespace moe {
+namespace dec {
+
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kChunk = 256;        // columns per unit: a lane's 64 columns, one 32-byte load per row
+constexpr int kMaxT = 8;           // tokens (the MMA's N)
+constexpr int kMaxEnt = 256;       // T * k
+constexpr int kMaxGroups = kMaxEnt + 1;
+constexpr int kMaxUnits = 64;      // gate/up partial tiles held per round
+constexpr int kSlice = 512;        // router row elements per warp pair
+constexpr int kMaxPairs = 2 * kWarps;
+constexpr int kTopkKP1 = 16;       // logits per lane of a top-k slice at most (E / warps-per-token <= 512)
+constexpr int kPadH = 32;          // f16 elements after each activation row: a row stride of 64 mod 128 bytes
+
+struct Args {
+  const uint16_t* x;         // bf16 [T, H]
+  const uint16_t* w_router;  // bf16 [E, H]
+  const float* bias;         // [E] or null
+  const uint16_t* w_sg;      // bf16 [H] or null
+  const uint8_t* shared_blob;
+  int T, H, I, E, k, layer, has_shared, Gw;
+  DevBlobLayout lay;
+  // the cache
+  const int32_t* resid;
+  const int32_t* stage;
+  const uint8_t* slots;
+  const uint8_t* staging;
+  size_t blob_bytes, shared_bytes;
+  int nslots, nstaging, tail_skip;
+  unsigned long long* stats;
+  float* heat_row;
+  // the workspace
+  float* logits;
+  float* gate_logit;
+  int32_t* topk_ids;
+  float* topk_w;
+  int32_t* num_groups;
+  int32_t* grp_expert;
+  int32_t* grp_off;
+  int32_t* grp_slot;
+  int32_t* grp_src;
+  const uint8_t** grp_blob;
+  int32_t* ent_tok;
+  int32_t* ent_pos;
+  float* h;
+  float* hmax;
+  float* o;                  // [(maxTk + maxT), H] expert outputs by position, then the shared rows
+  int Imax, maxTk;
+  void* y;
+  int y_fp32;
+  int32_t* err;
+  unsigned long long* bar;   // grid-barrier arrivals (a multiple of the grid between launches)
+  unsigned bar_extra;        // arrivals a barrier waits for beyond the grid (0; a test hook)
+  unsigned long long wait_ns;
+  // shared-memory carve (byte offsets)
+  int o_x16, o_xs, o_lg, o_cand, o_part, o_red, o_h16, o_small;
+};
+
+// Small tables, at the end of shared memory.
+struct Small {
+  int32_t ids[kMaxEnt];
+  float w[kMaxEnt];
+  uint32_t key[kMaxEnt];
+  uint32_t srt[kMaxEnt];
+  int32_t start[kMaxEnt];
+  int32_t ent_tok[kMaxEnt];
+  int32_t ent_pos[kMaxEnt];
+  int32_t inv[kMaxEnt];
+  int32_t gexp[kMaxGroups];
+  int32_t goff[kMaxGroups + 1];
+  int32_t gsrc[kMaxGroups];
+  const uint8_t* gblob[kMaxGroups];
+  float gs[kMaxGroups][3];
+  float xinv[kMaxT];
+  float gl[kMaxT];
+  float hs_inv[kMaxEnt + kMaxT];
+  int32_t resid[1024];  // the layer's residency and staging rows
+  int32_t stage[1024];
+  int G, ok, cnt[4];
+};
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Grid barrier on a monotonic arrival counter: every barrier of every launch
+// adds one arrival per CTA, so a barrier is complete when the counter reaches
+// the next multiple of the arrivals it expects (N = the grid, plus the test
+// hook's phantom arrivals).  One acquire-release add per CTA, then acquire
+// loads until the count is reached -- at most wait_ns, after which the wait
+// records MOE_ETIMEOUT and every later phase of the CTA is skipped (the host
+// resets the counter with the error word).  (A two-level tree of counters was
+// measured slower: its last arrival pays two dependent atomic round trips.)
+// Returns whether the barrier was passed.  Every thread of the CTA calls it.
+__device__ bool grid_barrier(const Args& a, Small& sm) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = sm.ok;
+    if (ok) {
+      const unsigned long long N = gridDim.x + a.bar_extra;
+      const unsigned long long old = atom_add_acq_rel_gpu(a.bar, 1ull);
+      const unsigned long long target = (old / N + 1) * N;
+      if (old + 1 != target) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (ld_acquire_gpu(a.bar) < target) {
+          if (globaltimer_ns() - t0 > a.wait_ns) {
+            set_error(a.err, MOE_ETIMEOUT);
+            ok = 0;
+            break;
+          }
+        }
+      }
+    }
+    sm.ok = ok;
+  }
+  __syncthreads();
+  return *reinterpret_cast<volatile int*>(&sm.ok) != 0;
+}
+
+// Column c of an activation row is stored where lane (., t4) finds its eight
+// columns 8q..8q+7 of each 256-column chunk as one 16-byte load: chunk-major,
+// then (q, t4), then the eight values.  Four lanes of a row read 64
+// consecutive bytes; with the row stride 64 mod 128 bytes, two rows' quarter
+// warps touch disjoint banks.
+__device__ __forceinline__ int perm_col(int c) {
+  const int cc = c & (kChunk - 1);
+  return (c - cc) + (((cc & 63) >> 3) * 4 + (cc >> 6)) * 8 + (c & 7);
+}
+
+// One unit as loaded by a lane: rows g8 and g8 + 8 of each matrix, the lane's
+// 64 columns (32 code bytes per row) and their four block scales.
+template <int NM>
+struct UnitRegs {
+  uint32_t c[NM][2][8];
+  uint32_t s[NM][2];
+};
+
+template <int NM>
+__device__ __forceinline__ void load_unit(const uint8_t* blob, const DevBlobLayout& lay, int mat0, int K, int row,
+                                          int ch, int t4, UnitRegs<NM>& R) {
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+    const uint8_t* cp = blob + lay.code_off[mat0 + m] + size_t(row) * (K / 2) + ch * 128 + 32 * t4;
+    ld_stream32(cp, R.c[m][0]);
+    ld_stream32(cp + size_t(8) * (K / 2), R.c[m][1]);
+    const uint8_t* sp = blob + lay.scale_off[mat0 + m] + size_t(row) * (K / 16) + ch * 16 + 4 * t4;
+    R.s[m][0] = ld_stream_u32(sp);
+    R.s[m][1] = ld_stream_u32(sp + size_t(8) * (K / 16));
+  }
+}
+
+// acc[m][even/odd MMA] += dq(W rows) . B for the lane's 64 columns of chunk ch.
+// brow: the lane's B row (activations, f16, perm_col layout), or null (zeros).
+template <int NM>
+__device__ __forceinline__ void mma_unit(const UnitRegs<NM>& R, const __half* brow, int ch, int t4,
+                                         float (&acc)[NM][2][4]) {
+  const uint4* xp = brow ? reinterpret_cast<const uint4*>(brow + ch * kChunk) + t4 : nullptr;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint4 xq = xp ? xp[q * 4] : make_uint4(0u, 0u, 0u, 0u);
+    const int blk = q >> 1;
+#pragma unroll
+    for (int m = 0; m < NM; ++m) {
+      const uint32_t sa = scale_pair((R.s[m][0] >> (8 * blk)) & 0xffu);
+      const uint32_t sb = scale_pair((R.s[m][1] >> (8 * blk)) & 0xffu);
+      const uint32_t w0 = R.c[m][0][q], w1 = R.c[m][1][q];
+      uint32_t a0, a1, a2, a3;
+      e2m1_pair2(w0, a0, a2);
+      e2m1_pair2(w1, a1, a3);
+      mma16816(acc[m][0], hmul2(a0, sa), hmul2(a1, sb), hmul2(a2, sa), hmul2(a3, sb), xq.x, xq.y);
+      e2m1_pair2(w0 >> 16, a0, a2);
+      e2m1_pair2(w1 >> 16, a1, a3);
+      mma16816(acc[m][1], hmul2(a0, sa), hmul2(a1, sb), hmul2(a2, sa), hmul2(a3, sb), xq.z, xq.w);
+    }
+  }
+}
+
+// KP1: logits per lane of a warp's top-k slice (4 when the slice fits 128 logits, else 16).
+template <int KP1>
+__global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __half* x16 = reinterpret_cast<__half*>(smem + a.o_x16);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + a.o_xs);
+  float* lg = reinterpret_cast<float*>(smem + a.o_lg);
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem + a.o_cand);
+  float* part = reinterpret_cast<float*>(smem + a.o_part);
+  float* red = reinterpret_cast<float*>(smem + a.o_red);
+  __half* h16 = reinterpret_cast<__half*>(smem + a.o_h16);
+  Small& sm = *reinterpret_cast<Small*>(smem + a.o_small);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, t4 = lane & 3;
+  const int cta = blockIdx.x, ncta = gridDim.x;
+  const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k;
+  const int n = T * k;
+  const int XR = H + kPadH, HR = I + kPadH;
+  const bool lead = cta == 0;
+  int32_t* err = lead ? a.err : nullptr;
+
+  // ================================================================ A: router
+  if (tid == 0) sm.ok = 1;
+  // this CTA's slice of the shared expert's blob into L2 (its gate/up tasks run in C)
+  if (a.has_shared && tid == 0) {
+    const size_t slice = ((a.shared_bytes + ncta - 1) / ncta + 15) & ~size_t(15);
+    const size_t b0 = size_t(cta) * slice;
+    if (b0 < a.shared_bytes) {
+      const size_t nb = (a.shared_bytes - b0 < slice ? a.shared_bytes - b0 : slice) & ~size_t(15);
+      if (nb) prefetch_bulk_l2(a.shared_blob + b0, uint32_t(nb));
+    }
+  }
+  // router rows of this CTA: row E is the shared gate vector
+  const int rows_total = E + (a.w_sg ? 1 : 0);
+  const int nrows = cta < rows_total ? (rows_total - 1 - cta) / ncta + 1 : 0;
+  const int QS = H / kSlice;
+  const int npairs = nrows * QS;
+  // the first of the warp's slices into registers now (no kernel writes the router weights);
+  // later slices (more than 16 per CTA) are loaded when their turn comes
+  auto router_row = [&](int p) {
+    const int j = p / QS, q = p - j * QS, row = cta + j * ncta;
+    return reinterpret_cast<const uint4*>(row < E ? a.w_router + size_t(row) * H : a.w_sg) + q * (kSlice / 8);
+  };
+  uint4 wv0 = make_uint4(0u, 0u, 0u, 0u), wv1 = wv0;
+  if (warp < npairs) {
+    const uint4* wr = router_row(warp);
+    wv0 = __ldg(wr + lane);
+    wv1 = __ldg(wr + 32 + lane);
+  }
+  // x into shared memory (all loads of a thread in flight together), and the
+  // layer's residency and staging rows for the lookups of phase B
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(a.x);
+    uint4* dst = reinterpret_cast<uint4*>(xs);
+    const int n16 = T * H / 8;
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = tid + j * kThreads;
+      if (i < n16) v[j] = src[i];
+    }
+    int32_t rv[2], sv[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int e = tid + j * kThreads;
+      rv[j] = e < E ? a.resid[size_t(a.layer) * E + e] : -1;
+      sv[j] = (e < E && a.stage) ? a.stage[size_t(a.layer) * E + e] : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = tid + j * kThreads;
+      if (i < n16) dst[i] = v[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int e = tid + j * kThreads;
+      if (e < E) {
+        sm.resid[e] = rv[j];
+        sm.stage[e] = sv[j];
+      }
+    }
+  }
+  // the expert kernels accumulate max|h| per row with atomicMax from phase C on
+  if (lead) {
+    for (int i = tid; i < n; i += kThreads) a.hmax[i] = 0.f;
+    for (int i = tid; i < T; i += kThreads) a.hmax[a.maxTk + i] = 0.f;
+  }
+  __syncthreads();
+  // per-token power of two, and x as f16 in the permuted layout
+  if (warp < T) {
+    float m = 0.f;
+    for (int i = lane; i < H / 8; i += 32) {
+      const uint4 q = reinterpret_cast<const uint4*>(xs + warp * H)[i];
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[j] << 16)), fabsf(__uint_as_float(u[j] & 0xffff0000u))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) sm.xinv[warp] = pow2_scale_for(m);
+  }
+  // router partial sums: the lane's 16 elements of the slice, each token
+#pragma unroll 1
+  for (int p = warp; p < npairs; p += kWarps) {
+    if (p != warp) {
+      const uint4* wr = router_row(p);
+      wv0 = __ldg(wr + lane);
+      wv1 = __ldg(wr + 32 + lane);
+    }
+    const int q = p % QS;
+    float pacc[kMaxT];
+#pragma unroll
+    for (int t = 0; t < kMaxT; ++t) pacc[t] = 0.f;
+#pragma unroll
+    for (int hv = 0; hv < 2; ++hv) {
+      const uint4 w4 = hv ? wv1 : wv0;
+      const uint32_t wu[4] = {w4.x, w4.y, w4.z, w4.w};
+      const int c0 = q * kSlice + (hv * 32 + lane) * 8;
+#pragma unroll
+      for (int t = 0; t < kMaxT; ++t) {
+        if (t < T) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * H + c0);
+          const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            pacc[t] = fmaf(__uint_as_float(wu[j] << 16), __uint_as_float(xu[j] << 16), pacc[t]);
+            pacc[t] = fmaf(__uint_as_float(wu[j] & 0xffff0000u), __uint_as_float(xu[j] & 0xffff0000u), pacc[t]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kMaxT; ++t) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) pacc[t] += __shfl_xor_sync(0xffffffffu, pacc[t], o);
+    }
+    if (lane < T) {
+      float v = pacc[0];
+#pragma unroll
+      for (int t = 1; t < kMaxT; ++t)
+        if (lane == t) v = pacc[t];
+      part[p * kMaxT + lane] = v;
+    }
+  }
+  __syncthreads();
+  // slices summed in order, plus the bias: the logits of this CTA's rows
+  for (int i = tid; i < nrows * T; i += kThreads) {
+    const int j = i / T, t = i - j * T, row = cta + j * ncta;
+    float v = 0.f;
+    for (int q = 0; q < QS; ++q) v += part[(j * QS + q) * kMaxT + t];
+    if (row < E)
+      a.logits[size_t(t) * E + row] = a.bias ? __fadd_rn(v, a.bias[row]) : v;
+    else
+      a.gate_logit[t] = v;
+  }
+  // x as f16 times the token's power of two (read by every gate/up unit), eight
+  // consecutive columns -- one 16-byte group of the permuted layout -- per item
+  for (int i = tid; i < T * H / 8; i += kThreads) {
+    const int t = (i * 8) / H, c = i * 8 - t * H;
+    const uint4 q = reinterpret_cast<const uint4*>(xs)[i];
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+    const float sc = sm.xinv[t];
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __half2 hh = __floats2half2_rn(__uint_as_float(u[j] << 16) * sc, __uint_as_float(u[j] & 0xffff0000u) * sc);
+      o[j] = *reinterpret_cast<uint32_t*>(&hh);
+    }
+    *reinterpret_cast<uint4*>(x16 + t * XR + perm_col(c)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (!grid_barrier(a, sm)) return;
+
+  // ============================================================ B: top-k, groups
+  for (int i0 = 0; i0 < T * E; i0 += 8 * kThreads) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + tid + j * kThreads;
+      if (i < T * E) v[j] = __ldcg(a.logits + i);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + tid + j * kThreads;
+      if (i < T * E) lg[i] = v[j];
+    }
+  }
+  if (tid < T) sm.gl[tid] = a.has_shared ? __ldcg(a.gate_logit + tid) : 0.f;
+  if (tid < T) sm.xinv[tid] = 1.0f / sm.xinv[tid];
+  __syncthreads();
+  topk_tokens_cta<KP1>(lg, T, E, k, a.Gw, sm.ids, sm.w, err, cand);
+  __syncthreads();
+  // groups: sort the n selections by (expert, position); position t*k + r orders like the token
+  for (int i = tid; i < n; i += kThreads) sm.key[i] = (uint32_t(sm.ids[i]) << 16) | uint32_t(i);
+  __syncthreads();
+  for (int i = tid; i < n; i += kThreads) {
+    const uint32_t kk = sm.key[i];
+    int r = 0;
+    for (int j = 0; j < n; ++j) r += sm.key[j] < kk ? 1 : 0;
+    sm.srt[r] = kk;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += kThreads) {
+    const uint32_t kk = sm.srt[i];
+    const int pos = int(kk & 0xffffu);
+    sm.start[i] = (i == 0 || (sm.srt[i - 1] >> 16) != (kk >> 16)) ? 1 : 0;
+    sm.ent_pos[i] = pos;
+    sm.ent_tok[i] = pos / k;
+    sm.inv[pos] = i;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += kThreads) {
+    if (sm.start[i]) {
+      int g = 0;
+      for (int j = 0; j < i; ++j) g += sm.start[j];
+      sm.gexp[g] = int(sm.srt[i] >> 16);
+      sm.goff[g] = i;
+    }
+  }
+  if (tid == 0) {
+    int g = 0;
+    for (int j = 0; j < n; ++j) g += sm.start[j];
+    sm.G = g;
+    sm.cnt[0] = sm.cnt[1] = sm.cnt[2] = sm.cnt[3] = 0;
+  }
+  __syncthreads();
+  const int G = sm.G;
+  const int Gt = G + a.has_shared;
+  if (tid == 0) sm.goff[G] = n;
+  // lookup of each routed group (the same tables in every CTA: the same result)
+  for (int g = tid; g < G; g += kThreads) {
+    const int e = sm.gexp[g], e0 = sm.goff[g], e1 = (g + 1 < G) ? sm.goff[g + 1] : n;
+    int slot = sm.resid[e];
+    const int st = sm.stage[e];
+    int src = MOE_SRC_MISSING;
+    const uint8_t* blob = nullptr;
+    if (slot >= 0) {
+      if (slot < a.nslots) { src = MOE_SRC_RESIDENT; blob = a.slots + size_t(slot) * a.blob_bytes; }
+      else { set_error(err, MOE_ERANGE); slot = -1; }
+    }
+    bool tail = false;
+    if (a.tail_skip > 0 && src != MOE_SRC_RESIDENT) {
+      int mr = k;
+      for (int i = e0; i < e1; ++i) mr = min(mr, sm.ent_pos[i] % k);
+      tail = mr >= a.tail_skip;
+    }
+    if (tail) {
+      src = MOE_SRC_SKIPPED;
+      slot = -1;
+    } else if (src == MOE_SRC_MISSING) {
+      if (st >= 0 && st < a.nstaging) { slot = st; src = MOE_SRC_STAGED; blob = a.staging + size_t(st) * a.blob_bytes; }
+      else if (st >= a.nstaging) set_error(err, MOE_ERANGE);
+      if (src == MOE_SRC_MISSING) { slot = -1; set_error(err, MOE_EMISSING); }
+    }
+    sm.gsrc[g] = src;
+    sm.gblob[g] = blob;
+    if (lead) {
+      a.grp_expert[g] = e;
+      a.grp_off[g] = e0;
+      a.grp_slot[g] = slot;
+      a.grp_src[g] = src;
+      a.grp_blob[g] = blob;
+      atomicAdd(&sm.cnt[src == MOE_SRC_RESIDENT ? 0 : src == MOE_SRC_STAGED ? 1 : src == MOE_SRC_SKIPPED ? 3 : 2], 1);
+      if (a.heat_row) a.heat_row[e] = __fadd_rn(a.heat_row[e], float(e1 - e0));  // as the heat-update kernel
+    }
+  }
+  if (a.has_shared && tid == 0) {
+    sm.gblob[G] = a.shared_blob;
+    sm.gsrc[G] = MOE_SRC_RESIDENT;
+    sm.goff[G + 1] = n + T;  // the shared expert's entries are the T tokens, after the routed ones
+  }
+  __syncthreads();
+  if (lead) {
+    for (int i = tid; i < n; i += kThreads) {
+      a.topk_ids[i] = sm.ids[i];
+      a.topk_w[i] = sm.w[i];
+      a.ent_tok[i] = sm.ent_tok[i];
+      a.ent_pos[i] = sm.ent_pos[i];
+    }
+    if (tid == 0) {
+      *a.num_groups = G;
+      a.grp_off[G] = n;
+      if (a.stats) add_stats(a.stats + size_t(a.layer) * kStats, G, sm.cnt[0], sm.cnt[1], sm.cnt[2], sm.cnt[3]);
+    }
+  }
+  // Work of phases C and D: gate/up tasks (group, 16-row block of I) and down tasks
+  // (group, 16-row block of H), each list group-major; CTA c owns a contiguous range of
+  // each, and prefetches its weight bytes into L2 now -- one bulk prefetch per group and
+  // region, the rows of consecutive tasks of a group being contiguous.
+  const int TPG = I / 16, NRB = H / 16;
+  const int NT = Gt * TPG, ND = Gt * NRB;
+  const int t0 = int((long long)cta * NT / ncta), t1 = int((long long)(cta + 1) * NT / ncta);
+  const int d0 = int((long long)cta * ND / ncta), d1 = int((long long)(cta + 1) * ND / ncta);
+  {
+    const int gu_g0 = t0 / TPG, gu_n = t1 > t0 ? (t1 - 1) / TPG - gu_g0 + 1 : 0;
+    const int dn_g0 = d0 / NRB, dn_n = d1 > d0 ? (d1 - 1) / NRB - dn_g0 + 1 : 0;
+    for (int p = tid; p < 4 * gu_n + 2 * dn_n; p += kThreads) {
+      if (p < 4 * gu_n) {
+        const int gi = gu_g0 + p / 4, part_i = p & 3, m = part_i & 1;
+        const uint8_t* blob = sm.gblob[gi];
+        if (!blob) continue;
+        const int ta = max(t0, gi * TPG) - gi * TPG, tb = min(t1, (gi + 1) * TPG) - gi * TPG;  // [ta, tb)
+        if (part_i < 2)
+          prefetch_bulk_l2(blob + a.lay.code_off[m] + size_t(ta) * 16 * (H / 2), uint32_t((tb - ta) * 16 * (H / 2)));
+        else
+          prefetch_bulk_l2(blob + a.lay.scale_off[m] + size_t(ta) * 16 * (H / 16), uint32_t((tb - ta) * 16 * (H / 16)));
+      } else {
+        const int q = p - 4 * gu_n, gi = dn_g0 + q / 2, part_i = q & 1;
+        const uint8_t* blob = sm.gblob[gi];
+        if (!blob) continue;
+        const int ra = max(d0, gi * NRB) - gi * NRB, rbb = min(d1, (gi + 1) * NRB) - gi * NRB;
+        if (part_i == 0)
+          prefetch_bulk_l2(blob + a.lay.code_off[2] + size_t(ra) * 16 * (I / 2), uint32_t((rbb - ra) * 16 * (I / 2)));
+        else
+          prefetch_bulk_l2(blob + a.lay.scale_off[2] + size_t(ra) * 16 * (I / 16), uint32_t((rbb - ra) * 16 * (I / 16)));
+      }
+    }
+  }
+
+  // the groups' global scales (read after the prefetches are on their way; used from the
+  // first epilogue on, after the __syncthreads that ends each round of units)
+  for (int g = tid; g < Gt; g += kThreads) {
+    const BlobHeader* hd = reinterpret_cast<const BlobHeader*>(sm.gblob[g]);
+    sm.gs[g][0] = hd ? hd->gscale[0] : 0.f;
+    sm.gs[g][1] = hd ? hd->gscale[1] : 0.f;
+    sm.gs[g][2] = hd ? hd->gscale[2] : 0.f;
+  }
+
+  // ============================================================ C: gate/up
+  const int NCH = H / kChunk;
+  const int U = (t1 - t0) * NCH;
+  for (int r0 = 0; r0 < U; r0 += kMaxUnits) {
+    const int nu = min(kMaxUnits, U - r0);
+    auto unit_at = [&](int u, int& gi, int& tb, int& ch) {
+      const int task = t0 + u / NCH;
+      ch = u - (u / NCH) * NCH;
+      gi = task / TPG;
+      tb = task - gi * TPG;
+    };
+    auto load = [&](int u, UnitRegs<2>& R) {
+      if (u >= r0 + nu) return;
+      int gi, tb, ch;
+      unit_at(u, gi, tb, ch);
+      const uint8_t* blob = sm.gblob[gi];
+      if (blob) load_unit<2>(blob, a.lay, 0, H, tb * 16 + g8, ch, t4, R);
+    };
+    auto run = [&](int u, const UnitRegs<2>& R) {
+      if (u >= r0 + nu) return;
+      int gi, tb, ch;
+      unit_at(u, gi, tb, ch);
+      const int e0 = sm.goff[gi], nv = sm.goff[gi + 1] - e0;
+      float acc[2][2][4];
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[m][q >> 2][q & 3] = 0.f;
+      if (sm.gblob[gi]) {
+        const __half* brow = nullptr;
+        if (g8 < nv) brow = x16 + size_t(gi == G ? g8 : sm.ent_tok[e0 + g8]) * XR;
+        mma_unit<2>(R, brow, ch, t4, acc);
+      }
+      float4* dst = reinterpret_cast<float4*>(red + (size_t(u - r0) * 32 + lane) * 8);
+      dst[0] = make_float4(acc[0][0][0] + acc[0][1][0], acc[0][0][1] + acc[0][1][1], acc[0][0][2] + acc[0][1][2],
+                           acc[0][0][3] + acc[0][1][3]);
+      dst[1] = make_float4(acc[1][0][0] + acc[1][1][0], acc[1][0][1] + acc[1][1][1], acc[1][0][2] + acc[1][1][2],
+                           acc[1][0][3] + acc[1][1][3]);
+    };
+    // two units in flight per warp: the next one loads while this one computes
+    UnitRegs<2> ra, rb;
+    int u = r0 + warp;
+    load(u, ra);
+    load(u + kWarps, rb);
+    for (; u < r0 + nu; u += 2 * kWarps) {
+      run(u, ra);
+      load(u + 2 * kWarps, ra);
+      run(u + kWarps, rb);
+      load(u + 3 * kWarps, rb);
+    }
+    __syncthreads();
+    // each task's chunks summed in order; epilogue h = SiLU(gs_g g / s_x) * (gs_u u / s_x)
+    const int ntk = nu / NCH;
+    for (int idx = tid; idx < ntk * 32; idx += kThreads) {
+      const int tl = idx >> 5;
+      const int task = t0 + r0 / NCH + tl, gi = task / TPG, tb = task - gi * TPG;
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.f;
+      for (int c = 0; c < NCH; ++c) {
+        const float4* src = reinterpret_cast<const float4*>(red + (size_t(tl * NCH + c) * 32 + lane) * 8);
+        const float4 p0 = src[0], p1 = src[1];
+        v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
+        v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+      }
+      const bool shared = gi == G;
+      const bool has_blob = sm.gblob[gi] != nullptr;
+      const int e0 = sm.goff[gi], nv = sm.goff[gi + 1] - e0;
+      const float gs0 = sm.gs[gi][0], gs1 = sm.gs[gi][1];
+      float hm[2] = {0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int jloc = 2 * t4 + (q & 1);
+        const int r = tb * 16 + g8 + 8 * (q >> 1);
+        if (jloc < nv) {
+          const int tok = shared ? jloc : sm.ent_tok[e0 + jloc];
+          const float inv = sm.xinv[tok];
+          const float hv = has_blob ? silu_f32(v[q] * inv * gs0) * (v[4 + q] * inv * gs1) : 0.f;
+          const int hrow = shared ? a.maxTk + jloc : e0 + jloc;
+          a.h[size_t(hrow) * a.Imax + r] = hv;
+          hm[q & 1] = fmaxf(hm[q & 1], fabsf(hv));
+        }
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        hm[0] = fmaxf(hm[0], __shfl_xor_sync(0xffffffffu, hm[0], o));
+        hm[1] = fmaxf(hm[1], __shfl_xor_sync(0xffffffffu, hm[1], o));
+      }
+      if (g8 == 0)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int jloc = 2 * t4 + q;
+          if (jloc < nv)
+            atomicMax(reinterpret_cast<unsigned int*>(a.hmax) + (shared ? a.maxTk + jloc : e0 + jloc),
+                      __float_as_uint(hm[q]));
+        }
+    }
+    __syncthreads();
+  }
+  if (!grid_barrier(a, sm)) return;
+
+  // ============================================================ D: down
+  // Tasks in group order; per group of the CTA's range, its (at most 8) h rows are
+  // staged as f16 times the power of two of each row's max|h| (11 significant bits),
+  // the (task, 256-column chunk) units run as in C, and each task's chunks are summed
+  // in order into o (fp32, by output position t*k + r; the shared expert's rows after).
+  const int NCD = I / kChunk;
+  for (int tk0 = d0; tk0 < d1;) {
+    const int gi = tk0 / NRB;
+    const int tk1 = min(min(d1, (gi + 1) * NRB), tk0 + kMaxUnits / NCD);
+    const bool shared = gi == G;
+    const int e0 = shared ? n : sm.goff[gi];
+    const int nv = shared ? T : sm.goff[gi + 1] - e0;
+    const bool has_blob = sm.gblob[gi] != nullptr;
+    const int ud = (tk1 - tk0) * NCD;
+    auto load = [&](int u, UnitRegs<1>& R) {
+      if (u >= ud || !has_blob) return;
+      const int tl = u / NCD, ch = u - tl * NCD, rb = tk0 + tl - gi * NRB;
+      load_unit<1>(sm.gblob[gi], a.lay, 2, I, rb * 16 + g8, ch, t4, R);
+    };
+    // the first units' weights are requested before the h rows: both round trips overlap
+    UnitRegs<1> ra, rb, rc;  // three units in flight per warp (a unit is half a gate/up unit)
+    int u = warp;
+    load(u, ra);
+    load(u + kWarps, rb);
+    load(u + 2 * kWarps, rc);
+    if (has_blob) {
+      const int per = I / 4;
+      for (int j = tid; j < nv; j += kThreads) sm.hs_inv[j] = __ldcg(a.hmax + (shared ? a.maxTk + j : e0 + j));
+      __syncthreads();
+      constexpr int kB = 8;
+      for (int i0 = 0; i0 < nv * per; i0 += kB * kThreads) {
+        float4 f[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const int i = i0 + tid + j * kThreads;
+          if (i < nv * per) {
+            const int R = i / per, q4 = i - R * per;
+            const int srow = shared ? a.maxTk + R : e0 + R;
+            f[j] = __ldcg(reinterpret_cast<const float4*>(a.h + size_t(srow) * a.Imax) + q4);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const int i = i0 + tid + j * kThreads;
+          if (i < nv * per) {
+            const int R = i / per, q4 = i - R * per;
+            const float sc = pow2_scale_for(sm.hs_inv[R]);
+            __half2 p0 = __floats2half2_rn(f[j].x * sc, f[j].y * sc), p1 = __floats2half2_rn(f[j].z * sc, f[j].w * sc);
+            uint2 w2;
+            w2.x = *reinterpret_cast<uint32_t*>(&p0);
+            w2.y = *reinterpret_cast<uint32_t*>(&p1);
+            *reinterpret_cast<uint2*>(h16 + size_t(R) * HR + perm_col(4 * q4)) = w2;
+          }
+        }
+      }
+      __syncthreads();
+      for (int j = tid; j < nv; j += kThreads) sm.hs_inv[j] = 1.0f / pow2_scale_for(sm.hs_inv[j]);
+    }
+    auto run = [&](int u, const UnitRegs<1>& R) {
+      if (u >= ud) return;
+      const int tl = u / NCD, ch = u - tl * NCD;
+      float acc[1][2][4];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[0][q >> 2][q & 3] = 0.f;
+      if (has_blob) mma_unit<1>(R, g8 < nv ? h16 + size_t(g8) * HR : nullptr, ch, t4, acc);
+      reinterpret_cast<float4*>(red + (size_t(tl * NCD + ch) * 32 + lane) * 4)[0] =
+          make_float4(acc[0][0][0] + acc[0][1][0], acc[0][0][1] + acc[0][1][1], acc[0][0][2] + acc[0][1][2],
+                      acc[0][0][3] + acc[0][1][3]);
+    };
+    __syncthreads();  // the staged rows are complete
+    for (; u < ud; u += 3 * kWarps) {
+      run(u, ra);
+      load(u + 3 * kWarps, ra);
+      run(u + kWarps, rb);
+      load(u + 4 * kWarps, rb);
+      run(u + 2 * kWarps, rc);
+      load(u + 5 * kWarps, rc);
+    }
+    __syncthreads();
+    const float gsd = sm.gs[gi][2];
+    for (int idx = tid; idx < (tk1 - tk0) * 32; idx += kThreads) {
+      const int tl = idx >> 5, rbk = tk0 + tl - gi * NRB;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int c = 0; c < NCD; ++c) {
+        const float4 pp = reinterpret_cast<const float4*>(red + (size_t(tl * NCD + c) * 32 + lane) * 4)[0];
+        v[0] += pp.x; v[1] += pp.y; v[2] += pp.z; v[3] += pp.w;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int jloc = 2 * t4 + (q & 1);
+        if (jloc < nv) {
+          const int pos = shared ? a.maxTk + jloc : sm.ent_pos[e0 + jloc];
+          a.o[size_t(pos) * H + rbk * 16 + g8 + 8 * (q >> 1)] = has_blob ? v[q] * sm.hs_inv[jloc] * gsd : 0.f;
+        }
+      }
+    }
+    __syncthreads();
+    tk0 = tk1;
+  }
+  if (!grid_barrier(a, sm)) return;
+
+  // ============================================================ combine
+  // y[t] = sum_r w[t,r] o[t*k + r] + sigmoid(gl_t) o[shared t], rank order, the shared
+  // term last; CTA c owns a contiguous range of the T x H/4 four-column items.
+  const int NI = T * (H / 4);
+  const int i0 = int((long long)cta * NI / ncta), i1 = int((long long)(cta + 1) * NI / ncta);
+  for (int i = i0 + tid; i < i1; i += kThreads) {
+    const int t = i / (H / 4), c4 = i - t * (H / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int nrow = k + a.has_shared;
+    for (int r0 = 0; r0 < nrow; r0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = r0 + j;
+        if (r < nrow) {
+          const size_t row = r < k ? size_t(t * k + r) : size_t(a.maxTk + t);
+          v[j] = __ldcg(reinterpret_cast<const float4*>(a.o + row * H) + c4);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = r0 + j;
+        if (r < nrow) {
+          const float cf = r < k ? sm.w[t * k + r] : sigmoid_f32(sm.gl[t]);
+          acc.x = fmaf(cf, v[j].x, acc.x);
+          acc.y = fmaf(cf, v[j].y, acc.y);
+          acc.z = fmaf(cf, v[j].z, acc.z);
+          acc.w = fmaf(cf, v[j].w, acc.w);
+        }
+      }
+    }
+    if (a.y_fp32) {
+      reinterpret_cast<float4*>(a.y)[i] = acc;
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(a.y)[i] = pk;
+    }
+  }
+}
+
+}  // namespace dec
+
+// ----------------------------------------------------------------- host
+namespace {
+
+int sm_count_dec() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+int align128(int v) { return (v + 127) & ~127; }
+
+}  // namespace
+
+// Shared-memory layout of one launch; false when the shapes do not fit the kernel.
+static bool decode_fused_layout(const moe_layer_shape& sh, int T, int Gw, dec::Args& a, size_t& smem) {
+  using namespace dec;
+  int off = 0;
+  a.o_x16 = off;
+  off += align128(T * (sh.H + kPadH) * 2);
+  const int ab = off;
+  // phases A and B: x (bf16), the logits, top-k candidates, router partial sums
+  a.o_xs = ab;
+  a.o_lg = a.o_xs + align128(T * sh.H * 2);
+  a.o_cand = a.o_lg + align128(T * sh.E * 4);
+  a.o_part = a.o_cand + align128(T * Gw * sh.k * 8);
+  const int end_ab = a.o_part + align128(kMaxPairs * kMaxT * 4);
+  // phases C and D: partial tiles (gate/up: 8 floats per lane and unit; down: 4), then one
+  // group's h rows as f16
+  a.o_red = ab;
+  a.o_h16 = a.o_red + kMaxUnits * 32 * 8 * 4;
+  const int end_cd = a.o_h16 + align128(kMaxT * (sh.I + kPadH) * 2);
+  a.o_small = align128(end_ab > end_cd ? end_ab : end_cd);
+  smem = size_t(a.o_small) + sizeof(Small);
+  return smem <= 227 * 1024;
+}
+
+// The fused decode forward when the shapes allow it, else kNotFused.
+int launch_decode_fused(const moe_layer_desc* d, moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
+                        moe_ws* ws, cudaStream_t s) {
+  using namespace dec;
+  const moe_layer_shape& sh = d->s;
+  const bool has_shared = sh.I_shared > 0 && d->shared_blob;
+  if (T < 1 || T > kMaxT || T * sh.k > kMaxEnt || sh.E > 1024) return kNotFused;
+  if (!pow2(sh.H) || sh.H < kSlice || sh.H > 2048 || !pow2(sh.I) || sh.I < kChunk || sh.I > 1024) return kNotFused;
+  if (has_shared && sh.I_shared != sh.I) return kNotFused;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 15) ||
+      (reinterpret_cast<uintptr_t>(d->w_router) & 15) ||
+      (has_shared && ((reinterpret_cast<uintptr_t>(d->shared_blob) & 31) ||
+                      (reinterpret_cast<uintptr_t>(d->w_shared_gate) & 15))))
+    return kNotFused;
+  const int ncta = sm_count_dec();
+  const int rows_total = sh.E + (has_shared && d->w_shared_gate ? 1 : 0);
+  if ((rows_total + ncta - 1) / ncta * (sh.H / kSlice) > kMaxPairs) return kNotFused;
+  // warps per token of the top-k: a power of two with T * Gw <= 16 and Gw * k <= 128
+  int Tp = 1;
+  while (Tp < T) Tp <<= 1;
+  int Gw = kWarps / Tp;
+  while (Gw > 1 && Gw * sh.k > 128) Gw >>= 1;
+  if ((sh.E + Gw - 1) / Gw > 32 * kTopkKP1) return kNotFused;
+  Args a = {};
+  size_t smem = 0;
+  if (!decode_fused_layout(sh, T, Gw, a, smem)) return kNotFused;
+  const bool small_slices = (sh.E + Gw - 1) / Gw <= 128;
+  auto kern = small_slices ? k_decode_fused<4> : k_decode_fused<kTopkKP1>;
+  static bool attr[2] = {false, false};
+  if (!attr[small_slices]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+      return MOE_ECUDA;
+    attr[small_slices] = true;
+  }
+  a.x = x;
+  a.w_router = d->w_router;
+  a.bias = d->bias;
+  a.w_sg = has_shared ? d->w_shared_gate : nullptr;
+  a.shared_blob = has_shared ? static_cast<const uint8_t*>(d->shared_blob) : nullptr;
+  a.T = T;
+  a.H = sh.H;
+  a.I = sh.I;
+  a.E = sh.E;
+  a.k = sh.k;
+  a.layer = d->layer;
+  a.has_shared = has_shared ? 1 : 0;
+  a.Gw = Gw;
+  a.lay = dev_layout(sh.H, sh.I);
+  a.resid = c->resid;
+  a.stage = c->stage;
+  a.slots = c->slots;
+  a.staging = c->staging;
+  a.blob_bytes = c->blob_bytes;
+  a.shared_bytes = has_shared ? blob_layout(sh.H, sh.I_shared).bytes : 0;
+  a.nslots = c->nslots;
+  a.nstaging = c->nstaging;
+  a.tail_skip = ws->tail_skip;
+  a.stats = c->stats;
+  a.heat_row = ws->fused_heat ? c->heat + size_t(d->layer) * sh.E : nullptr;
+  a.logits = ws->logits;
+  a.gate_logit = ws->gate_logit;
+  a.topk_ids = ws->topk_ids;
+  a.topk_w = ws->topk_w;
+  a.num_groups = ws->num_groups;
+  a.grp_expert = ws->grp_expert;
+  a.grp_off = ws->grp_off;
+  a.grp_slot = ws->grp_slot;
+  a.grp_src = ws->grp_src;
+  a.grp_blob = ws->grp_blob;
+  a.ent_tok = ws->ent_tok;
+  a.ent_pos = ws->ent_pos;
+  a.h = ws->h;
+  a.hmax = ws->hmax;
+  a.o = ws->o;
+  a.Imax = ws->s.I > ws->s.I_shared ? ws->s.I : ws->s.I_shared;
+  a.maxTk = ws->maxT * ws->s.k;
+  a.y = y;
+  a.y_fp32 = y_is_fp32;
+  a.err = ws->error;
+  a.bar = ws->bar;
+  a.bar_extra = ws->bar_extra;
+  a.wait_ns = ws->wait_ns;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ncta);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeCooperative;
+  attrs[0].val.cooperative = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ECUDA;
+  }
+  return MOE_OK;
+}
+
+}  // namespace moe

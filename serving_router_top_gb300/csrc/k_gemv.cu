@@ -23,7 +23,7 @@
 // meet, and each (task, row block) is then summed in warp order by one warp,
 // which writes its rows -- no split crosses CTAs and the results do not depend
 // on scheduling.
-#include "internal.h"
+#include "dequant.cuh"
 
 namespace moe {
 namespace gemv {
@@ -34,59 +34,6 @@ constexpr int kXPadH = 8;          // f16 elements after each activation row
 constexpr int kDownGroups = 4;     // down: groups whose h rows a CTA keeps in shared memory
 constexpr int kMaxRound = 16;      // tasks per round at most
 constexpr size_t kSmemBudget = 226 * 1024;  // leaves room for static shared variables
-
-__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-__device__ __forceinline__ void cp16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(su32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(su32(dst)), "l"(src) : "memory");
-}
-// 16 bytes, read-only, not kept in L1 (every weight byte is read once)
-__device__ __forceinline__ uint4 ld_stream16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-// 32 bytes (256-bit load): a lane's 64 codes of one row, so four lanes cover a 128-byte line
-__device__ __forceinline__ void ld_stream32(const void* p, uint32_t (&r)[8]) {
-  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "l"(p));
-}
-// An L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned address.
-__device__ __forceinline__ void prefetch_bulk_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ void e2m1_pair2(uint32_t two_bytes, uint32_t& lo, uint32_t& hi) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(two_bytes));
-}
-__device__ __forceinline__ uint32_t scale_pair(uint32_t byte) { return e4m3x2_to_f16x2(byte | (byte << 8)); }
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-
-
 
 // Geometry shared by host and device (the logged quantities are powers of two).
 struct Geo {

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "lib", "libmoe.so")
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_EMISSING, MOE_ERANGE, MOE_ENAN, MOE_ETIMEOUT = range(8)
 MOE_SRC_MISSING, MOE_SRC_RESIDENT, MOE_SRC_STAGED, MOE_SRC_SKIPPED = -1, 0, 1, 2
 MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL = 0, 1, 2
+MOE_DECODE_FUSED, MOE_DECODE_CHAIN = 0, 1
 
 # Every symbol include/moe.h declares.
 EXPORTED = (
@@ -27,7 +28,8 @@ EXPORTED = (
     "moe_sync_status", "moe_strerror", "moe_route", "moe_group", "moe_layer_forward", "cache_heat_update",
     "cache_plan_swaps", "moe_cache_apply_swaps", "moe_ws_set_profiling", "moe_ws_kernel_times",
     "cache_plan_swaps_noalloc", "moe_residual_rmsnorm", "moe_layer_forward_streamed", "moe_ws_set_tail_skip",
-    "moe_ws_set_fused_heat", "cache_lru_plan", "moe_cache_apply_lru",
+    "moe_ws_set_fused_heat", "cache_lru_plan", "moe_cache_apply_lru", "moe_ws_set_decode_path",
+    "moe_ws_set_wait_test",
 )
 
 
@@ -108,6 +110,8 @@ def load() -> C.CDLL:
         "moe_ws_set_profiling": (I, [P, I]),
         "moe_ws_set_tail_skip": (I, [P, I]),
         "moe_ws_set_fused_heat": (I, [P, I]),
+        "moe_ws_set_decode_path": (I, [P, I]),
+        "moe_ws_set_wait_test": (I, [P, C.c_ulonglong, I]),
         "cache_lru_plan": (I, [P, P, I, I, P, P, P]),
         "moe_cache_apply_lru": (I, [P, P, P, P, P]),
         "moe_ws_kernel_times": (I, [P, I, P, P, C.POINTER(C.c_int)]),
@@ -285,6 +289,14 @@ class Workspace:
     def set_fused_heat(self, enable: bool) -> None:
         """Let the grouping of later calls with a cache also add the window's counts to the layer's heat."""
         _check(load().moe_ws_set_fused_heat(self.handle, 1 if enable else 0), "moe_ws_set_fused_heat")
+
+    def set_decode_path(self, path: int) -> None:
+        """MOE_DECODE_FUSED (one cooperative kernel where the shapes fit) or MOE_DECODE_CHAIN."""
+        _check(load().moe_ws_set_decode_path(self.handle, int(path)), "moe_ws_set_decode_path")
+
+    def set_wait_test(self, wait_ns: int, phantom_arrivals: int) -> None:
+        """Bound of the decode kernel's grid-barrier waits, and arrivals they wait for that never come."""
+        _check(load().moe_ws_set_wait_test(self.handle, int(wait_ns), int(phantom_arrivals)), "moe_ws_set_wait_test")
 
     def set_profiling(self, enable: bool) -> None:
         _check(load().moe_ws_set_profiling(self.handle, 1 if enable else 0), "moe_ws_set_profiling")
