@@ -322,6 +322,27 @@ int moe_layer_forward_streamed(const moe_layer_desc* d, const uint16_t* x, void*
                                moe_cache* c, moe_ws* ws, int U, int buffers, moe_stream_t stream,
                                moe_stream_t copy_stream);
 
+/* Activation rows as sums of NVFP4 terms, the B operands of the block-scaled
+ * FP4 prefill GEMMs.  The format is the weights' (PLE offload page, "NVFP4 code
+ * 和 scale 如何反量化": value = E2M1 code x FP8-E4M3 scale per 16 values x FP32
+ * global scale); the pages give its decoding, and this quantiser is its plain
+ * reading, applied R times to the remaining residual: term r of row i is
+ * q = Q(v - q_1 - ... - q_{r-1}), Q with
+ *   G: the smallest power of two with max|row| / (6 G) <= 448;
+ *   s: per 16 values, the smallest non-negative E4M3 value with 6 s G >= max|block|;
+ *   code: the E2M1 value nearest to v / (s G) (correctly rounded quotient), ties to even.
+ *   src     rows x K activations, row i at src + i * ld elements: bf16 (src_is_fp32 = 0)
+ *           or fp32; 16-byte aligned, ld a multiple of 8;
+ *   codes   uint8 [rows * R][K / 2] out: term r of row i at row i * R + r, low nibble =
+ *           even column; 8-byte aligned;
+ *   scales  uint8 [rows * R][K / 16] out: the E4M3 block scales (sign bit clear);
+ *   gscale  fp32 [rows * R] out: the global scales.
+ * K a power of two in [64, 4096], 1 <= R <= 8, else MOE_EINVAL.  The residual is
+ * kept in fp32: exact for bf16 rows, within one rounding per term for fp32 rows.
+ * Asynchronous on `stream`. */
+int moe_nvfp4_split(const void* src, int src_is_fp32, int rows, int K, int ld, int R, uint8_t* codes,
+                    uint8_t* scales, float* gscale, moe_stream_t stream);
+
 /* Heat update (Strata page, "哪些专家能长期留在显存？": accumulate how often
  * each expert is routed to): heat[layer*E+e] = fl32(heat + (float)count_e)
  * with count_e the number of (token, rank) selections of e in topk_ids

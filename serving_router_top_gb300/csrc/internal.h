@@ -28,6 +28,11 @@ int launch_gemv_decode(bool gateup, const moe_layer_desc* d, int T, moe_ws* ws, 
 int launch_decode_fused(const moe_layer_desc* d, moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
                         moe_ws* ws, cudaStream_t s);
 
+// Activation rows -> R NVFP4 terms (codes [rows*R][K/2], scales [rows*R][K/16], global
+// scales [rows*R]); rows bf16 (src_is_fp32 = 0) or fp32, ld elements apart.
+int launch_split_nvfp4(const void* src, int src_is_fp32, int rows, int K, int ld, int R, uint8_t* codes,
+                       uint8_t* scales, float* gscale, cudaStream_t s);
+
 // Prefill path (tcgen05 GEMMs): router logits and gate logit, then the
 // experts, which write y directly.  x rows must be 16-byte aligned.
 bool prefill_supported(const moe_layer_shape& s);

@@ -29,7 +29,7 @@ EXPORTED = (
     "cache_plan_swaps", "moe_cache_apply_swaps", "moe_ws_set_profiling", "moe_ws_kernel_times",
     "cache_plan_swaps_noalloc", "moe_residual_rmsnorm", "moe_layer_forward_streamed", "moe_ws_set_tail_skip",
     "moe_ws_set_fused_heat", "cache_lru_plan", "moe_cache_apply_lru", "moe_ws_set_decode_path",
-    "moe_ws_set_wait_test",
+    "moe_ws_set_wait_test", "moe_nvfp4_split",
 )
 
 
@@ -112,6 +112,7 @@ def load() -> C.CDLL:
         "moe_ws_set_fused_heat": (I, [P, I]),
         "moe_ws_set_decode_path": (I, [P, I]),
         "moe_ws_set_wait_test": (I, [P, C.c_ulonglong, I]),
+        "moe_nvfp4_split": (I, [P, I, I, I, I, I, P, P, P, P]),
         "cache_lru_plan": (I, [P, P, I, I, P, P, P]),
         "moe_cache_apply_lru": (I, [P, P, P, P, P]),
         "moe_ws_kernel_times": (I, [P, I, P, P, C.POINTER(C.c_int)]),
@@ -347,6 +348,13 @@ def moe_layer_forward_streamed(desc: moe_layer_desc, x, y, y_is_fp32: bool, T: i
     _check(load().moe_layer_forward_streamed(C.byref(desc), _ptr(x), _ptr(y), 1 if y_is_fp32 else 0, T, cache.handle,
                                              ws.handle, U, buffers, _stream(stream), _stream(copy_stream)),
            "moe_layer_forward_streamed")
+
+
+def moe_nvfp4_split(src, src_is_fp32: bool, rows: int, K: int, ld: int, R: int, codes, scales, gscale,
+                    stream=None) -> None:
+    """Rows of activations -> R NVFP4 terms each (codes, block scales, global scales)."""
+    _check(load().moe_nvfp4_split(_ptr(src), 1 if src_is_fp32 else 0, rows, K, ld, R, _ptr(codes), _ptr(scales),
+                                  _ptr(gscale), _stream(stream)), "moe_nvfp4_split")
 
 
 def cache_heat_update(cache: Cache, topk_ids, T: int, k: int, layer: int, err=None, stream=None) -> None:
