@@ -71,6 +71,10 @@ def parse():
     p.add_argument("--large", action="store_true",
                    help="also time the 4096-hidden, 256-expert top-6 model: its 4096-token prefill chunk and "
                         "batch-64 decode")
+    p.add_argument("--no-stack", action="store_true", help="skip the 48-layer decode stack schedule")
+    p.add_argument("--no-mixed", action="store_true",
+                   help="skip the 8-layer prefill-then-decode run of the 4096-hidden model")
+    p.add_argument("--stack-steps", type=int, default=2048)
     return p.parse_args()
 
 
@@ -505,6 +509,78 @@ def measure_large(peaks, layers: int = 2, T_decode: int = 64, steps: int = 200):
     return out
 
 
+def measure_stack(Ts=(1, 2, 4, 8, 16), steps: int = 2048, layers: int = 48):
+    """The 48-layer decode stack as specified: every step a fresh window of T tokens through
+    48 layers (residual + RMSNorm between them, the heat update inside each layer's grouping),
+    a planning round with its swaps every 256 steps, the router biases re-drawn every 512
+    steps; 30% of the 48 x 512 experts resident in cache slots, every expert also staged.
+    One graph of a whole step, replayed; the batch sizes run one after another on one cache."""
+    import torch
+    from serving_router_top_gb300 import inputs as I, moe
+    from serving_router_top_gb300.stack import DecodeStack, run_schedule
+    w = I.WORKLOADS["stack48_decode_h2048_e512_k10"]
+    t0 = time.perf_counter()
+    stk = DecodeStack(w, layers=layers, maxT=max(Ts), plan_every=256, drift_every=512)
+    build_s = time.perf_counter() - t0
+    st = stk.st
+    stream = torch.cuda.Stream()
+    blob = moe.moe_blob_bytes(st.H, st.I)
+    fixed = st.E * st.H * 2 + blob  # router rows and the shared expert, every layer call
+    out = {"workload": w.name, "layers": layers, "steps": steps, "slots": st.cache.view.nslots,
+           "plan_every": 256, "drift_every": 512, "by_batch": {}}
+    for T in Ts:
+        windows = torch.from_numpy(np.stack([I.activations(w.seed, 50_000 + T * 100 + i, T, st.H)
+                                             for i in range(16)]).view(np.int16)).cuda()
+        win32 = (windows.view(torch.int16).to(torch.int32) << 16).view(torch.float32).contiguous()
+        stats0 = st.cache.stats()
+        ms, swaps, _, _ = run_schedule(stk, T, steps, win32, stream)
+        groups = int((st.cache.stats() - stats0)[:, 0].sum())
+        nbytes = groups * blob + steps * layers * fixed
+        out["by_batch"][str(T)] = {"tokens_per_s": T * steps / (ms / 1e3), "ms": ms,
+                                   "us_per_layer_step": 1e3 * ms / (steps * layers),
+                                   "weight_GBps": nbytes / (ms / 1e3) / 1e9, "swaps_applied": swaps,
+                                   "mean_groups_per_layer_call": groups / (steps * layers)}
+    rc = moe.moe_sync_status(st.ws)
+    if rc != moe.MOE_OK:
+        raise RuntimeError(f"device error in the stack run: {moe.strerror(rc)}")
+    out["build_s"] = build_s
+    out["timing"] = ("CUDA events around each batch size's whole schedule (graph replays, the planning rounds "
+                     "and drift between them); weight_GBps counts every distinct expert a layer call reads, "
+                     "its router rows and the shared expert")
+    del stk, st
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_mixed(layers: int = 8, Tp: int = 4096, Td: int = 64, steps: int = 256):
+    """The 4096-hidden, 256-expert top-6 model, all 8 layers resident: a 4096-token prefill
+    chunk through the 8 layers, then 256 decode steps of 64 tokens (one graph per step)."""
+    import torch
+    from serving_router_top_gb300 import inputs as I, moe
+    from serving_router_top_gb300.stack import DecodeStack, run_prefill_then_decode
+    w = I.WORKLOADS["large_h4096_e256_k6"]
+    t0 = time.perf_counter()
+    stk = DecodeStack(w, layers=layers, maxT=Tp, plan_every=0, drift_every=0, stage_all=False)
+    build_s = time.perf_counter() - t0
+    st = stk.st
+    stream = torch.cuda.Stream()
+    to32 = lambda b: (torch.from_numpy(b.view(np.int16)).cuda().to(torch.int32) << 16).view(torch.float32)
+    prompt = to32(I.activations(w.seed, 60_000, Tp, st.H))
+    wins = torch.stack([to32(I.activations(w.seed, 61_000 + i, Td, st.H)) for i in range(8)])
+    pre_ms, dec_ms, _, _ = run_prefill_then_decode(stk, prompt, wins, steps, stream)
+    rc = moe.moe_sync_status(st.ws)
+    if rc != moe.MOE_OK:
+        raise RuntimeError(f"device error in the mixed run: {moe.strerror(rc)}")
+    out = {"workload": w.name, "layers": layers, "prefill_tokens": Tp, "decode_batch": Td, "decode_steps": steps,
+           "prefill_ms": pre_ms, "prefill_tokens_per_s": Tp / (pre_ms / 1e3),
+           "decode_ms": dec_ms, "decode_tokens_per_s": Td * steps / (dec_ms / 1e3),
+           "decode_us_per_layer_step": 1e3 * dec_ms / (steps * layers), "build_s": build_s,
+           "timing": "CUDA events: the prefill chunk through every layer, then the decode steps (graph replays)"}
+    del stk, st
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_prefill_streamed(w, xs, on_device: bool, U: int = 64, n: int = 8, buffers: int = 2):
     """The same chunk with every expert of the layer streamed from the backing pool (HBM, or
     pinned host memory over the host link) through the staging pool in units of U experts:
@@ -714,6 +790,10 @@ def run_ours(args, w):
         out["prefill"] = measure_prefill(args, peaks)
     if args.large:
         out["large"] = measure_large(peaks)
+    if not args.no_stack:
+        out["stack"] = measure_stack(steps=args.stack_steps)
+    if not args.no_mixed:
+        out["mixed"] = measure_mixed()
     if not args.no_cpu_baseline:
         v, tok, calls, el = oracle_sample(w, args.cpu_seconds)
         out["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
