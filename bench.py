@@ -451,6 +451,7 @@ def measure_prefill(args, peaks):
     torch.cuda.empty_cache()
     out["streamed"] = {f"{src}_{nb}buf": measure_prefill_streamed(w, xs, on_device, buffers=nb)
                        for src, on_device in (("device", True), ("pinned_host", False)) for nb in (2, 1)}
+    out["layers_streamed"] = measure_layers_streamed()
     return out
 
 
@@ -578,6 +579,74 @@ def measure_mixed(layers: int = 8, Tp: int = 4096, Td: int = 64, steps: int = 25
            "timing": "CUDA events: the prefill chunk through every layer, then the decode steps (graph replays)"}
     del stk, st
     torch.cuda.empty_cache()
+    return out
+
+
+def measure_layers_streamed(layers: int = 4, n: int = 5):
+    """Layers of the 8192-token prefill chunk with each layer's 512 experts streamed whole
+    into one half of the staging pool one layer ahead (two buffers) or into one buffer (each
+    copy waits for the previous layer), from pinned host memory and from HBM."""
+    import torch
+    from serving_router_top_gb300 import inputs as I, moe
+    from serving_router_top_gb300.model import ModelState
+    w = I.WORKLOADS["prefill_t8192_h2048_e512_k10"]
+    s, T = w.shape, w.T
+    out = {"workload": w.name, "layers": layers}
+    for on_device in (False, True):
+        st = ModelState(w, layers=layers, resident=np.zeros((layers, s.E), dtype=bool), stage_rest=False, nslots=1,
+                        nstaging=2 * s.E, backing_on_device=on_device)
+        x0 = (torch.from_numpy(I.activations(w.seed, 70_000, T, s.H).view(np.int16)).cuda().to(torch.int32)
+              << 16).view(torch.float32)
+        xn = torch.zeros((T, s.H), dtype=torch.int16, device="cuda")
+        y = torch.zeros((T, s.H), dtype=torch.int16, device="cuda")
+        stream, copy = torch.cuda.Stream(), torch.cuda.Stream()
+        descs = [st.layers[l].desc for l in range(layers)]
+        # one layer's blobs copied alone (after a first, page-mapping copy), and beside a bf16
+        # GEMM loop on the compute stream: what the copy engine delivers with and without
+        # busy SMs
+        nb = s.E * moe.moe_blob_bytes(s.H, s.I)
+        stag = moe.device_view(st.cache.view.staging, (nb,), "uint8", st.cache)
+        src = st.backing[:nb]
+        A = torch.randn(4096, 4096, dtype=torch.bfloat16, device="cuda")
+        for beside in (False, False, True):
+            with torch.cuda.stream(copy):
+                c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                c0.record(copy)
+                stag.copy_(src, non_blocking=True)
+                c1.record(copy)
+            if beside:
+                with torch.cuda.stream(stream):
+                    for _ in range(40):
+                        A @ A
+            torch.cuda.synchronize()
+            key = f"{'device' if on_device else 'pinned_host'}_copy_{'beside_gemm' if beside else 'alone'}_GBps"
+            out[key] = nb / (c0.elapsed_time(c1) / 1e3) / 1e9
+        del A
+        for buffers in (2, 1):
+            with torch.cuda.stream(stream):
+                x = x0.clone()
+                moe.moe_layers_forward_streamed(descs, x, xn, y, T, st.cache, st.ws, buffers=buffers, stream=stream,
+                                                copy_stream=copy)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(n):
+                    x.copy_(x0)
+                    moe.moe_layers_forward_streamed(descs, x, xn, y, T, st.cache, st.ws, buffers=buffers,
+                                                    stream=stream, copy_stream=copy)
+                e1.record(stream)
+                torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / (n * layers)
+            out[f"{'device' if on_device else 'pinned_host'}_{buffers}buf"] = {
+                "ms_per_layer": ms, "tokens_per_s": T / (ms / 1e3),
+                "weight_GBps": s.E * moe.moe_blob_bytes(s.H, s.I) / (ms / 1e3) / 1e9}
+        rc = moe.moe_sync_status(st.ws)
+        if rc != moe.MOE_OK:
+            raise RuntimeError(f"device error in the layer-streamed prefill: {moe.strerror(rc)}")
+        del st
+        torch.cuda.empty_cache()
+    out["timing"] = (f"{n} calls of {layers} layers back to back, events on the compute stream; per layer: "
+                     "residual + RMSNorm, router, top-k, groups, the expert GEMMs on the layer's staged half")
     return out
 
 

@@ -343,6 +343,30 @@ int moe_layer_forward_streamed(const moe_layer_desc* d, const uint16_t* x, void*
 int moe_nvfp4_split(const void* src, int src_is_fp32, int rows, int K, int ld, int R, uint8_t* codes,
                     uint8_t* scales, float* gscale, moe_stream_t stream);
 
+/* Several MoE layers of a prefill chunk, each layer's experts streamed whole
+ * through the staging pool one layer ahead (FreeToken notes, section 3.1: layer
+ * l + 1's experts copy into the second buffer while layer l computes with the
+ * first; section 5.3: with the second buffer off, each copy waits until the
+ * previous layer is done).  The layers sit on an fp32 residual stream as in
+ * moe_residual_rmsnorm: for l = 0 .. L-1, x_res += y (l > 0), xn = bf16(RMSNorm
+ * (x_res)), y = MoE_l(xn) in prefill mode; finally x_res += y.
+ *   d       moe_layer_desc [L] (host), the same H, E and k, each with its layer;
+ *   x_res   fp32 [T, H] device, the residual stream, updated in place (16-byte aligned);
+ *   xn, y   bf16 [T, H] device scratch (16-byte aligned); on return xn holds the
+ *           normalised final stream, y the last layer's output.
+ * Layer l uses staging slots h * E .. h * E + E - 1 with h = l % buffers: the copy
+ * stream waits on `used` of the layer that last read half h, copies the layer's E
+ * blobs from the cache's backing pool (device or pinned host) in one
+ * cudaMemcpyAsync and records `copied`; the compute stream waits on `copied` before
+ * the layer's expert GEMMs and records `used` after them.  The residency and
+ * staging tables are not consulted or changed.  buffers 1 or 2, buffers * E <= the
+ * cache's staging slots, a backing pool, eps > 0, copy_stream distinct from
+ * stream, and every layer valid for moe_layer_forward in prefill mode, else
+ * MOE_EINVAL.  Both streams may be reused as soon as the call returns. */
+int moe_layers_forward_streamed(const moe_layer_desc* d, int L, float* x_res, uint16_t* xn, uint16_t* y, int T,
+                                moe_cache* c, moe_ws* ws, int buffers, float eps, moe_stream_t stream,
+                                moe_stream_t copy_stream);
+
 /* Heat update (Strata page, "哪些专家能长期留在显存？": accumulate how often
  * each expert is routed to): heat[layer*E+e] = fl32(heat + (float)count_e)
  * with count_e the number of (token, rank) selections of e in topk_ids

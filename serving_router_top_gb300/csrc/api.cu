@@ -489,6 +489,26 @@ int moe_layer_forward_streamed(const moe_layer_desc* d, const uint16_t* x, void*
                                  reinterpret_cast<cudaStream_t>(copy_stream));
 }
 
+int moe_layers_forward_streamed(const moe_layer_desc* d, int L, float* x_res, uint16_t* xn, uint16_t* y, int T,
+                                moe_cache* c, moe_ws* ws, int buffers, float eps, moe_stream_t stream,
+                                moe_stream_t copy_stream) {
+  if (!d || L < 1 || !x_res || !xn || !y || (buffers != 1 && buffers != 2) || !(eps > 0.f) || !c || !c->backing ||
+      !copy_stream || copy_stream == stream)
+    return MOE_EINVAL;
+  int rc;
+  for (int l = 0; l < L; ++l) {
+    if ((rc = forward_args_ok(&d[l], xn, y, T, c, ws, true))) return rc;
+    if (d[l].s.H != d[0].s.H || d[l].s.E != d[0].s.E || d[l].s.k != d[0].s.k) return MOE_EINVAL;
+  }
+  if (size_t(buffers) * d[0].s.E > size_t(c->nstaging) || (reinterpret_cast<uintptr_t>(x_res) & 15) ||
+      d[0].s.H % 4 || d[0].s.H > 4096)
+    return MOE_EINVAL;
+  if (T == 0) return MOE_OK;
+  ws->prof_n = 0;
+  return launch_prefill_layers_streamed(d, L, x_res, xn, y, T, c, ws, buffers, eps, reinterpret_cast<cudaStream_t>(stream),
+                                        reinterpret_cast<cudaStream_t>(copy_stream));
+}
+
 int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T, moe_cache* c,
                       moe_ws* ws, int mode, moe_stream_t stream) {
   if (!d || !x || !y || !c || !ws || !d->w_router) return MOE_EINVAL;

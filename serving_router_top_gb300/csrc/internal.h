@@ -41,6 +41,9 @@ int launch_prefill_experts(const moe_layer_desc* d, const moe_cache* c, const ui
                            moe_ws* ws, cudaStream_t s);
 int launch_prefill_streamed(const moe_layer_desc* d, moe_cache* c, const uint16_t* x, void* y, int y_is_fp32, int T,
                             int U, int buffers, moe_ws* ws, cudaStream_t s, cudaStream_t cs);
+int launch_prefill_layers_streamed(const moe_layer_desc* d, int L, float* x_res, uint16_t* xn, uint16_t* y, int T,
+                                   moe_cache* c, moe_ws* ws, int buffers, float eps, cudaStream_t s,
+                                   cudaStream_t cs);
 
 // Policy.
 int launch_heat_update(moe_cache* c, const int32_t* ids, int T, int k, int layer, int32_t* err, cudaStream_t s);

@@ -1344,4 +1344,49 @@ int launch_prefill_streamed(const moe_layer_desc* d, moe_cache* c, const uint16_
   return prefill_end(d, y, y_is_fp32, T, ws, s);
 }
 
+// Several layers of a prefill chunk with each layer's experts streamed whole into
+// one half of the staging pool (FreeToken notes, section 3.1: while layer l computes
+// with the experts of one buffer, layer l + 1's are copied into the other; section
+// 5.3: with the second buffer off, each copy waits for the previous layer).  Per
+// layer l, half h = l % buffers: the copy stream waits until the layer that last
+// used half h is done (`used`), copies layer l's E blobs from the backing pool in
+// one cudaMemcpyAsync and records `copied`; the compute stream adds the previous
+// layer's output to the residual stream and normalises it, waits on `copied`,
+// runs the layer's prefill with every group bound to staging slot h * E + expert,
+// and records `used`.  A final residual add closes the stack.
+int launch_prefill_layers_streamed(const moe_layer_desc* d, int L, float* x_res, uint16_t* xn, uint16_t* y, int T,
+                                   moe_cache* c, moe_ws* ws, int buffers, float eps, cudaStream_t s,
+                                   cudaStream_t cs) {
+  using namespace prefill;
+  const moe_layer_shape& sh = d[0].s;
+  const size_t layer_bytes = size_t(sh.E) * c->blob_bytes;
+  int rc;
+  MOE_CUDA_TRY(cudaEventRecord(c->ev_ring[4], s));
+  MOE_CUDA_TRY(cudaStreamWaitEvent(cs, c->ev_ring[4], 0));
+  for (int l = 0; l < L; ++l) {
+    const int half = l % buffers;
+    cudaEvent_t copied = c->ev_ring[half], used = c->ev_ring[2 + half];
+    if (l >= buffers) MOE_CUDA_TRY(cudaStreamWaitEvent(cs, used, 0));
+    const uint8_t* pool = static_cast<const uint8_t*>(c->backing) + size_t(d[l].layer) * layer_bytes;
+    MOE_CUDA_TRY(cudaMemcpyAsync(c->staging + size_t(half) * layer_bytes, pool, layer_bytes, cudaMemcpyDefault, cs));
+    MOE_CUDA_TRY(cudaEventRecord(copied, cs));
+    if ((rc = moe_residual_rmsnorm(x_res, l > 0 ? y : nullptr, xn, T, sh.H, eps, reinterpret_cast<moe_stream_t>(s))))
+      return rc;
+    if ((rc = launch_prefill_router(&d[l], xn, T, ws, s))) return rc;
+    if ((rc = launch_topk(ws->logits, T, sh.E, sh.k, ws->topk_ids, ws->topk_w, ws->error, s))) return rc;
+    if ((rc = launch_group(ws->topk_ids, T, sh.k, sh.E, d[l].layer, c, ws, s, false))) return rc;
+    prefill::Args a = base_args(&d[l], T, ws);
+    if ((rc = prefill_begin(a, &d[l], xn, y, 0, T, ws, s))) return rc;
+    MOE_CUDA_TRY(cudaStreamWaitEvent(s, copied, 0));
+    if (launch_pdl(k_unit_bind, dim3(1), dim3(256), 0, s, 0, sh.E, half * sh.E, ws->num_groups, ws->grp_expert,
+                   ws->grp_src, ws->grp_slot, ws->grp_blob, static_cast<const uint8_t*>(c->staging), c->blob_bytes,
+                   ws->grange) != cudaSuccess)
+      return MOE_ECUDA;
+    if ((rc = prefill_groups(a, &d[l], c, T, ws, ws->grange, 1, false, s))) return rc;
+    MOE_CUDA_TRY(cudaEventRecord(used, s));
+    if ((rc = prefill_end(&d[l], y, 0, T, ws, s))) return rc;
+  }
+  return moe_residual_rmsnorm(x_res, y, xn, T, sh.H, eps, reinterpret_cast<moe_stream_t>(s));
+}
+
 }  // namespace moe

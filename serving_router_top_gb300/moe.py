@@ -29,7 +29,7 @@ EXPORTED = (
     "cache_plan_swaps", "moe_cache_apply_swaps", "moe_ws_set_profiling", "moe_ws_kernel_times",
     "cache_plan_swaps_noalloc", "moe_residual_rmsnorm", "moe_layer_forward_streamed", "moe_ws_set_tail_skip",
     "moe_ws_set_fused_heat", "cache_lru_plan", "moe_cache_apply_lru", "moe_ws_set_decode_path",
-    "moe_ws_set_wait_test", "moe_nvfp4_split",
+    "moe_ws_set_wait_test", "moe_nvfp4_split", "moe_layers_forward_streamed",
 )
 
 
@@ -113,6 +113,7 @@ def load() -> C.CDLL:
         "moe_ws_set_decode_path": (I, [P, I]),
         "moe_ws_set_wait_test": (I, [P, C.c_ulonglong, I]),
         "moe_nvfp4_split": (I, [P, I, I, I, I, I, P, P, P, P]),
+        "moe_layers_forward_streamed": (I, [P, I, P, P, P, I, P, P, I, F, P, P]),
         "cache_lru_plan": (I, [P, P, I, I, P, P, P]),
         "moe_cache_apply_lru": (I, [P, P, P, P, P]),
         "moe_ws_kernel_times": (I, [P, I, P, P, C.POINTER(C.c_int)]),
@@ -348,6 +349,15 @@ def moe_layer_forward_streamed(desc: moe_layer_desc, x, y, y_is_fp32: bool, T: i
     _check(load().moe_layer_forward_streamed(C.byref(desc), _ptr(x), _ptr(y), 1 if y_is_fp32 else 0, T, cache.handle,
                                              ws.handle, U, buffers, _stream(stream), _stream(copy_stream)),
            "moe_layer_forward_streamed")
+
+
+def moe_layers_forward_streamed(descs, x_res, xn, y, T: int, cache: Cache, ws: Workspace, buffers: int = 2,
+                                eps: float = 1e-6, stream=None, copy_stream=None) -> None:
+    """Layers of a prefill chunk on a residual stream, each layer's experts streamed one layer ahead."""
+    arr = (moe_layer_desc * len(descs))(*descs)
+    _check(load().moe_layers_forward_streamed(arr, len(descs), _ptr(x_res), _ptr(xn), _ptr(y), T, cache.handle,
+                                              ws.handle, buffers, eps, _stream(stream), _stream(copy_stream)),
+           "moe_layers_forward_streamed")
 
 
 def moe_nvfp4_split(src, src_is_fp32: bool, rows: int, K: int, ld: int, R: int, codes, scales, gscale,

@@ -220,3 +220,60 @@ def test_prefill_streamed_rejects_bad_units():
             st.forward_streamed(0, x, y, 64, 2, buffers=bad_buffers)
     with pytest.raises(moe.MoeError):  # one buffer of 5 does not fit four slots either
         st.forward_streamed(0, x, y, 64, 5, buffers=1)
+
+
+def _stack_ref_gpu(st, x_res0, T, L):
+    """The same layers through moe_layer_forward in prefill mode, experts from the cache's
+    slots; every layer's input rows, logits and output are kept for teacher-forced checks."""
+    x_res = x_res0.clone()
+    xn = torch.zeros((T, st.H), dtype=torch.int16, device="cuda")
+    y = torch.zeros((T, st.H), dtype=torch.int16, device="cuda")
+    prev, seen = None, []
+    for l in range(L):
+        moe.moe_residual_rmsnorm(x_res, prev, xn, T, st.H)
+        st.forward(l, xn, y, T, y_is_fp32=False, mode=moe.MOE_MODE_PREFILL)
+        torch.cuda.synchronize()
+        seen.append(dict(xn=xn.cpu().numpy().view(np.uint16).copy(), y=y.cpu().numpy().view(np.uint16).copy(),
+                         logits=st.ws.routing(T)[0].cpu().numpy().copy()))
+        prev = y
+    moe.moe_residual_rmsnorm(x_res, prev, xn, T, st.H)
+    torch.cuda.synchronize()
+    return x_res, seen
+
+
+@pytest.mark.parametrize("backing_on_device", [True, False])
+def test_layers_streamed_double_buffer(backing_on_device):
+    """Three layers of a prefill chunk with each layer's experts streamed into one half of the
+    staging pool one layer ahead (two buffers), and with the second buffer off (each copy
+    waits for the previous layer), against the same layers run one call each from resident
+    slots -- whose every layer is held against the oracle on that layer's own input rows and
+    logits.  The two runs may route a token differently where a layer's bf16 input differs in
+    its last bit at a near-tie (the fp32 atomic adds of the prefill combine vary in order), so
+    all but at most 2% of the token rows must agree within the layer tolerance."""
+    from oracle import formats
+    from serving_router_top_gb300.model import ModelState
+    L, T = 3, 300
+    w = I.small_workload(T=T, H=256, I=128, E=16, k=2, I_shared=128, zipf_s=0.0, resident_frac=1.0, seed=31,
+                         layers=L)
+    st = ModelState(w, nstaging=32, backing_on_device=backing_on_device, stage_rest=False)
+    x0 = torch.from_numpy(formats.bf16_value(I.activations(w.seed, 5, T, st.H)).astype(np.float32)).cuda()
+    ref, seen = _stack_ref_gpu(st, x0, T, L)
+    for l, d in enumerate(seen):
+        li = st.layers[l].host
+        o = olayer.moe_layer(d["xn"], li.w_router, li.bias, st.k, lambda e, l=l: st.expert_host(l, e), st.H, st.I,
+                             layer=l, shared=li.shared, I_shared=st.I_shared, w_shared_gate_bits=li.w_shared_gate,
+                             logits=d["logits"])
+        U.assert_close_layer(formats.bf16_value(d["y"]), o.y, bf16_out=True, what=f"layer {l}")
+    copy = torch.cuda.Stream()
+    r = ref.cpu().numpy().astype(np.float64)
+    tol = U.TOL_REL * np.sqrt(np.mean(r * r)) + U.TOL_ABS
+    for buffers in (2, 1):
+        x_res = x0.clone()
+        xn = torch.zeros((T, st.H), dtype=torch.int16, device="cuda")
+        y = torch.zeros((T, st.H), dtype=torch.int16, device="cuda")
+        moe.moe_layers_forward_streamed([st.layers[l].desc for l in range(L)], x_res, xn, y, T, st.cache, st.ws,
+                                        buffers=buffers, copy_stream=copy)
+        torch.cuda.synchronize()
+        assert moe.moe_sync_status(st.ws) == moe.MOE_OK
+        rows_ok = (np.abs(x_res.cpu().numpy() - r) <= tol).all(axis=1)
+        assert rows_ok.mean() >= 0.98, (buffers, int((~rows_ok).sum()))
