@@ -10,7 +10,7 @@
 // A decode window of a few tokens touches tens of experts but moves only a few
 // tens of megabytes, so a chain of dependent launches spends more time between
 // and inside the prologues of its kernels than streaming weights.  Here one CTA
-// per SM runs every step, the CTAs meeting at two grid barriers:
+// per SM runs every step, the CTAs meeting at three grid barriers:
 //
 //   A  router logits and the shared-gate logit: CTA c owns rows c, c + ncta, ...
 //      (row E is the gate vector), each row cut into 512-element slices, one
@@ -18,27 +18,33 @@
 //      prefetches its slice of the shared expert's blob into L2 and stages x,
 //      then x as f16 times a per-token power of two (exact for bf16 values).
 //   -- grid barrier --
-//   B  every CTA reads all T x E logits and runs the same top-k and the same
+//   B  every CTA reads all T x E logits and runs the same top-k (a threshold
+//      from the 32-expert chunk maxima, then ranks by counting) and the same
 //      grouping on them, so every CTA holds the same groups without another
 //      barrier; CTA 0 writes them, with the top-k, lookups, statistics and the
-//      heat update, to the workspace.  Each CTA then issues bulk L2 prefetches
-//      of every weight byte it will read in C and D: the step's expert bytes
-//      stream from HBM at once instead of behind each consumer's own loads.
+//      heat update, to the workspace.
 //   C  gate/up: tasks are (group, 16-row block of I), CTA c owns a contiguous
 //      range of them, and the (task, 256-column chunk) units go round-robin to
-//      the 16 warps; mma.sync m16n8k16 f16 -> f32 with the weights dequantised
-//      exactly into f16 (E2M1 code x E4M3 scale) as A and up to 8 of the
-//      group's token rows as B; partial tiles are summed in chunk order and the
-//      epilogue writes h = SiLU(gs_g g) * gs_u u (fp32) and max|h| per row.
+//      the 16 warps, two units in flight per warp in registers (the first two
+//      requested right after grouping); mma.sync m16n8k16 f16 -> f32 with the
+//      weights dequantised exactly into f16 (E2M1 code x E4M3 scale) as A and up
+//      to 8 of the group's token rows as B; partial tiles are summed in chunk
+//      order and the epilogue writes h = SiLU(gs_g g) * gs_u u (fp32) and max|h|
+//      per row.  One lane meanwhile issues bulk L2 prefetches of the CTA's later
+//      gate/up weights and of all its down weights.
 //   -- grid barrier --
-//   D  down and combine: CTA c owns 16-row blocks c, c + ncta, ... of the
-//      output.  It reads every entry's h row (f16 times a per-row power of two,
-//      exact to 11 bits), runs the (group, 256-column chunk) units of its row
-//      block and then, per token, y = sum_r w[t,r] o[t,r] + sigmoid(gl_t) s_t
-//      in rank order with the shared term last -- deterministic, no atomics.
+//   D  down: tasks are (group, 16-row block of H), CTA c owns a contiguous
+//      range; the h rows of its groups are staged once as f16 times a per-row
+//      power of two (exact to 11 bits), the units run as in C (three in flight
+//      per warp, from L2), each task's chunks summed in order into o (by output
+//      position).
+//   -- grid barrier --
+//   combine: y = sum_r w[t,r] o[t,r] + sigmoid(gl_t) s_t in rank order with the
+//      shared term last, each CTA a slice of the T x H outputs -- deterministic,
+//      no atomics.
 //
-// Every wait is bounded (the grid barriers give up after the workspace's wait
-// limit, record MOE_ETIMEOUT and the CTAs skip the remaining phases).
+// Every wait is bounded: the grid barriers give up after the workspace's wait limit,
+// record MOE_ETIMEOUT, and the CTAs skip the remaining phases.
 #include "dequant.cuh"
 #include "topk.cuh"
 
@@ -51,11 +57,11 @@ constexpr int kChunk = 256;        // columns per unit: a lane's 64 columns, one
 constexpr int kMaxT = 8;           // tokens (the MMA's N)
 constexpr int kMaxEnt = 256;       // T * k
 constexpr int kMaxGroups = kMaxEnt + 1;
-constexpr int kMaxUnits = 64;      // gate/up partial tiles held per round
 constexpr int kSlice = 512;        // router row elements per warp pair
 constexpr int kMaxPairs = 2 * kWarps;
-constexpr int kTopkKP1 = 16;       // logits per lane of a top-k slice at most (E / warps-per-token <= 512)
 constexpr int kPadH = 32;          // f16 elements after each activation row: a row stride of 64 mod 128 bytes
+constexpr int kMaxUnits = 64;      // gate/up partial tiles held per round (8 floats per lane)
+constexpr int kMaxUnitsD = 128;    // down partial tiles held per round (4 floats per lane)
 
 struct Args {
   const uint16_t* x;         // bf16 [T, H]
@@ -63,7 +69,7 @@ struct Args {
   const float* bias;         // [E] or null
   const uint16_t* w_sg;      // bf16 [H] or null
   const uint8_t* shared_blob;
-  int T, H, I, E, k, layer, has_shared, Gw;
+  int T, H, I, E, k, layer, has_shared;
   DevBlobLayout lay;
   // the cache
   const int32_t* resid;
@@ -97,8 +103,10 @@ struct Args {
   unsigned long long* bar;   // grid-barrier arrivals (a multiple of the grid between launches)
   unsigned bar_extra;        // arrivals a barrier waits for beyond the grid (0; a test hook)
   unsigned long long wait_ns;
-  // shared-memory carve (byte offsets)
-  int o_x16, o_xs, o_lg, o_cand, o_part, o_red, o_h16, o_small;
+  // shared-memory carve (byte offsets); capc: top-k candidates per token; hrows: h rows
+  // the down phase stages at once
+  int o_x16, o_xs, o_lg, o_cb, o_cand, o_sel, o_pr, o_part, o_red, o_h16, o_small;
+  int capc, hrows;
 };
 
 // Small tables, at the end of shared memory.
@@ -107,21 +115,20 @@ struct Small {
   float w[kMaxEnt];
   uint32_t key[kMaxEnt];
   uint32_t srt[kMaxEnt];
-  int32_t start[kMaxEnt];
   int32_t ent_tok[kMaxEnt];
   int32_t ent_pos[kMaxEnt];
-  int32_t inv[kMaxEnt];
+  unsigned long long tau[kMaxT];  // top-k thresholds and candidate counts per token
+  int32_t ncand[kMaxT];
   int32_t gexp[kMaxGroups];
   int32_t goff[kMaxGroups + 1];
-  int32_t gsrc[kMaxGroups];
   const uint8_t* gblob[kMaxGroups];
-  float gs[kMaxGroups][3];
   float xinv[kMaxT];
   float gl[kMaxT];
   float hs_inv[kMaxEnt + kMaxT];
   int32_t resid[1024];  // the layer's residency and staging rows
   int32_t stage[1024];
-  int G, ok, cnt[4];
+  __align__(16) float gs[kMaxGroups][4];  // each group's global scales (gate, up, down) and a pad
+  int ok, cnt[4];
 };
 
 __device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
@@ -206,6 +213,27 @@ __device__ __forceinline__ void load_unit(const uint8_t* blob, const DevBlobLayo
   }
 }
 
+// The same unit from a copy of 16 weight rows in shared memory: matrix m's code rows at
+// base + m * mstride (K / 2 bytes each), its scale rows at base + soff + m * K (K / 16 each).
+template <int NM>
+__device__ __forceinline__ void load_unit_smem(const uint8_t* base, int mstride, int soff, int K, int row, int ch,
+                                               int t4, UnitRegs<NM>& R) {
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+    const uint8_t* cp = base + m * mstride + row * (K / 2) + ch * 128 + 32 * t4;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint4 lo = *reinterpret_cast<const uint4*>(cp + r * 8 * (K / 2));
+      const uint4 hi = *reinterpret_cast<const uint4*>(cp + r * 8 * (K / 2) + 16);
+      R.c[m][r][0] = lo.x; R.c[m][r][1] = lo.y; R.c[m][r][2] = lo.z; R.c[m][r][3] = lo.w;
+      R.c[m][r][4] = hi.x; R.c[m][r][5] = hi.y; R.c[m][r][6] = hi.z; R.c[m][r][7] = hi.w;
+    }
+    const uint8_t* sp = base + soff + m * K + row * (K / 16) + ch * 16 + 4 * t4;
+    R.s[m][0] = *reinterpret_cast<const uint32_t*>(sp);
+    R.s[m][1] = *reinterpret_cast<const uint32_t*>(sp + 8 * (K / 16));
+  }
+}
+
 // acc[m][even/odd MMA] += dq(W rows) . B for the lane's 64 columns of chunk ch.
 // brow: the lane's B row (activations, f16, perm_col layout), or null (zeros).
 template <int NM>
@@ -232,17 +260,125 @@ __device__ __forceinline__ void mma_unit(const UnitRegs<NM>& R, const __half* br
   }
 }
 
-// KP1: logits per lane of a warp's top-k slice (4 when the slice fits 128 logits, else 16).
-template <int KP1>
+// An entry's place in the top-k order: the order-preserving key of its logit above, the
+// complement of its id below -- a larger value is a better entry, equal logits going to the
+// lower id (the order of the top-k kernel).
+__device__ __forceinline__ unsigned long long rank_key(float x, int e) {
+  return (static_cast<unsigned long long>(ordered_key(x)) << 32) | (0xffffffffu - unsigned(e));
+}
+
+// Top-k of the T tokens by the whole CTA from the logits in shared memory (lg [T, E]):
+//   1. the best entry of each 32-expert chunk of a token (two warp reductions);
+//   2. tau_t, the k-th best of the token's chunk bests (0 when it has fewer than k
+//      chunks): k entries reach tau_t, so each of the token's k best does too;
+//   3. the entries that reach tau_t -- those of the k chunks whose best does, at most
+//      min(E, 32 k), usually a few more than k -- are compacted, and each takes as its rank
+//      the number of candidates above it; rank r < k is the token's selection r.
+// No step is a chain of warp-wide selections, which a decode step cannot afford.  Ids
+// and weights equal the top-k kernel's: the same order, and w_r = p_r / sum_j p_j with
+// p_r = exp(l_r - l_0) summed in rank order.  NaN logits rank as -inf and record
+// MOE_ENAN.  Leaves key[i] = id << 16 | i for the grouping.  Every thread of the CTA calls
+// this; it holds four __syncthreads and ends without one.
+__device__ void topk_ranked(const float* __restrict__ lg, int T, int E, int k, Small& sm, int32_t* err,
+                            unsigned long long* __restrict__ cbest, unsigned long long* __restrict__ cand, int capc,
+                            unsigned long long* __restrict__ sel, float* __restrict__ pr) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NCH = (E + 31) >> 5;
+  bool nan_seen = false;
+  for (int it = warp; it < T * NCH; it += kWarps) {
+    const int t = it / NCH, e = (it - t * NCH) * 32 + lane;
+    unsigned long long ck = 0ull;
+    if (e < E) {
+      float x = lg[t * E + e];
+      if (x != x) {
+        nan_seen = true;
+        x = -INFINITY;
+      }
+      ck = rank_key(x, e);
+    }
+    const unsigned hi = __reduce_max_sync(0xffffffffu, unsigned(ck >> 32));
+    const unsigned lo = __reduce_max_sync(0xffffffffu, unsigned(ck >> 32) == hi ? unsigned(ck) : 0u);
+    if (lane == 0) cbest[it] = (static_cast<unsigned long long>(hi) << 32) | lo;
+  }
+  if (nan_seen) set_error(err, MOE_ENAN);
+  if (tid < T) sm.ncand[tid] = 0;
+  __syncthreads();
+  if (warp < T) {
+    const unsigned long long* cb = cbest + warp * NCH;
+    const unsigned long long mine = lane < NCH ? cb[lane] : 0ull;
+    int r = 0;
+    for (int c = 0; c < NCH; ++c) r += cb[c] > mine ? 1 : 0;
+    if (NCH < k) {
+      if (lane == 0) sm.tau[warp] = 0ull;
+    } else if (lane < NCH && r == k - 1) {
+      sm.tau[warp] = mine;
+    }
+  }
+  __syncthreads();
+  for (int it = warp; it < T * NCH; it += kWarps) {
+    const int t = it / NCH, e = (it - t * NCH) * 32 + lane;
+    unsigned long long ck = 0ull;
+    if (e < E) {
+      float x = lg[t * E + e];
+      if (x != x) x = -INFINITY;
+      ck = rank_key(x, e);
+    }
+    const bool take = e < E && ck >= sm.tau[t];
+    const unsigned b = __ballot_sync(0xffffffffu, take);
+    int base = 0;
+    if (lane == 0 && b) base = atomicAdd(&sm.ncand[t], __popc(b));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int pos = base + __popc(b & ((1u << lane) - 1u));
+    if (take) {
+      if (pos < capc) cand[t * capc + pos] = ck;
+      else set_error(err, MOE_ERANGE);  // unreachable: at most min(E, 32 k) entries reach tau
+    }
+  }
+  __syncthreads();
+  {
+    const int S = kThreads / T, t = tid / S;
+    if (t < T) {
+      const int C = min(sm.ncand[t], capc);
+      const unsigned long long* cc = cand + t * capc;
+      for (int i = tid - t * S; i < C; i += S) {
+        const unsigned long long me = cc[i];
+        int r = 0;
+#pragma unroll 4
+        for (int j = 0; j < C; ++j) r += cc[j] > me ? 1 : 0;
+        if (r < k) sel[t * k + r] = me;
+      }
+    }
+  }
+  __syncthreads();
+  const int n = T * k;
+  for (int i = tid; i < n; i += kThreads) {
+    const int t = i / k;
+    const unsigned long long s = sel[i];
+    sm.ids[i] = int(0xffffffffu - unsigned(s));
+    pr[i] = expf(float_of_key(unsigned(s >> 32)) - float_of_key(unsigned(sel[t * k] >> 32)));
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += kThreads) {
+    const float* p = pr + (i / k) * k;
+    float den = 0.f;
+    for (int r = 0; r < k; ++r) den += p[r];
+    sm.w[i] = pr[i] / den;
+    sm.key[i] = (uint32_t(sm.ids[i]) << 16) | uint32_t(i);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __half* x16 = reinterpret_cast<__half*>(smem + a.o_x16);
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + a.o_xs);
   float* lg = reinterpret_cast<float*>(smem + a.o_lg);
+  unsigned long long* cbest = reinterpret_cast<unsigned long long*>(smem + a.o_cb);
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem + a.o_cand);
+  unsigned long long* sel = reinterpret_cast<unsigned long long*>(smem + a.o_sel);
+  float* pr = reinterpret_cast<float*>(smem + a.o_pr);
   float* part = reinterpret_cast<float*>(smem + a.o_part);
-  float* red = reinterpret_cast<float*>(smem + a.o_red);
   __half* h16 = reinterpret_cast<__half*>(smem + a.o_h16);
+  float* red = reinterpret_cast<float*>(smem + a.o_red);
   Small& sm = *reinterpret_cast<Small*>(smem + a.o_small);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, t4 = lane & 3;
@@ -254,7 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
   int32_t* err = lead ? a.err : nullptr;
 
   // ================================================================ A: router
-  if (tid == 0) sm.ok = 1;
+  if (tid == 0) {
+    sm.ok = 1;
+    sm.cnt[0] = sm.cnt[1] = sm.cnt[2] = sm.cnt[3] = 0;
+  }
   // this CTA's slice of the shared expert's blob into L2 (its gate/up tasks run in C)
   if (a.has_shared && tid == 0) {
     const size_t slice = ((a.shared_bytes + ncta - 1) / ncta + 15) & ~size_t(15);
@@ -406,59 +545,55 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
   if (!grid_barrier(a, sm)) return;
 
   // ============================================================ B: top-k, groups
-  for (int i0 = 0; i0 < T * E; i0 += 8 * kThreads) {
-    float v[8];
+  {
+    float glv = 0.f;
+    if (tid < T && a.has_shared) glv = __ldcg(a.gate_logit + tid);  // in the same round trip
+    for (int i0 = 0; i0 < T * E; i0 += 8 * kThreads) {
+      float v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = i0 + tid + j * kThreads;
-      if (i < T * E) v[j] = __ldcg(a.logits + i);
+      for (int j = 0; j < 8; ++j) {
+        const int i = i0 + tid + j * kThreads;
+        if (i < T * E) v[j] = __ldcg(a.logits + i);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = i0 + tid + j * kThreads;
+        if (i < T * E) lg[i] = v[j];
+      }
     }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = i0 + tid + j * kThreads;
-      if (i < T * E) lg[i] = v[j];
+    if (tid < T) {
+      sm.gl[tid] = glv;
+      sm.xinv[tid] = 1.0f / sm.xinv[tid];
     }
   }
-  if (tid < T) sm.gl[tid] = a.has_shared ? __ldcg(a.gate_logit + tid) : 0.f;
-  if (tid < T) sm.xinv[tid] = 1.0f / sm.xinv[tid];
   __syncthreads();
-  topk_tokens_cta<KP1>(lg, T, E, k, a.Gw, sm.ids, sm.w, err, cand);
+  topk_ranked(lg, T, E, k, sm, err, cbest, cand, a.capc, sel, pr);
   __syncthreads();
-  // groups: sort the n selections by (expert, position); position t*k + r orders like the token
-  for (int i = tid; i < n; i += kThreads) sm.key[i] = (uint32_t(sm.ids[i]) << 16) | uint32_t(i);
-  __syncthreads();
-  for (int i = tid; i < n; i += kThreads) {
-    const uint32_t kk = sm.key[i];
+  // groups: the n selections sorted by (expert, position); position t*k + r orders like the
+  // token.  n <= 256 < the CTA's threads: one entry per thread.
+  int my_start = 0;
+  if (tid < n) {
+    const uint32_t kk = sm.key[tid];
     int r = 0;
+#pragma unroll 4
     for (int j = 0; j < n; ++j) r += sm.key[j] < kk ? 1 : 0;
     sm.srt[r] = kk;
   }
   __syncthreads();
-  for (int i = tid; i < n; i += kThreads) {
-    const uint32_t kk = sm.srt[i];
+  if (tid < n) {
+    const uint32_t kk = sm.srt[tid];
     const int pos = int(kk & 0xffffu);
-    sm.start[i] = (i == 0 || (sm.srt[i - 1] >> 16) != (kk >> 16)) ? 1 : 0;
-    sm.ent_pos[i] = pos;
-    sm.ent_tok[i] = pos / k;
-    sm.inv[pos] = i;
-  }
-  __syncthreads();
-  for (int i = tid; i < n; i += kThreads) {
-    if (sm.start[i]) {
-      int g = 0;
-      for (int j = 0; j < i; ++j) g += sm.start[j];
-      sm.gexp[g] = int(sm.srt[i] >> 16);
-      sm.goff[g] = i;
+    sm.ent_pos[tid] = pos;
+    sm.ent_tok[tid] = pos / k;
+    if (tid == 0 || (sm.srt[tid - 1] >> 16) != (kk >> 16)) {
+      my_start = 1;
+      int g = 0;  // distinct experts before this entry
+      for (int j = 1; j <= tid; ++j) g += (sm.srt[j - 1] >> 16) != (sm.srt[j] >> 16) ? 1 : 0;
+      sm.gexp[g] = int(kk >> 16);
+      sm.goff[g] = tid;
     }
   }
-  if (tid == 0) {
-    int g = 0;
-    for (int j = 0; j < n; ++j) g += sm.start[j];
-    sm.G = g;
-    sm.cnt[0] = sm.cnt[1] = sm.cnt[2] = sm.cnt[3] = 0;
-  }
-  __syncthreads();
-  const int G = sm.G;
+  const int G = __syncthreads_count(my_start);
   const int Gt = G + a.has_shared;
   if (tid == 0) sm.goff[G] = n;
   // lookup of each routed group (the same tables in every CTA: the same result)
@@ -486,7 +621,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
       else if (st >= a.nstaging) set_error(err, MOE_ERANGE);
       if (src == MOE_SRC_MISSING) { slot = -1; set_error(err, MOE_EMISSING); }
     }
-    sm.gsrc[g] = src;
     sm.gblob[g] = blob;
     if (lead) {
       a.grp_expert[g] = e;
@@ -500,7 +634,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
   }
   if (a.has_shared && tid == 0) {
     sm.gblob[G] = a.shared_blob;
-    sm.gsrc[G] = MOE_SRC_RESIDENT;
     sm.goff[G + 1] = n + T;  // the shared expert's entries are the T tokens, after the routed ones
   }
   __syncthreads();
@@ -518,98 +651,96 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     }
   }
   // Work of phases C and D: gate/up tasks (group, 16-row block of I) and down tasks
-  // (group, 16-row block of H), each list group-major; CTA c owns a contiguous range of
-  // each, and prefetches its weight bytes into L2 now -- one bulk prefetch per group and
-  // region, the rows of consecutive tasks of a group being contiguous.
+  // (group, 16-row block of H), each list group-major; CTA c owns a contiguous range of each.
   const int TPG = I / 16, NRB = H / 16;
   const int NT = Gt * TPG, ND = Gt * NRB;
   const int t0 = int((long long)cta * NT / ncta), t1 = int((long long)(cta + 1) * NT / ncta);
   const int d0 = int((long long)cta * ND / ncta), d1 = int((long long)(cta + 1) * ND / ncta);
-  {
-    const int gu_g0 = t0 / TPG, gu_n = t1 > t0 ? (t1 - 1) / TPG - gu_g0 + 1 : 0;
-    const int dn_g0 = d0 / NRB, dn_n = d1 > d0 ? (d1 - 1) / NRB - dn_g0 + 1 : 0;
-    for (int p = tid; p < 4 * gu_n + 2 * dn_n; p += kThreads) {
-      if (p < 4 * gu_n) {
-        const int gi = gu_g0 + p / 4, part_i = p & 3, m = part_i & 1;
-        const uint8_t* blob = sm.gblob[gi];
-        if (!blob) continue;
-        const int ta = max(t0, gi * TPG) - gi * TPG, tb = min(t1, (gi + 1) * TPG) - gi * TPG;  // [ta, tb)
-        if (part_i < 2)
-          prefetch_bulk_l2(blob + a.lay.code_off[m] + size_t(ta) * 16 * (H / 2), uint32_t((tb - ta) * 16 * (H / 2)));
-        else
-          prefetch_bulk_l2(blob + a.lay.scale_off[m] + size_t(ta) * 16 * (H / 16), uint32_t((tb - ta) * 16 * (H / 16)));
-      } else {
-        const int q = p - 4 * gu_n, gi = dn_g0 + q / 2, part_i = q & 1;
-        const uint8_t* blob = sm.gblob[gi];
-        if (!blob) continue;
-        const int ra = max(d0, gi * NRB) - gi * NRB, rbb = min(d1, (gi + 1) * NRB) - gi * NRB;
-        if (part_i == 0)
-          prefetch_bulk_l2(blob + a.lay.code_off[2] + size_t(ra) * 16 * (I / 2), uint32_t((rbb - ra) * 16 * (I / 2)));
-        else
-          prefetch_bulk_l2(blob + a.lay.scale_off[2] + size_t(ra) * 16 * (I / 16), uint32_t((rbb - ra) * 16 * (I / 16)));
-      }
-    }
-  }
-
-  // the groups' global scales (read after the prefetches are on their way; used from the
-  // first epilogue on, after the __syncthreads that ends each round of units)
-  for (int g = tid; g < Gt; g += kThreads) {
-    const BlobHeader* hd = reinterpret_cast<const BlobHeader*>(sm.gblob[g]);
-    sm.gs[g][0] = hd ? hd->gscale[0] : 0.f;
-    sm.gs[g][1] = hd ? hd->gscale[1] : 0.f;
-    sm.gs[g][2] = hd ? hd->gscale[2] : 0.f;
-  }
+  const int NCH = H / kChunk, NCD = I / kChunk;
 
   // ============================================================ C: gate/up
-  const int NCH = H / kChunk;
   const int U = (t1 - t0) * NCH;
-  for (int r0 = 0; r0 < U; r0 += kMaxUnits) {
-    const int nu = min(kMaxUnits, U - r0);
-    auto unit_at = [&](int u, int& gi, int& tb, int& ch) {
-      const int task = t0 + u / NCH;
-      ch = u - (u / NCH) * NCH;
-      gi = task / TPG;
-      tb = task - gi * TPG;
-    };
-    auto load = [&](int u, UnitRegs<2>& R) {
-      if (u >= r0 + nu) return;
-      int gi, tb, ch;
-      unit_at(u, gi, tb, ch);
+  int r0 = 0, nu = min(kMaxUnits, U);
+  auto unit_at = [&](int u, int& gi, int& tb, int& ch) {
+    const int task = t0 + u / NCH;
+    ch = u - (u / NCH) * NCH;
+    gi = task / TPG;
+    tb = task - gi * TPG;
+  };
+  auto load = [&](int u, UnitRegs<2>& R) {
+    if (u >= r0 + nu) return;
+    int gi, tb, ch;
+    unit_at(u, gi, tb, ch);
+    const uint8_t* blob = sm.gblob[gi];
+    if (blob) load_unit<2>(blob, a.lay, 0, H, tb * 16 + g8, ch, t4, R);
+  };
+  auto run = [&](int u, const UnitRegs<2>& R) {
+    if (u >= r0 + nu) return;
+    int gi, tb, ch;
+    unit_at(u, gi, tb, ch);
+    const int e0 = sm.goff[gi], nv = sm.goff[gi + 1] - e0;
+    float acc[2][2][4];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[m][q >> 2][q & 3] = 0.f;
+    if (sm.gblob[gi]) {
+      const __half* brow = nullptr;
+      if (g8 < nv) brow = x16 + size_t(gi == G ? g8 : sm.ent_tok[e0 + g8]) * XR;
+      mma_unit<2>(R, brow, ch, t4, acc);
+    }
+    float4* dst = reinterpret_cast<float4*>(red + (size_t(u - r0) * 32 + lane) * 8);
+    dst[0] = make_float4(acc[0][0][0] + acc[0][1][0], acc[0][0][1] + acc[0][1][1], acc[0][0][2] + acc[0][1][2],
+                         acc[0][0][3] + acc[0][1][3]);
+    dst[1] = make_float4(acc[1][0][0] + acc[1][1][0], acc[1][0][1] + acc[1][1][1], acc[1][0][2] + acc[1][1][2],
+                         acc[1][0][3] + acc[1][1][3]);
+  };
+  // two units in flight per warp: the first two are requested before anything else
+  UnitRegs<2> ra, rb;
+  load(warp, ra);
+  load(warp + kWarps, rb);
+  if (tid == kThreads - 32) {
+    // every weight byte of the CTA's later gate/up units and of its down tasks into L2 --
+    // one bulk prefetch per group and region, the rows of consecutive tasks of a group
+    // being contiguous -- so the step's expert bytes stream from HBM at once
+    const int ta0 = t0 + min(t1 - t0, (2 * kWarps + NCH - 1) / NCH);
+    for (int gi = ta0 / TPG; ta0 < t1 && gi <= (t1 - 1) / TPG; ++gi) {
       const uint8_t* blob = sm.gblob[gi];
-      if (blob) load_unit<2>(blob, a.lay, 0, H, tb * 16 + g8, ch, t4, R);
-    };
-    auto run = [&](int u, const UnitRegs<2>& R) {
-      if (u >= r0 + nu) return;
-      int gi, tb, ch;
-      unit_at(u, gi, tb, ch);
-      const int e0 = sm.goff[gi], nv = sm.goff[gi + 1] - e0;
-      float acc[2][2][4];
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[m][q >> 2][q & 3] = 0.f;
-      if (sm.gblob[gi]) {
-        const __half* brow = nullptr;
-        if (g8 < nv) brow = x16 + size_t(gi == G ? g8 : sm.ent_tok[e0 + g8]) * XR;
-        mma_unit<2>(R, brow, ch, t4, acc);
+      if (!blob) continue;
+      const int ta = max(ta0, gi * TPG) - gi * TPG, tb = min(t1, (gi + 1) * TPG) - gi * TPG;
+      for (int m = 0; m < 2; ++m) {
+        prefetch_bulk_l2(blob + a.lay.code_off[m] + size_t(ta) * 8 * H, uint32_t((tb - ta) * 8 * H));
+        prefetch_bulk_l2(blob + a.lay.scale_off[m] + size_t(ta) * H, uint32_t((tb - ta) * H));
       }
-      float4* dst = reinterpret_cast<float4*>(red + (size_t(u - r0) * 32 + lane) * 8);
-      dst[0] = make_float4(acc[0][0][0] + acc[0][1][0], acc[0][0][1] + acc[0][1][1], acc[0][0][2] + acc[0][1][2],
-                           acc[0][0][3] + acc[0][1][3]);
-      dst[1] = make_float4(acc[1][0][0] + acc[1][1][0], acc[1][0][1] + acc[1][1][1], acc[1][0][2] + acc[1][1][2],
-                           acc[1][0][3] + acc[1][1][3]);
-    };
-    // two units in flight per warp: the next one loads while this one computes
-    UnitRegs<2> ra, rb;
-    int u = r0 + warp;
-    load(u, ra);
-    load(u + kWarps, rb);
-    for (; u < r0 + nu; u += 2 * kWarps) {
+    }
+    for (int gi = d0 / NRB; d1 > d0 && gi <= (d1 - 1) / NRB; ++gi) {
+      const uint8_t* blob = sm.gblob[gi];
+      if (!blob) continue;
+      const int ra_ = max(d0, gi * NRB) - gi * NRB, rbb = min(d1, (gi + 1) * NRB) - gi * NRB;
+      prefetch_bulk_l2(blob + a.lay.code_off[2] + size_t(ra_) * 8 * I, uint32_t((rbb - ra_) * 8 * I));
+      prefetch_bulk_l2(blob + a.lay.scale_off[2] + size_t(ra_) * I, uint32_t((rbb - ra_) * I));
+    }
+  }
+  // the groups' global scales (the 16 header bytes at offset 16 of each blob) by
+  // asynchronous copies, waited for only before the first epilogue
+  for (int g = tid; g < Gt; g += kThreads) {
+    if (sm.gblob[g]) cp16(&sm.gs[g][0], sm.gblob[g] + 16);
+    else sm.gs[g][0] = sm.gs[g][1] = sm.gs[g][2] = 0.f;
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  for (; r0 < U; r0 += kMaxUnits) {
+    nu = min(kMaxUnits, U - r0);
+    if (r0 > 0) {
+      load(r0 + warp, ra);
+      load(r0 + warp + kWarps, rb);
+    }
+    for (int u = r0 + warp; u < r0 + nu; u += 2 * kWarps) {
       run(u, ra);
       load(u + 2 * kWarps, ra);
       run(u + kWarps, rb);
       load(u + 3 * kWarps, rb);
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     // each task's chunks summed in order; epilogue h = SiLU(gs_g g / s_x) * (gs_u u / s_x)
     const int ntk = nu / NCH;
@@ -662,103 +793,117 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
   if (!grid_barrier(a, sm)) return;
 
   // ============================================================ D: down
-  // Tasks in group order; per group of the CTA's range, its (at most 8) h rows are
-  // staged as f16 times the power of two of each row's max|h| (11 significant bits),
-  // the (task, 256-column chunk) units run as in C, and each task's chunks are summed
-  // in order into o (fp32, by output position t*k + r; the shared expert's rows after).
-  const int NCD = I / kChunk;
-  for (int tk0 = d0; tk0 < d1;) {
-    const int gi = tk0 / NRB;
-    const int tk1 = min(min(d1, (gi + 1) * NRB), tk0 + kMaxUnits / NCD);
-    const bool shared = gi == G;
-    const int e0 = shared ? n : sm.goff[gi];
-    const int nv = shared ? T : sm.goff[gi + 1] - e0;
-    const bool has_blob = sm.gblob[gi] != nullptr;
-    const int ud = (tk1 - tk0) * NCD;
-    auto load = [&](int u, UnitRegs<1>& R) {
-      if (u >= ud || !has_blob) return;
-      const int tl = u / NCD, ch = u - tl * NCD, rb = tk0 + tl - gi * NRB;
-      load_unit<1>(sm.gblob[gi], a.lay, 2, I, rb * 16 + g8, ch, t4, R);
+  // The CTA's tasks [d0, d1) in group order.  The h rows of every group of its range --
+  // entries goff[gA] .. goff[gB + 1], the shared expert's T rows counted as entries n ..
+  // n + T - 1 -- are staged in ONE batch of loads with their max|h|, as f16 times the
+  // power of two of each row's max|h| (11 significant bits); the (task, 256-column chunk)
+  // units then run as in C, their weights already in L2, and each task's chunks are
+  // summed in order into o (fp32, by output position t*k + r; the shared expert's rows
+  // after).
+  {
+    const int gA = d1 > d0 ? d0 / NRB : 0, gB = d1 > d0 ? (d1 - 1) / NRB : -1;
+    const int rbase = d1 > d0 ? sm.goff[gA] : 0, nrows = d1 > d0 ? sm.goff[gB + 1] - rbase : 0;
+    const bool fits = nrows <= a.hrows;  // always, by the launch's row bound
+    if (!fits) set_error(a.err, MOE_ERANGE);
+    const int ud = fits ? (d1 - d0) * NCD : 0;
+    auto unit_of = [&](int u, int& gi, int& rb, int& ch) {
+      const int tl = u / NCD, task = d0 + tl;
+      ch = u - tl * NCD;
+      gi = task / NRB;
+      rb = task - gi * NRB;
     };
-    // the first units' weights are requested before the h rows: both round trips overlap
-    UnitRegs<1> ra, rb, rc;  // three units in flight per warp (a unit is half a gate/up unit)
-    int u = warp;
-    load(u, ra);
-    load(u + kWarps, rb);
-    load(u + 2 * kWarps, rc);
-    if (has_blob) {
-      const int per = I / 4;
-      for (int j = tid; j < nv; j += kThreads) sm.hs_inv[j] = __ldcg(a.hmax + (shared ? a.maxTk + j : e0 + j));
-      __syncthreads();
-      constexpr int kB = 8;
-      for (int i0 = 0; i0 < nv * per; i0 += kB * kThreads) {
-        float4 f[kB];
+    for (int q0 = 0; q0 < ud; q0 += kMaxUnitsD) {
+      const int nq = min(kMaxUnitsD, ud - q0);
+      auto load_d = [&](int u, UnitRegs<1>& R) {
+        if (u >= q0 + nq) return;
+        int gi, rb, ch;
+        unit_of(u, gi, rb, ch);
+        if (sm.gblob[gi]) load_unit<1>(sm.gblob[gi], a.lay, 2, I, rb * 16 + g8, ch, t4, R);
+      };
+      // three units in flight per warp (a unit is half a gate/up unit); the first ones are
+      // requested before the h rows, so both round trips overlap
+      UnitRegs<1> da, db, dc;
+      load_d(q0 + warp, da);
+      load_d(q0 + warp + kWarps, db);
+      load_d(q0 + warp + 2 * kWarps, dc);
+      if (q0 == 0) {
+        const int per = I / 4;
+        constexpr int kB = 4;  // 16 rows of 512 in one batch
+        for (int i0 = 0; i0 < nrows * per; i0 += kB * kThreads) {
+          float4 f[kB];
+          float hmx[kB];
 #pragma unroll
-        for (int j = 0; j < kB; ++j) {
-          const int i = i0 + tid + j * kThreads;
-          if (i < nv * per) {
-            const int R = i / per, q4 = i - R * per;
-            const int srow = shared ? a.maxTk + R : e0 + R;
-            f[j] = __ldcg(reinterpret_cast<const float4*>(a.h + size_t(srow) * a.Imax) + q4);
+          for (int j = 0; j < kB; ++j) {
+            const int i = i0 + tid + j * kThreads;
+            if (i < nrows * per) {
+              const int R = i / per, q4 = i - R * per, e = rbase + R;
+              const size_t grow = e < n ? size_t(e) : size_t(a.maxTk + e - n);
+              f[j] = __ldcg(reinterpret_cast<const float4*>(a.h + grow * a.Imax) + q4);
+              hmx[j] = __ldcg(a.hmax + grow);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < kB; ++j) {
+            const int i = i0 + tid + j * kThreads;
+            if (i < nrows * per) {
+              const int R = i / per, q4 = i - R * per;
+              const float sc = pow2_scale_for(hmx[j]);
+              __half2 p0 = __floats2half2_rn(f[j].x * sc, f[j].y * sc), p1 = __floats2half2_rn(f[j].z * sc, f[j].w * sc);
+              uint2 w2;
+              w2.x = *reinterpret_cast<uint32_t*>(&p0);
+              w2.y = *reinterpret_cast<uint32_t*>(&p1);
+              *reinterpret_cast<uint2*>(h16 + size_t(R) * HR + perm_col(4 * q4)) = w2;
+              if (q4 == 0) sm.hs_inv[R] = 1.0f / sc;
+            }
           }
         }
+        __syncthreads();  // the staged rows are complete
+      }
+      auto run_d = [&](int u, const UnitRegs<1>& R) {
+        if (u >= q0 + nq) return;
+        int gi, rb, ch;
+        unit_of(u, gi, rb, ch);
+        const int nv = sm.goff[gi + 1] - sm.goff[gi];
+        float acc[1][2][4];
 #pragma unroll
-        for (int j = 0; j < kB; ++j) {
-          const int i = i0 + tid + j * kThreads;
-          if (i < nv * per) {
-            const int R = i / per, q4 = i - R * per;
-            const float sc = pow2_scale_for(sm.hs_inv[R]);
-            __half2 p0 = __floats2half2_rn(f[j].x * sc, f[j].y * sc), p1 = __floats2half2_rn(f[j].z * sc, f[j].w * sc);
-            uint2 w2;
-            w2.x = *reinterpret_cast<uint32_t*>(&p0);
-            w2.y = *reinterpret_cast<uint32_t*>(&p1);
-            *reinterpret_cast<uint2*>(h16 + size_t(R) * HR + perm_col(4 * q4)) = w2;
+        for (int x = 0; x < 8; ++x) acc[0][x >> 2][x & 3] = 0.f;
+        if (sm.gblob[gi])
+          mma_unit<1>(R, g8 < nv ? h16 + size_t(sm.goff[gi] - rbase + g8) * HR : nullptr, ch, t4, acc);
+        reinterpret_cast<float4*>(red + (size_t(u - q0) * 32 + lane) * 4)[0] =
+            make_float4(acc[0][0][0] + acc[0][1][0], acc[0][0][1] + acc[0][1][1], acc[0][0][2] + acc[0][1][2],
+                        acc[0][0][3] + acc[0][1][3]);
+      };
+      for (int u = q0 + warp; u < q0 + nq; u += 3 * kWarps) {
+        run_d(u, da);
+        load_d(u + 3 * kWarps, da);
+        run_d(u + kWarps, db);
+        load_d(u + 4 * kWarps, db);
+        run_d(u + 2 * kWarps, dc);
+        load_d(u + 5 * kWarps, dc);
+      }
+      __syncthreads();
+      for (int idx = tid; idx < (nq / NCD) * 32; idx += kThreads) {
+        const int tl = idx >> 5, task = d0 + q0 / NCD + tl, gi = task / NRB, rbk = task - gi * NRB;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int c = 0; c < NCD; ++c) {
+          const float4 pp = reinterpret_cast<const float4*>(red + (size_t(tl * NCD + c) * 32 + lane) * 4)[0];
+          v[0] += pp.x; v[1] += pp.y; v[2] += pp.z; v[3] += pp.w;
+        }
+        const bool shared = gi == G, has_blob = sm.gblob[gi] != nullptr;
+        const int e0 = sm.goff[gi], nv = sm.goff[gi + 1] - e0;
+        const float gsd = sm.gs[gi][2];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int jloc = 2 * t4 + (x & 1);
+          if (jloc < nv) {
+            const int pos = shared ? a.maxTk + jloc : sm.ent_pos[e0 + jloc];
+            a.o[size_t(pos) * H + rbk * 16 + g8 + 8 * (x >> 1)] =
+                has_blob ? v[x] * sm.hs_inv[e0 - rbase + jloc] * gsd : 0.f;
           }
         }
       }
       __syncthreads();
-      for (int j = tid; j < nv; j += kThreads) sm.hs_inv[j] = 1.0f / pow2_scale_for(sm.hs_inv[j]);
     }
-    auto run = [&](int u, const UnitRegs<1>& R) {
-      if (u >= ud) return;
-      const int tl = u / NCD, ch = u - tl * NCD;
-      float acc[1][2][4];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[0][q >> 2][q & 3] = 0.f;
-      if (has_blob) mma_unit<1>(R, g8 < nv ? h16 + size_t(g8) * HR : nullptr, ch, t4, acc);
-      reinterpret_cast<float4*>(red + (size_t(tl * NCD + ch) * 32 + lane) * 4)[0] =
-          make_float4(acc[0][0][0] + acc[0][1][0], acc[0][0][1] + acc[0][1][1], acc[0][0][2] + acc[0][1][2],
-                      acc[0][0][3] + acc[0][1][3]);
-    };
-    __syncthreads();  // the staged rows are complete
-    for (; u < ud; u += 3 * kWarps) {
-      run(u, ra);
-      load(u + 3 * kWarps, ra);
-      run(u + kWarps, rb);
-      load(u + 4 * kWarps, rb);
-      run(u + 2 * kWarps, rc);
-      load(u + 5 * kWarps, rc);
-    }
-    __syncthreads();
-    const float gsd = sm.gs[gi][2];
-    for (int idx = tid; idx < (tk1 - tk0) * 32; idx += kThreads) {
-      const int tl = idx >> 5, rbk = tk0 + tl - gi * NRB;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int c = 0; c < NCD; ++c) {
-        const float4 pp = reinterpret_cast<const float4*>(red + (size_t(tl * NCD + c) * 32 + lane) * 4)[0];
-        v[0] += pp.x; v[1] += pp.y; v[2] += pp.z; v[3] += pp.w;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int jloc = 2 * t4 + (q & 1);
-        if (jloc < nv) {
-          const int pos = shared ? a.maxTk + jloc : sm.ent_pos[e0 + jloc];
-          a.o[size_t(pos) * H + rbk * 16 + g8 + 8 * (q >> 1)] = has_blob ? v[q] * sm.hs_inv[jloc] * gsd : 0.f;
-        }
-      }
-    }
-    __syncthreads();
-    tk0 = tk1;
   }
   if (!grid_barrier(a, sm)) return;
 
@@ -771,10 +916,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     const int t = i / (H / 4), c4 = i - t * (H / 4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const int nrow = k + a.has_shared;
-    for (int r0 = 0; r0 < nrow; r0 += 8) {
-      float4 v[8];
+    for (int r0 = 0; r0 < nrow; r0 += 16) {  // one round trip for k <= 15
+      float4 v[16];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 16; ++j) {
         const int r = r0 + j;
         if (r < nrow) {
           const size_t row = r < k ? size_t(t * k + r) : size_t(a.maxTk + t);
@@ -782,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
         }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 16; ++j) {
         const int r = r0 + j;
         if (r < nrow) {
           const float cf = r < k ? sm.w[t * k + r] : sigmoid_f32(sm.gl[t]);
@@ -828,23 +973,30 @@ int align128(int v) { return (v + 127) & ~127; }
 }  // namespace
 
 // Shared-memory layout of one launch; false when the shapes do not fit the kernel.
-static bool decode_fused_layout(const moe_layer_shape& sh, int T, int Gw, dec::Args& a, size_t& smem) {
+static bool decode_fused_layout(const moe_layer_shape& sh, int T, int ncta, dec::Args& a, size_t& smem) {
   using namespace dec;
-  int off = 0;
-  a.o_x16 = off;
-  off += align128(T * (sh.H + kPadH) * 2);
-  const int ab = off;
-  // phases A and B: x (bf16), the logits, top-k candidates, router partial sums
-  a.o_xs = ab;
-  a.o_lg = a.o_xs + align128(T * sh.H * 2);
-  a.o_cand = a.o_lg + align128(T * sh.E * 4);
-  a.o_part = a.o_cand + align128(T * Gw * sh.k * 8);
-  const int end_ab = a.o_part + align128(kMaxPairs * kMaxT * 4);
-  // phases C and D: partial tiles (gate/up: 8 floats per lane and unit; down: 4), then one
-  // group's h rows as f16
-  a.o_red = ab;
+  const int H = sh.H, I = sh.I, k = sh.k, E = sh.E;
+  // x as f16 (phases A..C); the partial tiles (C: 8 floats per lane and unit, D: 4); the
+  // staged h rows (D): as many as a CTA's range of down tasks can reach -- the groups it
+  // spans times T, at most every entry's and the shared expert's
+  a.o_x16 = 0;
+  const int nrb = H / 16, tasks = ((T * k + 1) * nrb + ncta - 1) / ncta;
+  a.hrows = ((tasks + nrb - 1) / nrb + 1) * T;
+  if (a.hrows > T * k + T) a.hrows = T * k + T;
+  a.o_red = align128(T * (H + kPadH) * 2);
   a.o_h16 = a.o_red + kMaxUnits * 32 * 8 * 4;
-  const int end_cd = a.o_h16 + align128(kMaxT * (sh.I + kPadH) * 2);
+  const int end_cd = a.o_h16 + align128(a.hrows * (I + kPadH) * 2);
+  // phases A and B (over the tiles and the rows, unused until C): x (bf16), the logits,
+  // the top-k's chunk bests, candidates, selections and terms, the router partial sums
+  a.capc = E < 32 * k ? E : 32 * k;
+  a.o_xs = a.o_red;
+  a.o_lg = a.o_xs + align128(T * H * 2);
+  a.o_cb = a.o_lg + align128(T * E * 4);
+  a.o_cand = a.o_cb + align128(T * 32 * 8);
+  a.o_sel = a.o_cand + align128(T * a.capc * 8);
+  a.o_pr = a.o_sel + align128(T * k * 8);
+  a.o_part = a.o_pr + align128(T * k * 4);
+  const int end_ab = a.o_part + align128(kMaxPairs * kMaxT * 4);
   a.o_small = align128(end_ab > end_cd ? end_ab : end_cd);
   smem = size_t(a.o_small) + sizeof(Small);
   return smem <= 227 * 1024;
@@ -867,22 +1019,14 @@ int launch_decode_fused(const moe_layer_desc* d, moe_cache* c, const uint16_t* x
   const int ncta = sm_count_dec();
   const int rows_total = sh.E + (has_shared && d->w_shared_gate ? 1 : 0);
   if ((rows_total + ncta - 1) / ncta * (sh.H / kSlice) > kMaxPairs) return kNotFused;
-  // warps per token of the top-k: a power of two with T * Gw <= 16 and Gw * k <= 128
-  int Tp = 1;
-  while (Tp < T) Tp <<= 1;
-  int Gw = kWarps / Tp;
-  while (Gw > 1 && Gw * sh.k > 128) Gw >>= 1;
-  if ((sh.E + Gw - 1) / Gw > 32 * kTopkKP1) return kNotFused;
   Args a = {};
   size_t smem = 0;
-  if (!decode_fused_layout(sh, T, Gw, a, smem)) return kNotFused;
-  const bool small_slices = (sh.E + Gw - 1) / Gw <= 128;
-  auto kern = small_slices ? k_decode_fused<4> : k_decode_fused<kTopkKP1>;
-  static bool attr[2] = {false, false};
-  if (!attr[small_slices]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+  if (!decode_fused_layout(sh, T, ncta, a, smem)) return kNotFused;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(k_decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
       return MOE_ECUDA;
-    attr[small_slices] = true;
+    attr = true;
   }
   a.x = x;
   a.w_router = d->w_router;
@@ -896,7 +1040,6 @@ int launch_decode_fused(const moe_layer_desc* d, moe_cache* c, const uint16_t* x
   a.k = sh.k;
   a.layer = d->layer;
   a.has_shared = has_shared ? 1 : 0;
-  a.Gw = Gw;
   a.lay = dev_layout(sh.H, sh.I);
   a.resid = c->resid;
   a.stage = c->stage;
@@ -942,7 +1085,7 @@ int launch_decode_fused(const moe_layer_desc* d, moe_cache* c, const uint16_t* x
   attrs[0].val.cooperative = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, k_decode_fused, a) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ECUDA;
   }
