@@ -53,12 +53,15 @@ namespace dec {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
+constexpr int kGuDepth = 2;  // gate/up units in flight per warp (in registers)
+constexpr int kXVec = (8 * 2048 / 8 + kThreads - 1) / kThreads;  // 16-byte pieces of x per thread, at most
+constexpr int kEVec = (1024 + kThreads - 1) / kThreads;          // residency entries per thread, at most
 constexpr int kChunk = 256;        // columns per unit: a lane's 64 columns, one 32-byte load per row
 constexpr int kMaxT = 8;           // tokens (the MMA's N)
 constexpr int kMaxEnt = 256;       // T * k
 constexpr int kMaxGroups = kMaxEnt + 1;
 constexpr int kSlice = 512;        // router row elements per warp pair
-constexpr int kMaxPairs = 2 * kWarps;
+constexpr int kMaxPairs = 32;      // router slices per CTA at most (each warp takes every kWarps-th)
 constexpr int kPadH = 32;          // f16 elements after each activation row: a row stride of 64 mod 128 bytes
 constexpr int kMaxUnits = 64;      // gate/up partial tiles held per round (8 floats per lane)
 constexpr int kMaxUnitsD = 128;    // down partial tiles held per round (4 floats per lane)
@@ -426,26 +429,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     const uint4* src = reinterpret_cast<const uint4*>(a.x);
     uint4* dst = reinterpret_cast<uint4*>(xs);
     const int n16 = T * H / 8;
-    uint4 v[4];
+    uint4 v[kXVec];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kXVec; ++j) {
       const int i = tid + j * kThreads;
       if (i < n16) v[j] = src[i];
     }
-    int32_t rv[2], sv[2];
+    int32_t rv[kEVec], sv[kEVec];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < kEVec; ++j) {
       const int e = tid + j * kThreads;
       rv[j] = e < E ? a.resid[size_t(a.layer) * E + e] : -1;
       sv[j] = (e < E && a.stage) ? a.stage[size_t(a.layer) * E + e] : -1;
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kXVec; ++j) {
       const int i = tid + j * kThreads;
       if (i < n16) dst[i] = v[j];
     }
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < kEVec; ++j) {
       const int e = tid + j * kThreads;
       if (e < E) {
         sm.resid[e] = rv[j];
@@ -695,15 +698,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     dst[1] = make_float4(acc[1][0][0] + acc[1][1][0], acc[1][0][1] + acc[1][1][1], acc[1][0][2] + acc[1][1][2],
                          acc[1][0][3] + acc[1][1][3]);
   };
-  // two units in flight per warp: the first two are requested before anything else
-  UnitRegs<2> ra, rb;
-  load(warp, ra);
-  load(warp + kWarps, rb);
+  // kGuDepth units in flight per warp: the first ones are requested before anything else
+  UnitRegs<2> rr[kGuDepth];
+#pragma unroll
+  for (int d = 0; d < kGuDepth; ++d) load(warp + d * kWarps, rr[d]);
   if (tid == kThreads - 32) {
     // every weight byte of the CTA's later gate/up units and of its down tasks into L2 --
     // one bulk prefetch per group and region, the rows of consecutive tasks of a group
     // being contiguous -- so the step's expert bytes stream from HBM at once
-    const int ta0 = t0 + min(t1 - t0, (2 * kWarps + NCH - 1) / NCH);
+    const int ta0 = t0 + min(t1 - t0, (kGuDepth * kWarps + NCH - 1) / NCH);
     for (int gi = ta0 / TPG; ta0 < t1 && gi <= (t1 - 1) / TPG; ++gi) {
       const uint8_t* blob = sm.gblob[gi];
       if (!blob) continue;
@@ -731,14 +734,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
   for (; r0 < U; r0 += kMaxUnits) {
     nu = min(kMaxUnits, U - r0);
     if (r0 > 0) {
-      load(r0 + warp, ra);
-      load(r0 + warp + kWarps, rb);
+#pragma unroll
+      for (int d = 0; d < kGuDepth; ++d) load(r0 + warp + d * kWarps, rr[d]);
     }
-    for (int u = r0 + warp; u < r0 + nu; u += 2 * kWarps) {
-      run(u, ra);
-      load(u + 2 * kWarps, ra);
-      run(u + kWarps, rb);
-      load(u + 3 * kWarps, rb);
+    for (int u = r0 + warp; u < r0 + nu; u += kGuDepth * kWarps) {
+#pragma unroll
+      for (int d = 0; d < kGuDepth; ++d) {
+        run(u + d * kWarps, rr[d]);
+        load(u + (d + kGuDepth) * kWarps, rr[d]);
+      }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
@@ -820,12 +824,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
         unit_of(u, gi, rb, ch);
         if (sm.gblob[gi]) load_unit<1>(sm.gblob[gi], a.lay, 2, I, rb * 16 + g8, ch, t4, R);
       };
-      // three units in flight per warp (a unit is half a gate/up unit); the first ones are
-      // requested before the h rows, so both round trips overlap
+      // three units in flight per warp (a unit is half a gate/up unit), requested once the
+      // h rows are staged (their weights are in L2 by then; the rows' loads go first)
       UnitRegs<1> da, db, dc;
-      load_d(q0 + warp, da);
-      load_d(q0 + warp + kWarps, db);
-      load_d(q0 + warp + 2 * kWarps, dc);
       if (q0 == 0) {
         const int per = I / 4;
         constexpr int kB = 4;  // 16 rows of 512 in one batch
@@ -859,6 +860,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
         }
         __syncthreads();  // the staged rows are complete
       }
+      load_d(q0 + warp, da);
+      load_d(q0 + warp + kWarps, db);
+      load_d(q0 + warp + 2 * kWarps, dc);
       auto run_d = [&](int u, const UnitRegs<1>& R) {
         if (u >= q0 + nq) return;
         int gi, rb, ch;
