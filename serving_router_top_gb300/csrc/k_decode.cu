@@ -370,6 +370,8 @@ __device__ void topk_ranked(const float* __restrict__ lg, int T, int E, int k, S
   }
 }
 
+// TP: T rounded up to a power of two (the router's unrolled token loops).
+template <int TP>
 __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __half* x16 = reinterpret_cast<__half*>(smem + a.o_x16);
@@ -485,16 +487,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
       wv1 = __ldg(wr + 32 + lane);
     }
     const int q = p % QS;
-    float pacc[kMaxT];
+    float pacc[TP];
 #pragma unroll
-    for (int t = 0; t < kMaxT; ++t) pacc[t] = 0.f;
+    for (int t = 0; t < TP; ++t) pacc[t] = 0.f;
 #pragma unroll
     for (int hv = 0; hv < 2; ++hv) {
       const uint4 w4 = hv ? wv1 : wv0;
       const uint32_t wu[4] = {w4.x, w4.y, w4.z, w4.w};
       const int c0 = q * kSlice + (hv * 32 + lane) * 8;
 #pragma unroll
-      for (int t = 0; t < kMaxT; ++t) {
+      for (int t = 0; t < TP; ++t) {
         if (t < T) {
           const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * H + c0);
           const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
@@ -507,14 +509,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
       }
     }
 #pragma unroll
-    for (int t = 0; t < kMaxT; ++t) {
+    for (int t = 0; t < TP; ++t) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) pacc[t] += __shfl_xor_sync(0xffffffffu, pacc[t], o);
     }
     if (lane < T) {
       float v = pacc[0];
 #pragma unroll
-      for (int t = 1; t < kMaxT; ++t)
+      for (int t = 1; t < TP; ++t)
         if (lane == t) v = pacc[t];
       part[p * kMaxT + lane] = v;
     }
@@ -660,15 +662,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
   const int t0 = int((long long)cta * NT / ncta), t1 = int((long long)(cta + 1) * NT / ncta);
   const int d0 = int((long long)cta * ND / ncta), d1 = int((long long)(cta + 1) * ND / ncta);
   const int NCH = H / kChunk, NCD = I / kChunk;
+  // H and I are powers of two here: the unit arithmetic of the hot loops in shifts
+  const int lNCH = __ffs(NCH) - 1, lTPG = __ffs(TPG) - 1, lNRB = __ffs(NRB) - 1, lNCD = __ffs(NCD) - 1;
 
   // ============================================================ C: gate/up
   const int U = (t1 - t0) * NCH;
   int r0 = 0, nu = min(kMaxUnits, U);
   auto unit_at = [&](int u, int& gi, int& tb, int& ch) {
-    const int task = t0 + u / NCH;
-    ch = u - (u / NCH) * NCH;
-    gi = task / TPG;
-    tb = task - gi * TPG;
+    const int task = t0 + (u >> lNCH);
+    ch = u & (NCH - 1);
+    gi = task >> lTPG;
+    tb = task & (TPG - 1);
   };
   auto load = [&](int u, UnitRegs<2>& R) {
     if (u >= r0 + nu) return;
@@ -750,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     const int ntk = nu / NCH;
     for (int idx = tid; idx < ntk * 32; idx += kThreads) {
       const int tl = idx >> 5;
-      const int task = t0 + r0 / NCH + tl, gi = task / TPG, tb = task - gi * TPG;
+      const int task = t0 + (r0 >> lNCH) + tl, gi = task >> lTPG, tb = task & (TPG - 1);
       float v[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] = 0.f;
@@ -811,10 +815,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     if (!fits) set_error(a.err, MOE_ERANGE);
     const int ud = fits ? (d1 - d0) * NCD : 0;
     auto unit_of = [&](int u, int& gi, int& rb, int& ch) {
-      const int tl = u / NCD, task = d0 + tl;
-      ch = u - tl * NCD;
-      gi = task / NRB;
-      rb = task - gi * NRB;
+      const int task = d0 + (u >> lNCD);
+      ch = u & (NCD - 1);
+      gi = task >> lNRB;
+      rb = task & (NRB - 1);
     };
     for (int q0 = 0; q0 < ud; q0 += kMaxUnitsD) {
       const int nq = min(kMaxUnitsD, ud - q0);
@@ -828,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
       // h rows are staged (their weights are in L2 by then; the rows' loads go first)
       UnitRegs<1> da, db, dc;
       if (q0 == 0) {
-        const int per = I / 4;
+        const int per = I / 4, lper = __ffs(per) - 1;
         constexpr int kB = 4;  // 16 rows of 512 in one batch
         for (int i0 = 0; i0 < nrows * per; i0 += kB * kThreads) {
           float4 f[kB];
@@ -837,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
           for (int j = 0; j < kB; ++j) {
             const int i = i0 + tid + j * kThreads;
             if (i < nrows * per) {
-              const int R = i / per, q4 = i - R * per, e = rbase + R;
+              const int R = i >> lper, q4 = i & (per - 1), e = rbase + R;
               const size_t grow = e < n ? size_t(e) : size_t(a.maxTk + e - n);
               f[j] = __ldcg(reinterpret_cast<const float4*>(a.h + grow * a.Imax) + q4);
               hmx[j] = __ldcg(a.hmax + grow);
@@ -847,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
           for (int j = 0; j < kB; ++j) {
             const int i = i0 + tid + j * kThreads;
             if (i < nrows * per) {
-              const int R = i / per, q4 = i - R * per;
+              const int R = i >> lper, q4 = i & (per - 1);
               const float sc = pow2_scale_for(hmx[j]);
               __half2 p0 = __floats2half2_rn(f[j].x * sc, f[j].y * sc), p1 = __floats2half2_rn(f[j].z * sc, f[j].w * sc);
               uint2 w2;
@@ -887,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
       }
       __syncthreads();
       for (int idx = tid; idx < (nq / NCD) * 32; idx += kThreads) {
-        const int tl = idx >> 5, task = d0 + q0 / NCD + tl, gi = task / NRB, rbk = task - gi * NRB;
+        const int tl = idx >> 5, task = d0 + (q0 >> lNCD) + tl, gi = task >> lNRB, rbk = task & (NRB - 1);
         float v[4] = {0.f, 0.f, 0.f, 0.f};
         for (int c = 0; c < NCD; ++c) {
           const float4 pp = reinterpret_cast<const float4*>(red + (size_t(tl * NCD + c) * 32 + lane) * 4)[0];
@@ -917,7 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
   const int NI = T * (H / 4);
   const int i0 = int((long long)cta * NI / ncta), i1 = int((long long)(cta + 1) * NI / ncta);
   for (int i = i0 + tid; i < i1; i += kThreads) {
-    const int t = i / (H / 4), c4 = i - t * (H / 4);
+    const int t = i >> (__ffs(H) - 3), c4 = i & (H / 4 - 1);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const int nrow = k + a.has_shared;
     for (int r0 = 0; r0 < nrow; r0 += 16) {  // one round trip for k <= 15
@@ -1026,11 +1030,15 @@ int launch_decode_fused(const moe_layer_desc* d, moe_cache* c, const uint16_t* x
   Args a = {};
   size_t smem = 0;
   if (!decode_fused_layout(sh, T, ncta, a, smem)) return kNotFused;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(k_decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+  const int tp = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
+  void (*kern)(const Args) = tp == 1 ? k_decode_fused<1> : tp == 2 ? k_decode_fused<2>
+                           : tp == 4 ? k_decode_fused<4> : k_decode_fused<8>;
+  static bool attr[4] = {false, false, false, false};
+  const int ti = tp == 1 ? 0 : tp == 2 ? 1 : tp == 4 ? 2 : 3;
+  if (!attr[ti]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
       return MOE_ECUDA;
-    attr = true;
+    attr[ti] = true;
   }
   a.x = x;
   a.w_router = d->w_router;
@@ -1089,7 +1097,7 @@ int launch_decode_fused(const moe_layer_desc* d, moe_cache* c, const uint16_t* x
   attrs[0].val.cooperative = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, k_decode_fused, a) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ECUDA;
   }
