@@ -226,11 +226,11 @@ int moe_ws_kernel_times(moe_ws* ws, int max, float* ms_out, const char** names_o
  * MOE_DECODE_FUSED (the default) runs a decode call as ONE cooperative kernel
  * -- router, top-k, groups and lookup (with the heat update and the tail skip
  * when set), gate/up, down, combine, separated by grid barriers -- whenever the
- * shapes fit it: T <= 8, T*k <= 256, E <= 256 * (16 / T rounded down to a power
- * of two, at most 128 / k rounded likewise) and <= 1024, H a power of two in
- * [512, 2048], I a power of two in [256, 1024], I_shared 0 or I, x, y and
- * w_router 16-byte aligned, the shared blob 32-byte aligned; other calls run
- * the chain.  MOE_DECODE_CHAIN always runs the chain of kernels (router,
+ * shapes fit it: T <= 8, T*k <= 256, E <= 1024, H a power of two in
+ * [512, 2048], I a power of two in [256, 1024], I_shared 0 or I, each CTA's
+ * router rows (E + 1 over the SM count, rounded up) times H / 512 at most 32,
+ * its shared-memory layout within 227 KB, x, y and w_router 16-byte aligned,
+ * the shared blob 32-byte aligned; other calls run the chain.  MOE_DECODE_CHAIN always runs the chain of kernels (router,
  * top-k + groups, gate/up, down, combine).  The single kernel needs every
  * SM of the device for its CTAs (a cooperative launch: MOE_ECUDA if the device
  * cannot hold them at once).  Results agree within the layer's tolerance, not
