@@ -291,12 +291,15 @@ int moe_group(const int32_t* topk_ids, int T, int k, int E, int layer, moe_cache
  * (Strata page, "路由以后，专家怎样分工？"; FreeToken notes section 3.2: the
  * merge is exact, no expert dropped unless the workspace's tail skip is on).  x: bf16 [T, H]; y: bf16 [T, H], or
  * fp32 [T, H] when y_is_fp32.  T <= the workspace's maxT.  mode selects the
- * decode kernels (CUDA-core router, GEMVs) or the prefill kernels (router and
- * grouped expert GEMMs on the tensor cores); AUTO takes prefill from 128
- * tokens on.  Prefill needs H >= 128 and 16-byte aligned x, y, w_router and
- * w_shared_gate, else MOE_EINVAL; its y accumulates in fp32 with atomic
- * adds, so the order of the (at most k + 1) terms per element may vary
- * between runs. */
+ * decode kernels (the single-kernel decode or the chain: CUDA-core router,
+ * mma.sync expert tiles) or the prefill kernels (router and grouped expert
+ * GEMMs on the tensor cores); AUTO takes prefill from 32 tokens on where the
+ * shape and the pointers allow it, else decode (from 32 tokens the grouped
+ * GEMMs' 128-row weight tiles, reused across a group's tokens, are faster
+ * than decode's 16-row units).  MOE_MODE_PREFILL needs H >= 128 and
+ * 16-byte aligned x, y, w_router and w_shared_gate, else MOE_EINVAL; its y
+ * accumulates in fp32 with atomic adds, so the order of the (at most k + 1)
+ * terms per element may vary between runs. */
 int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y_is_fp32, int T, moe_cache* c,
                       moe_ws* ws, int mode, moe_stream_t stream);
 

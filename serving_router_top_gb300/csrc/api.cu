@@ -13,7 +13,7 @@ using namespace moe;
 namespace {
 
 // AUTO mode runs the prefill (tcgen05 grouped GEMM) path from this many tokens on.
-constexpr int kPrefillMinTokens = 128;
+constexpr int kPrefillMinTokens = 32;  // measured crossover: 16 tokens still faster on the decode kernels
 
 bool shape_ok(const moe_layer_shape& s) {
   // row widths: powers of two from 64 to 4096 (lanes per row and chunks per lane are powers of two)
@@ -522,12 +522,12 @@ int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, void* y, int y
   if (T == 0) return MOE_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int rc;
-  // decode GEMVs for small windows, tcgen05 GEMMs for prefill chunks
-  const bool prefill = mode == MOE_MODE_PREFILL || (mode == MOE_MODE_AUTO && T >= kPrefillMinTokens);
-  if (prefill && (!prefill_supported(s) || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 15) ||
-                  (reinterpret_cast<uintptr_t>(d->w_router) & 15) ||
-                  (s.I_shared > 0 && (reinterpret_cast<uintptr_t>(d->w_shared_gate) & 15))))
-    return MOE_EINVAL;
+  // decode kernels for small windows, tcgen05 grouped GEMMs from kPrefillMinTokens on
+  const bool prefill_ok = prefill_supported(s) && !(reinterpret_cast<uintptr_t>(x) & 15) &&
+                          !(reinterpret_cast<uintptr_t>(y) & 15) && !(reinterpret_cast<uintptr_t>(d->w_router) & 15) &&
+                          !(s.I_shared > 0 && (reinterpret_cast<uintptr_t>(d->w_shared_gate) & 15));
+  if (mode == MOE_MODE_PREFILL && !prefill_ok) return MOE_EINVAL;
+  const bool prefill = mode == MOE_MODE_PREFILL || (mode == MOE_MODE_AUTO && T >= kPrefillMinTokens && prefill_ok);
   ws->prof_n = 0;
   if (!prefill && ws->decode_path == MOE_DECODE_FUSED) {  // one cooperative kernel where the shapes fit
     ProfScope p(ws, "decode_fused", st);

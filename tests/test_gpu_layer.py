@@ -17,21 +17,21 @@ def _gpu():
     U.require_gpu()
 
 
-def run_layer(st, x_bits, T, bf16_out=False, layer=0):
+def run_layer(st, x_bits, T, bf16_out=False, layer=0, mode=moe.MOE_MODE_AUTO):
     x = torch.from_numpy(x_bits.view(np.int16)).cuda()
     if bf16_out:
         y = torch.zeros((T, st.H), dtype=torch.int16, device="cuda")
     else:
         y = torch.zeros((T, st.H), dtype=torch.float32, device="cuda")
-    st.forward(layer, x, y, T, y_is_fp32=not bf16_out)
+    st.forward(layer, x, y, T, y_is_fp32=not bf16_out, mode=mode)
     rc = moe.moe_sync_status(st.ws)
     assert rc == moe.MOE_OK, moe.strerror(rc)
     return U.y_to_numpy(y, bf16_out)
 
 
-def check_layer(st, T, bf16_out=False, step=0, layer=0, tail_skip=0):
+def check_layer(st, T, bf16_out=False, step=0, layer=0, tail_skip=0, mode=moe.MOE_MODE_AUTO):
     x_bits = I.activations(st.w.seed, step, T, st.H)
-    y = run_layer(st, x_bits, T, bf16_out, layer)
+    y = run_layer(st, x_bits, T, bf16_out, layer, mode)
     logits_t, ids_t, w_t = st.ws.routing(T)
     logits = logits_t.cpu().numpy()
     ids = ids_t.cpu().numpy()
@@ -84,11 +84,13 @@ def test_layer_t8_h256_e16_k2():
     (9, 256, 128, 40, 7, 64, 0.5),      # the smallest window of the streaming kernels
 ])
 def test_layer_small_shapes(T, H, I_, E, k, Is, frac):
+    """The decode kernels at every window size (forced past 32 tokens, where AUTO takes the
+    prefill kernels), then AUTO on fewer tokens than the workspace was sized for."""
     from serving_router_top_gb300.model import ModelState
     w = I.small_workload(T=T, H=H, I=I_, E=E, k=k, I_shared=Is, zipf_s=0.8, resident_frac=frac, seed=T + E)
     st = ModelState(w)
-    check_layer(st, T)
-    check_layer(st, max(1, T // 2), step=1)   # fewer tokens than the workspace was sized for
+    check_layer(st, T, mode=moe.MOE_MODE_DECODE)
+    check_layer(st, max(1, T // 2), step=1)
 
 
 def test_layer_decode_t4_h2048_e512_k10():
@@ -135,7 +137,7 @@ def test_tail_skip_small_windows(T, R):
     st.ws.set_tail_skip(R)
     n_skip = 0
     for step in range(3):
-        _, ref = check_layer(st, T, step=step, tail_skip=R)
+        _, ref = check_layer(st, T, step=step, tail_skip=R, mode=moe.MOE_MODE_DECODE)
         n_skip += int((ref.src == olayer.SRC_SKIPPED).sum())
     assert n_skip > 0
 
@@ -277,11 +279,17 @@ def test_group_rejects_out_of_range_ids():
 
 def test_large_expert_layer_decode_batch64_all_tokens():
     """One layer of the 4096-hidden, 256-expert top-6 model (I = I_shared = 2048) decoding a batch of
-    64 tokens: every token against the oracle, plus the router, routing and groups as check_layer."""
+    64 tokens: every token against the oracle, plus the router, routing and groups as check_layer --
+    on the decode kernels (the streaming expert tiles) and under AUTO (the grouped GEMMs, which
+    AUTO takes from 32 tokens on)."""
     from serving_router_top_gb300.model import ModelState
     w = I.WORKLOADS["large_h4096_e256_k6"]
     st = ModelState(w, layers=1, maxT=64)
-    check_layer(st, 64, step=7)
+    check_layer(st, 64, step=7, mode=moe.MOE_MODE_DECODE)
+    st.ws.set_profiling(True)
+    check_layer(st, 64, step=8)
+    assert "gateup_gemm" in [n for n, _ in st.ws.kernel_times()]
+    st.ws.set_profiling(False)
 
 
 @pytest.mark.parametrize("T", [6, 20])   # the decode GEMVs; the streaming kernel past 8 tokens
