@@ -226,7 +226,7 @@ int moe_ws_kernel_times(moe_ws* ws, int max, float* ms_out, const char** names_o
  * MOE_DECODE_FUSED (the default) runs a decode call as ONE cooperative kernel
  * -- router, top-k, groups and lookup (with the heat update and the tail skip
  * when set), gate/up, down, combine, separated by grid barriers -- whenever the
- * shapes fit it: T <= 8, T*k <= 256, E <= 1024, H a power of two in
+ * shapes fit it: T <= 16, T*k <= 256, E <= 1024, H a power of two in
  * [512, 2048], I a power of two in [256, 1024], I_shared 0 or I, each CTA's
  * router rows (E + 1 over the SM count, rounded up) times H / 512 at most 32,
  * its shared-memory layout within 227 KB, x, y and w_router 16-byte aligned,

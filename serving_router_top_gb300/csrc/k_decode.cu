@@ -54,10 +54,10 @@ namespace dec {
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kGuDepth = 2;  // gate/up units in flight per warp (in registers)
-constexpr int kXVec = (8 * 2048 / 8 + kThreads - 1) / kThreads;  // 16-byte pieces of x per thread, at most
-constexpr int kEVec = (1024 + kThreads - 1) / kThreads;          // residency entries per thread, at most
 constexpr int kChunk = 256;        // columns per unit: a lane's 64 columns, one 32-byte load per row
-constexpr int kMaxT = 8;           // tokens (the MMA's N)
+constexpr int kMaxT = 16;          // tokens (two 8-row tiles of the MMA's N)
+constexpr int kXVec = (kMaxT * 2048 / 8 + kThreads - 1) / kThreads;  // 16-byte pieces of x per thread, at most
+constexpr int kEVec = (1024 + kThreads - 1) / kThreads;          // residency entries per thread, at most
 constexpr int kMaxEnt = 256;       // T * k
 constexpr int kMaxGroups = kMaxEnt + 1;
 constexpr int kSlice = 512;        // router row elements per warp pair
@@ -237,15 +237,21 @@ __device__ __forceinline__ void load_unit_smem(const uint8_t* base, int mstride,
   }
 }
 
-// acc[m][even/odd MMA] += dq(W rows) . B for the lane's 64 columns of chunk ch.
-// brow: the lane's B row (activations, f16, perm_col layout), or null (zeros).
-template <int NM>
-__device__ __forceinline__ void mma_unit(const UnitRegs<NM>& R, const __half* brow, int ch, int t4,
-                                         float (&acc)[NM][2][4]) {
-  const uint4* xp = brow ? reinterpret_cast<const uint4*>(brow + ch * kChunk) + t4 : nullptr;
+// The lane's 64 columns of chunk ch: dq(W rows) . B.  NT = 1: one tile of 8 B rows
+// (brow0 = the lane's row), acc[m][0] and acc[m][1] the even and odd MMAs of each code
+// word (two accumulation chains, summed by the caller).  NT = 2: two tiles (brow0 for
+// rows 0..7, brow1 for rows 8..15 of the group), acc[m][tile]; the dequantised A
+// fragments serve both.  A null B row reads zeros.
+template <int NM, int NT>
+__device__ __forceinline__ void mma_unit(const UnitRegs<NM>& R, const __half* brow0, const __half* brow1, int ch,
+                                         int t4, float (&acc)[NM][2][4]) {
+  const uint4* xp0 = brow0 ? reinterpret_cast<const uint4*>(brow0 + ch * kChunk) + t4 : nullptr;
+  const uint4* xp1 = (NT == 2 && brow1) ? reinterpret_cast<const uint4*>(brow1 + ch * kChunk) + t4 : nullptr;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
-    const uint4 xq = xp ? xp[q * 4] : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 xq = xp0 ? xp0[q * 4] : make_uint4(0u, 0u, 0u, 0u);
+    uint4 xr = make_uint4(0u, 0u, 0u, 0u);
+    if (NT == 2 && xp1) xr = xp1[q * 4];
     const int blk = q >> 1;
 #pragma unroll
     for (int m = 0; m < NM; ++m) {
@@ -255,10 +261,14 @@ __device__ __forceinline__ void mma_unit(const UnitRegs<NM>& R, const __half* br
       uint32_t a0, a1, a2, a3;
       e2m1_pair2(w0, a0, a2);
       e2m1_pair2(w1, a1, a3);
-      mma16816(acc[m][0], hmul2(a0, sa), hmul2(a1, sb), hmul2(a2, sa), hmul2(a3, sb), xq.x, xq.y);
+      const uint32_t p0 = hmul2(a0, sa), p1 = hmul2(a1, sb), p2 = hmul2(a2, sa), p3 = hmul2(a3, sb);
+      mma16816(acc[m][0], p0, p1, p2, p3, xq.x, xq.y);
+      if (NT == 2) mma16816(acc[m][1], p0, p1, p2, p3, xr.x, xr.y);
       e2m1_pair2(w0 >> 16, a0, a2);
       e2m1_pair2(w1 >> 16, a1, a3);
-      mma16816(acc[m][1], hmul2(a0, sa), hmul2(a1, sb), hmul2(a2, sa), hmul2(a3, sb), xq.z, xq.w);
+      const uint32_t r0 = hmul2(a0, sa), r1 = hmul2(a1, sb), r2 = hmul2(a2, sa), r3 = hmul2(a3, sb);
+      mma16816(acc[m][NT == 2 ? 0 : 1], r0, r1, r2, r3, xq.z, xq.w);
+      if (NT == 2) mma16816(acc[m][1], r0, r1, r2, r3, xr.z, xr.w);
     }
   }
 }
@@ -370,9 +380,13 @@ __device__ void topk_ranked(const float* __restrict__ lg, int T, int E, int k, S
   }
 }
 
-// TP: T rounded up to a power of two (the router's unrolled token loops).
+// TP: T rounded up to a power of two (the router's unrolled token loops); above 8 tokens
+// the expert units run two 8-row tiles of B on the same dequantised weights.
 template <int TP>
 __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
+  constexpr int kNT = TP > 8 ? 2 : 1;  // 8-row tiles of B per unit
+  constexpr int kGD = TP > 8 ? 1 : kGuDepth;  // gate/up units in flight per warp (two tiles: registers)
+  constexpr int kUnitsGU = kMaxUnits / kNT, kUnitsDN = kMaxUnitsD / kNT;  // partial tiles of one round
   extern __shared__ __align__(128) uint8_t smem[];
   __half* x16 = reinterpret_cast<__half*>(smem + a.o_x16);
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + a.o_xs);
@@ -667,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
 
   // ============================================================ C: gate/up
   const int U = (t1 - t0) * NCH;
-  int r0 = 0, nu = min(kMaxUnits, U);
+  int r0 = 0, nu = min(kUnitsGU, U);
   auto unit_at = [&](int u, int& gi, int& tb, int& ch) {
     const int task = t0 + (u >> lNCH);
     ch = u & (NCH - 1);
@@ -692,25 +706,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[m][q >> 2][q & 3] = 0.f;
     if (sm.gblob[gi]) {
-      const __half* brow = nullptr;
-      if (g8 < nv) brow = x16 + size_t(gi == G ? g8 : sm.ent_tok[e0 + g8]) * XR;
-      mma_unit<2>(R, brow, ch, t4, acc);
+      const __half* b0 = nullptr;
+      const __half* b1 = nullptr;
+      if (g8 < nv) b0 = x16 + size_t(gi == G ? g8 : sm.ent_tok[e0 + g8]) * XR;
+      if (kNT == 2 && g8 + 8 < nv) b1 = x16 + size_t(gi == G ? g8 + 8 : sm.ent_tok[e0 + g8 + 8]) * XR;
+      mma_unit<2, kNT>(R, b0, b1, ch, t4, acc);
     }
-    float4* dst = reinterpret_cast<float4*>(red + (size_t(u - r0) * 32 + lane) * 8);
-    dst[0] = make_float4(acc[0][0][0] + acc[0][1][0], acc[0][0][1] + acc[0][1][1], acc[0][0][2] + acc[0][1][2],
-                         acc[0][0][3] + acc[0][1][3]);
-    dst[1] = make_float4(acc[1][0][0] + acc[1][1][0], acc[1][0][1] + acc[1][1][1], acc[1][0][2] + acc[1][1][2],
-                         acc[1][0][3] + acc[1][1][3]);
-  };
-  // kGuDepth units in flight per warp: the first ones are requested before anything else
-  UnitRegs<2> rr[kGuDepth];
+    float4* dst = reinterpret_cast<float4*>(red + (size_t(u - r0) * 32 + lane) * 8 * kNT);
+    if (kNT == 1) {
+      dst[0] = make_float4(acc[0][0][0] + acc[0][1][0], acc[0][0][1] + acc[0][1][1], acc[0][0][2] + acc[0][1][2],
+                           acc[0][0][3] + acc[0][1][3]);
+      dst[1] = make_float4(acc[1][0][0] + acc[1][1][0], acc[1][0][1] + acc[1][1][1], acc[1][0][2] + acc[1][1][2],
+                           acc[1][0][3] + acc[1][1][3]);
+    } else {  // per tile: gate, then up
 #pragma unroll
-  for (int d = 0; d < kGuDepth; ++d) load(warp + d * kWarps, rr[d]);
+      for (int tl = 0; tl < kNT; ++tl) {
+        dst[2 * tl] = make_float4(acc[0][tl][0], acc[0][tl][1], acc[0][tl][2], acc[0][tl][3]);
+        dst[2 * tl + 1] = make_float4(acc[1][tl][0], acc[1][tl][1], acc[1][tl][2], acc[1][tl][3]);
+      }
+    }
+  };
+  // kGD units in flight per warp: the first ones are requested before anything else
+  UnitRegs<2> rr[kGD];
+#pragma unroll
+  for (int d = 0; d < kGD; ++d) load(warp + d * kWarps, rr[d]);
   if (tid == kThreads - 32) {
     // every weight byte of the CTA's later gate/up units and of its down tasks into L2 --
     // one bulk prefetch per group and region, the rows of consecutive tasks of a group
     // being contiguous -- so the step's expert bytes stream from HBM at once
-    const int ta0 = t0 + min(t1 - t0, (kGuDepth * kWarps + NCH - 1) / NCH);
+    const int ta0 = t0 + min(t1 - t0, (kGD * kWarps + NCH - 1) / NCH);
     for (int gi = ta0 / TPG; ta0 < t1 && gi <= (t1 - 1) / TPG; ++gi) {
       const uint8_t* blob = sm.gblob[gi];
       if (!blob) continue;
@@ -735,17 +759,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     else sm.gs[g][0] = sm.gs[g][1] = sm.gs[g][2] = 0.f;
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
-  for (; r0 < U; r0 += kMaxUnits) {
-    nu = min(kMaxUnits, U - r0);
+  for (; r0 < U; r0 += kUnitsGU) {
+    nu = min(kUnitsGU, U - r0);
     if (r0 > 0) {
 #pragma unroll
-      for (int d = 0; d < kGuDepth; ++d) load(r0 + warp + d * kWarps, rr[d]);
+      for (int d = 0; d < kGD; ++d) load(r0 + warp + d * kWarps, rr[d]);
     }
-    for (int u = r0 + warp; u < r0 + nu; u += kGuDepth * kWarps) {
+    for (int u = r0 + warp; u < r0 + nu; u += kGD * kWarps) {
 #pragma unroll
-      for (int d = 0; d < kGuDepth; ++d) {
+      for (int d = 0; d < kGD; ++d) {
         run(u + d * kWarps, rr[d]);
-        load(u + (d + kGuDepth) * kWarps, rr[d]);
+        load(u + (d + kGD) * kWarps, rr[d]);
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -755,46 +779,52 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     for (int idx = tid; idx < ntk * 32; idx += kThreads) {
       const int tl = idx >> 5;
       const int task = t0 + (r0 >> lNCH) + tl, gi = task >> lTPG, tb = task & (TPG - 1);
-      float v[8];
+      float v[8 * kNT];  // per tile: gate (4), up (4)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.f;
+      for (int j = 0; j < 8 * kNT; ++j) v[j] = 0.f;
       for (int c = 0; c < NCH; ++c) {
-        const float4* src = reinterpret_cast<const float4*>(red + (size_t(tl * NCH + c) * 32 + lane) * 8);
-        const float4 p0 = src[0], p1 = src[1];
-        v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
-        v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+        const float4* src = reinterpret_cast<const float4*>(red + (size_t(tl * NCH + c) * 32 + lane) * 8 * kNT);
+#pragma unroll
+        for (int j = 0; j < 2 * kNT; ++j) {
+          const float4 pj = src[j];
+          v[4 * j] += pj.x; v[4 * j + 1] += pj.y; v[4 * j + 2] += pj.z; v[4 * j + 3] += pj.w;
+        }
       }
       const bool shared = gi == G;
       const bool has_blob = sm.gblob[gi] != nullptr;
       const int e0 = sm.goff[gi], nv = sm.goff[gi + 1] - e0;
       const float gs0 = sm.gs[gi][0], gs1 = sm.gs[gi][1];
-      float hm[2] = {0.f, 0.f};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int jloc = 2 * t4 + (q & 1);
-        const int r = tb * 16 + g8 + 8 * (q >> 1);
-        if (jloc < nv) {
-          const int tok = shared ? jloc : sm.ent_tok[e0 + jloc];
-          const float inv = sm.xinv[tok];
-          const float hv = has_blob ? silu_f32(v[q] * inv * gs0) * (v[4 + q] * inv * gs1) : 0.f;
-          const int hrow = shared ? a.maxTk + jloc : e0 + jloc;
-          a.h[size_t(hrow) * a.Imax + r] = hv;
-          hm[q & 1] = fmaxf(hm[q & 1], fabsf(hv));
+      for (int tt = 0; tt < kNT; ++tt) {
+        float hm[2] = {0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int jloc = 8 * tt + 2 * t4 + (q & 1);
+          const int r = tb * 16 + g8 + 8 * (q >> 1);
+          if (jloc < nv) {
+            const int tok = shared ? jloc : sm.ent_tok[e0 + jloc];
+            const float inv = sm.xinv[tok];
+            const float hv =
+                has_blob ? silu_f32(v[8 * tt + q] * inv * gs0) * (v[8 * tt + 4 + q] * inv * gs1) : 0.f;
+            const int hrow = shared ? a.maxTk + jloc : e0 + jloc;
+            a.h[size_t(hrow) * a.Imax + r] = hv;
+            hm[q & 1] = fmaxf(hm[q & 1], fabsf(hv));
+          }
         }
-      }
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        hm[0] = fmaxf(hm[0], __shfl_xor_sync(0xffffffffu, hm[0], o));
-        hm[1] = fmaxf(hm[1], __shfl_xor_sync(0xffffffffu, hm[1], o));
-      }
-      if (g8 == 0)
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int jloc = 2 * t4 + q;
-          if (jloc < nv)
-            atomicMax(reinterpret_cast<unsigned int*>(a.hmax) + (shared ? a.maxTk + jloc : e0 + jloc),
-                      __float_as_uint(hm[q]));
+        for (int o = 4; o < 32; o <<= 1) {
+          hm[0] = fmaxf(hm[0], __shfl_xor_sync(0xffffffffu, hm[0], o));
+          hm[1] = fmaxf(hm[1], __shfl_xor_sync(0xffffffffu, hm[1], o));
         }
+        if (g8 == 0)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int jloc = 8 * tt + 2 * t4 + q;
+            if (jloc < nv)
+              atomicMax(reinterpret_cast<unsigned int*>(a.hmax) + (shared ? a.maxTk + jloc : e0 + jloc),
+                        __float_as_uint(hm[q]));
+          }
+      }
     }
     __syncthreads();
   }
@@ -820,8 +850,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
       gi = task >> lNRB;
       rb = task & (NRB - 1);
     };
-    for (int q0 = 0; q0 < ud; q0 += kMaxUnitsD) {
-      const int nq = min(kMaxUnitsD, ud - q0);
+    for (int q0 = 0; q0 < ud; q0 += kUnitsDN) {
+      const int nq = min(kUnitsDN, ud - q0);
       auto load_d = [&](int u, UnitRegs<1>& R) {
         if (u >= q0 + nq) return;
         int gi, rb, ch;
@@ -875,11 +905,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
         float acc[1][2][4];
 #pragma unroll
         for (int x = 0; x < 8; ++x) acc[0][x >> 2][x & 3] = 0.f;
-        if (sm.gblob[gi])
-          mma_unit<1>(R, g8 < nv ? h16 + size_t(sm.goff[gi] - rbase + g8) * HR : nullptr, ch, t4, acc);
-        reinterpret_cast<float4*>(red + (size_t(u - q0) * 32 + lane) * 4)[0] =
-            make_float4(acc[0][0][0] + acc[0][1][0], acc[0][0][1] + acc[0][1][1], acc[0][0][2] + acc[0][1][2],
-                        acc[0][0][3] + acc[0][1][3]);
+        if (sm.gblob[gi]) {
+          const __half* hb = h16 + size_t(sm.goff[gi] - rbase) * HR;
+          mma_unit<1, kNT>(R, g8 < nv ? hb + size_t(g8) * HR : nullptr,
+                          (kNT == 2 && g8 + 8 < nv) ? hb + size_t(g8 + 8) * HR : nullptr, ch, t4, acc);
+        }
+        float4* dst = reinterpret_cast<float4*>(red + (size_t(u - q0) * 32 + lane) * 4 * kNT);
+        if (kNT == 1)
+          dst[0] = make_float4(acc[0][0][0] + acc[0][1][0], acc[0][0][1] + acc[0][1][1], acc[0][0][2] + acc[0][1][2],
+                               acc[0][0][3] + acc[0][1][3]);
+        else
+#pragma unroll
+          for (int tl = 0; tl < kNT; ++tl) dst[tl] = make_float4(acc[0][tl][0], acc[0][tl][1], acc[0][tl][2], acc[0][tl][3]);
       };
       for (int u = q0 + warp; u < q0 + nq; u += 3 * kWarps) {
         run_d(u, da);
@@ -892,20 +929,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
       __syncthreads();
       for (int idx = tid; idx < (nq / NCD) * 32; idx += kThreads) {
         const int tl = idx >> 5, task = d0 + (q0 >> lNCD) + tl, gi = task >> lNRB, rbk = task & (NRB - 1);
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        float v[4 * kNT];
+#pragma unroll
+        for (int j = 0; j < 4 * kNT; ++j) v[j] = 0.f;
         for (int c = 0; c < NCD; ++c) {
-          const float4 pp = reinterpret_cast<const float4*>(red + (size_t(tl * NCD + c) * 32 + lane) * 4)[0];
-          v[0] += pp.x; v[1] += pp.y; v[2] += pp.z; v[3] += pp.w;
+          const float4* pp = reinterpret_cast<const float4*>(red + (size_t(tl * NCD + c) * 32 + lane) * 4 * kNT);
+#pragma unroll
+          for (int tt = 0; tt < kNT; ++tt) {
+            const float4 f = pp[tt];
+            v[4 * tt] += f.x; v[4 * tt + 1] += f.y; v[4 * tt + 2] += f.z; v[4 * tt + 3] += f.w;
+          }
         }
         const bool shared = gi == G, has_blob = sm.gblob[gi] != nullptr;
         const int e0 = sm.goff[gi], nv = sm.goff[gi + 1] - e0;
         const float gsd = sm.gs[gi][2];
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int jloc = 2 * t4 + (x & 1);
+        for (int x = 0; x < 4 * kNT; ++x) {
+          const int jloc = 8 * (x >> 2) + 2 * t4 + (x & 1);
           if (jloc < nv) {
             const int pos = shared ? a.maxTk + jloc : sm.ent_pos[e0 + jloc];
-            a.o[size_t(pos) * H + rbk * 16 + g8 + 8 * (x >> 1)] =
+            a.o[size_t(pos) * H + rbk * 16 + g8 + 8 * ((x >> 1) & 1)] =
                 has_blob ? v[x] * sm.hs_inv[e0 - rbase + jloc] * gsd : 0.f;
           }
         }
@@ -994,17 +1037,20 @@ static bool decode_fused_layout(const moe_layer_shape& sh, int T, int ncta, dec:
   a.o_red = align128(T * (H + kPadH) * 2);
   a.o_h16 = a.o_red + kMaxUnits * 32 * 8 * 4;
   const int end_cd = a.o_h16 + align128(a.hrows * (I + kPadH) * 2);
-  // phases A and B (over the tiles and the rows, unused until C): x (bf16), the logits,
-  // the top-k's chunk bests, candidates, selections and terms, the router partial sums
+  // over the tiles and the rows (unused until C): phase A's x (bf16) and router partial
+  // sums, then, over those (dead after the first barrier), phase B's logits and the
+  // top-k's chunk bests, candidates, selections and terms
   a.capc = E < 32 * k ? E : 32 * k;
   a.o_xs = a.o_red;
-  a.o_lg = a.o_xs + align128(T * H * 2);
+  a.o_part = a.o_xs + align128(T * H * 2);
+  const int end_a = a.o_part + align128(kMaxPairs * dec::kMaxT * 4);
+  a.o_lg = a.o_red;
   a.o_cb = a.o_lg + align128(T * E * 4);
   a.o_cand = a.o_cb + align128(T * 32 * 8);
   a.o_sel = a.o_cand + align128(T * a.capc * 8);
   a.o_pr = a.o_sel + align128(T * k * 8);
-  a.o_part = a.o_pr + align128(T * k * 4);
-  const int end_ab = a.o_part + align128(kMaxPairs * kMaxT * 4);
+  const int end_b = a.o_pr + align128(T * k * 4);
+  const int end_ab = end_a > end_b ? end_a : end_b;
   a.o_small = align128(end_ab > end_cd ? end_ab : end_cd);
   smem = size_t(a.o_small) + sizeof(Small);
   return smem <= 227 * 1024;
@@ -1016,7 +1062,7 @@ int launch_decode_fused(const moe_layer_desc* d, moe_cache* c, const uint16_t* x
   using namespace dec;
   const moe_layer_shape& sh = d->s;
   const bool has_shared = sh.I_shared > 0 && d->shared_blob;
-  if (T < 1 || T > kMaxT || T * sh.k > kMaxEnt || sh.E > 1024) return kNotFused;
+  if (T < 1 || T > dec::kMaxT || T * sh.k > dec::kMaxEnt || sh.E > 1024) return kNotFused;
   if (!pow2(sh.H) || sh.H < kSlice || sh.H > 2048 || !pow2(sh.I) || sh.I < kChunk || sh.I > 1024) return kNotFused;
   if (has_shared && sh.I_shared != sh.I) return kNotFused;
   if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 15) ||
@@ -1030,11 +1076,11 @@ int launch_decode_fused(const moe_layer_desc* d, moe_cache* c, const uint16_t* x
   Args a = {};
   size_t smem = 0;
   if (!decode_fused_layout(sh, T, ncta, a, smem)) return kNotFused;
-  const int tp = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
+  const int tp = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16;
   void (*kern)(const Args) = tp == 1 ? k_decode_fused<1> : tp == 2 ? k_decode_fused<2>
-                           : tp == 4 ? k_decode_fused<4> : k_decode_fused<8>;
-  static bool attr[4] = {false, false, false, false};
-  const int ti = tp == 1 ? 0 : tp == 2 ? 1 : tp == 4 ? 2 : 3;
+                           : tp == 4 ? k_decode_fused<4> : tp == 8 ? k_decode_fused<8> : k_decode_fused<16>;
+  static bool attr[5] = {false, false, false, false, false};
+  const int ti = tp == 1 ? 0 : tp == 2 ? 1 : tp == 4 ? 2 : tp == 8 ? 3 : 4;
   if (!attr[ti]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
       return MOE_ECUDA;

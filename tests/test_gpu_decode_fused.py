@@ -39,6 +39,10 @@ def ran_fused(st, T, x_bits=None):
     (7, 1024, 256, 64, 9, 256, 0.25, 0.5),     # ragged token count, 9 of 64 experts per token
     (2, 512, 512, 1, 1, 512, 1.0, 0.0),        # a single routed expert (weight 1) and the shared one
     (8, 2048, 256, 256, 32, 256, 0.5, 0.6),    # 256 selections, many shared groups
+    (16, 2048, 512, 512, 10, 512, 0.5, 1.1),   # two 8-row tiles of B per unit, the shared expert on both
+    (12, 1024, 256, 64, 9, 256, 0.25, 0.5),    # ragged second tile, groups above 8 tokens
+    (9, 512, 512, 40, 7, 0, 1.0, 0.0),         # one token past a tile, no shared expert
+    (13, 2048, 1024, 200, 16, 1024, 0.5, 0.8),  # 208 selections, I of four chunks, second tile
 ])
 def test_fused_decode_layer(T, H, I_, E, k, Is, frac, zipf):
     """Logits within the fp32 bound of the oracle's, ids bit-exact on the same logits (near-ties
