@@ -131,6 +131,8 @@ struct Small {
   int32_t resid[1024];  // the layer's residency and staging rows
   int32_t stage[1024];
   __align__(16) float gs[kMaxGroups][4];  // each group's global scales (gate, up, down) and a pad
+  unsigned long long bar_base;  // the grid-barrier counter at the CTA's start, rounded down to the grid
+  unsigned long long bar_idx;   // barriers passed
   int ok, cnt[4];
 };
 
@@ -139,42 +141,46 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu(unsigned long long* p, unsigned long long v) {
-  unsigned long long old;
-  asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
-  return old;
-}
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
 
-// Grid barrier on a monotonic arrival counter: every barrier of every launch
-// adds one arrival per CTA, so a barrier is complete when the counter reaches
-// the next multiple of the arrivals it expects (N = the grid, plus the test
-// hook's phantom arrivals).  One acquire-release add per CTA, then acquire
-// loads until the count is reached -- at most wait_ns, after which the wait
-// records MOE_ETIMEOUT and every later phase of the CTA is skipped (the host
-// resets the counter with the error word).  (A two-level tree of counters was
-// measured slower: its last arrival pays two dependent atomic round trips.)
-// Returns whether the barrier was passed.  Every thread of the CTA calls it.
+__device__ __forceinline__ void red_add_release_gpu(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid barrier on a monotonic arrival counter: every barrier of every launch adds one
+// arrival per CTA, so between launches the counter is a multiple of the grid.  Each CTA
+// reads it once at its start (other CTAs may have arrived at the first barrier by then,
+// but fewer than the grid) and rounds down to that multiple, its base; barrier i is
+// complete when the counter reaches base + i * grid (+ the test hook's phantom arrivals,
+// which never come).  An arrival is a release add whose result nobody waits for; then
+// acquire loads until the count is reached -- at most wait_ns, after which the wait
+// records MOE_ETIMEOUT and every later phase of the CTA is skipped (the host resets the
+// counter with the error word).  (A two-level tree of counters was measured slower: its
+// last arrival pays two dependent atomic round trips; an acquire-release add that returns
+// the count costs every CTA a round trip before it starts polling.)  Returns whether the
+// barrier was passed.  Every thread of the CTA calls it.
 __device__ bool grid_barrier(const Args& a, Small& sm) {
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = sm.ok;
     if (ok) {
-      const unsigned long long N = gridDim.x + a.bar_extra;
-      const unsigned long long old = atom_add_acq_rel_gpu(a.bar, 1ull);
-      const unsigned long long target = (old / N + 1) * N;
-      if (old + 1 != target) {
-        const unsigned long long t0 = globaltimer_ns();
-        while (ld_acquire_gpu(a.bar) < target) {
-          if (globaltimer_ns() - t0 > a.wait_ns) {
-            set_error(a.err, MOE_ETIMEOUT);
-            ok = 0;
-            break;
-          }
+      const unsigned long long target = sm.bar_base + (++sm.bar_idx) * gridDim.x + a.bar_extra;
+      red_add_release_gpu(a.bar, 1ull);
+      const unsigned long long t0 = globaltimer_ns();
+      while (ld_acquire_gpu(a.bar) < target) {
+        if (globaltimer_ns() - t0 > a.wait_ns) {
+          set_error(a.err, MOE_ETIMEOUT);
+          ok = 0;
+          break;
         }
       }
     }
@@ -412,6 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
   if (tid == 0) {
     sm.ok = 1;
     sm.cnt[0] = sm.cnt[1] = sm.cnt[2] = sm.cnt[3] = 0;
+    sm.bar_base = ld_relaxed_gpu(a.bar) / gridDim.x * gridDim.x;  // before this CTA's first arrival
+    sm.bar_idx = 0;
   }
   // this CTA's slice of the shared expert's blob into L2 (its gate/up tasks run in C)
   if (a.has_shared && tid == 0) {

@@ -93,6 +93,28 @@ def test_layer_small_shapes(T, H, I_, E, k, Is, frac):
     check_layer(st, max(1, T // 2), step=1)
 
 
+@pytest.mark.parametrize("T,H,I_,E,k,Is,frac", [
+    (1, 128, 64, 12, 3, 64, 1.0),
+    (5, 128, 64, 12, 3, 64, 0.5),
+    (7, 256, 128, 40, 7, 64, 0.25),
+    (8, 256, 128, 40, 7, 64, 0.5),      # the largest window of the chain's GEMVs
+    (12, 512, 256, 64, 6, 256, 0.5),    # the chain's streaming kernel below 32 tokens
+    (4, 2048, 512, 512, 10, 512, 0.5),  # the decode window's shapes
+])
+def test_layer_decode_chain(T, H, I_, E, k, Is, frac):
+    """The chain of decode kernels (router, top-k + groups, gate/up, down, combine), which the
+    single kernel replaces by default: every shape against the oracle, fp32 and bf16 out."""
+    from serving_router_top_gb300.model import ModelState
+    w = I.small_workload(T=T, H=H, I=I_, E=E, k=k, I_shared=Is, zipf_s=0.8, resident_frac=frac, seed=2 * T + E)
+    st = ModelState(w)
+    st.ws.set_decode_path(moe.MOE_DECODE_CHAIN)
+    st.ws.set_profiling(True)
+    check_layer(st, T, mode=moe.MOE_MODE_DECODE)
+    assert "decode_fused" not in [n for n, _ in st.ws.kernel_times()]
+    st.ws.set_profiling(False)
+    check_layer(st, T, bf16_out=True, step=1, mode=moe.MOE_MODE_DECODE)
+
+
 def test_layer_decode_t4_h2048_e512_k10():
     from serving_router_top_gb300.model import ModelState
     w = I.WORKLOADS["decode_t4_h2048_e512_k10"]
