@@ -22,7 +22,9 @@
 //      from the 32-expert chunk maxima, then ranks by counting) and the same
 //      grouping on them, so every CTA holds the same groups without another
 //      barrier; CTA 0 writes them, with the top-k, lookups, statistics and the
-//      heat update, to the workspace.
+//      heat update, to the workspace.  As soon as the top-k's candidates are
+//      known (a superset of the selections), CTA c requests its share of their
+//      gate/up bytes into L2, so the stream from HBM starts before the grouping.
 //   C  gate/up: tasks are (group, 16-row block of I), CTA c owns a contiguous
 //      range of them, and the (task, 256-column chunk) units go round-robin to
 //      the 16 warps, two units in flight per warp in registers (the first two
@@ -43,6 +45,8 @@
 //      shared term last, each CTA a slice of the T x H outputs -- deterministic,
 //      no atomics.
 //
+// The first two barriers are split: a CTA arrives, does work that no other CTA's
+// results feed (x into f16; the first down units' weight loads), then waits.
 // Every wait is bounded: the grid barriers give up after the workspace's wait limit,
 // record MOE_ETIMEOUT, and the CTAs skip the remaining phases.
 #include "dequant.cuh"
@@ -120,12 +124,15 @@ struct Small {
   uint32_t srt[kMaxEnt];
   int32_t ent_tok[kMaxEnt];
   int32_t ent_pos[kMaxEnt];
-  unsigned long long tau[kMaxT];  // top-k thresholds and candidate counts per token
+  unsigned long long tau[kMaxT];  // top-k per token: threshold, best entry, candidates
+  unsigned long long top[kMaxT];
   int32_t ncand[kMaxT];
+  uint32_t cbits[32];  // candidate experts of the window (bit e)
   int32_t gexp[kMaxGroups];
   int32_t goff[kMaxGroups + 1];
   const uint8_t* gblob[kMaxGroups];
   float xinv[kMaxT];
+  float bias_r[kMaxPairs];  // the router bias of the CTA's rows
   float gl[kMaxT];
   float hs_inv[kMaxEnt + kMaxT];
   int32_t resid[1024];  // the layer's residency and staging rows
@@ -166,15 +173,19 @@ __device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long
 // records MOE_ETIMEOUT and every later phase of the CTA is skipped (the host resets the
 // counter with the error word).  (A two-level tree of counters was measured slower: its
 // last arrival pays two dependent atomic round trips; an acquire-release add that returns
-// the count costs every CTA a round trip before it starts polling.)  Returns whether the
-// barrier was passed.  Every thread of the CTA calls it.
-__device__ bool grid_barrier(const Args& a, Small& sm) {
+// the count costs every CTA a round trip before it starts polling; so were four staggered
+// pollers per CTA.)  grid_arrive and grid_wait are the two halves: between them a CTA may
+// do work that reads nothing another CTA writes before the barrier.  grid_wait returns
+// whether the barrier was passed.  Every thread of the CTA calls both.
+__device__ void grid_arrive(const Args& a, Small& sm) {
   __syncthreads();
+  if (threadIdx.x == 0 && sm.ok) red_add_release_gpu(a.bar, 1ull);
+}
+__device__ bool grid_wait(const Args& a, Small& sm) {
   if (threadIdx.x == 0) {
     int ok = sm.ok;
     if (ok) {
       const unsigned long long target = sm.bar_base + (++sm.bar_idx) * gridDim.x + a.bar_extra;
-      red_add_release_gpu(a.bar, 1ull);
       const unsigned long long t0 = globaltimer_ns();
       while (ld_acquire_gpu(a.bar) < target) {
         if (globaltimer_ns() - t0 > a.wait_ns) {
@@ -189,6 +200,10 @@ __device__ bool grid_barrier(const Args& a, Small& sm) {
   __syncthreads();
   return *reinterpret_cast<volatile int*>(&sm.ok) != 0;
 }
+__device__ bool grid_barrier(const Args& a, Small& sm) {
+  grid_arrive(a, sm);
+  return grid_wait(a, sm);
+}
 
 // Column c of an activation row is stored where lane (., t4) finds its eight
 // columns 8q..8q+7 of each 256-column chunk as one 16-byte load: chunk-major,
@@ -198,6 +213,36 @@ __device__ bool grid_barrier(const Args& a, Small& sm) {
 __device__ __forceinline__ int perm_col(int c) {
   const int cc = c & (kChunk - 1);
   return (c - cc) + (((cc & 63) >> 3) * 4 + (cc >> 6)) * 8 + (c & 7);
+}
+
+// L2 eviction policies: the router weights (read by every step) kept, the expert weights
+// (read once per step) first to go
+__device__ __forceinline__ unsigned long long policy_evict_last() {
+  unsigned long long p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ unsigned long long policy_evict_first() {
+  unsigned long long p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_keep16(const void* p, unsigned long long pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void ld_once32(const void* p, uint32_t (&r)[8], unsigned long long pol) {
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "l"(p), "l"(pol));
+}
+__device__ __forceinline__ uint32_t ld_once_u32(const void* p, unsigned long long pol) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
+  return v;
 }
 
 // One unit as loaded by a lane: rows g8 and g8 + 8 of each matrix, the lane's
@@ -214,11 +259,12 @@ __device__ __forceinline__ void load_unit(const uint8_t* blob, const DevBlobLayo
 #pragma unroll
   for (int m = 0; m < NM; ++m) {
     const uint8_t* cp = blob + lay.code_off[mat0 + m] + size_t(row) * (K / 2) + ch * 128 + 32 * t4;
-    ld_stream32(cp, R.c[m][0]);
-    ld_stream32(cp + size_t(8) * (K / 2), R.c[m][1]);
+    const unsigned long long pol = policy_evict_first();
+    ld_once32(cp, R.c[m][0], pol);
+    ld_once32(cp + size_t(8) * (K / 2), R.c[m][1], pol);
     const uint8_t* sp = blob + lay.scale_off[mat0 + m] + size_t(row) * (K / 16) + ch * 16 + 4 * t4;
-    R.s[m][0] = ld_stream_u32(sp);
-    R.s[m][1] = ld_stream_u32(sp + size_t(8) * (K / 16));
+    R.s[m][0] = ld_once_u32(sp, pol);
+    R.s[m][1] = ld_once_u32(sp + size_t(8) * (K / 16), pol);
   }
 }
 
@@ -291,16 +337,21 @@ __device__ __forceinline__ unsigned long long rank_key(float x, int e) {
 //   2. tau_t, the k-th best of the token's chunk bests (0 when it has fewer than k
 //      chunks): k entries reach tau_t, so each of the token's k best does too;
 //   3. the entries that reach tau_t -- those of the k chunks whose best does, at most
-//      min(E, 32 k), usually a few more than k -- are compacted, and each takes as its rank
-//      the number of candidates above it; rank r < k is the token's selection r.
-// No step is a chain of warp-wide selections, which a decode step cannot afford.  Ids
-// and weights equal the top-k kernel's: the same order, and w_r = p_r / sum_j p_j with
-// p_r = exp(l_r - l_0) summed in rank order.  NaN logits rank as -inf and record
-// MOE_ENAN.  Leaves key[i] = id << 16 | i for the grouping.  Every thread of the CTA calls
-// this; it holds four __syncthreads and ends without one.
+//      min(E, 32 k), usually a few more than k -- are compacted (their experts, over all
+//      tokens, also as bits of sm.cbits), then on_cands runs;
+//   4. each candidate takes as its rank the number of candidates above it; rank r < k is
+//      the token's selection r, whose term p_r = exp(l_r - l_0) is taken at once (l_0,
+//      the token's best entry, is its best chunk best).
+// No step is a chain of warp-wide selections, which a decode step cannot afford (nor one
+// warp per token: its chain of dependent shared-memory and shuffle steps was measured
+// slower than the CTA-wide steps and their barriers).  Ids and weights equal the top-k
+// kernel's: the same order, and w_r = p_r / sum_j p_j summed in rank order.  NaN logits
+// rank as -inf and record MOE_ENAN.  Leaves key[i] = id << 16 | i for the grouping.  Every
+// thread of the CTA calls this; it holds four __syncthreads and ends without one.
+template <typename OnCands>
 __device__ void topk_ranked(const float* __restrict__ lg, int T, int E, int k, Small& sm, int32_t* err,
                             unsigned long long* __restrict__ cbest, unsigned long long* __restrict__ cand, int capc,
-                            unsigned long long* __restrict__ sel, float* __restrict__ pr) {
+                            unsigned long long* __restrict__ sel, float* __restrict__ pr, OnCands on_cands) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NCH = (E + 31) >> 5;
   bool nan_seen = false;
@@ -332,6 +383,7 @@ __device__ void topk_ranked(const float* __restrict__ lg, int T, int E, int k, S
     } else if (lane < NCH && r == k - 1) {
       sm.tau[warp] = mine;
     }
+    if (lane < NCH && r == 0) sm.top[warp] = mine;
   }
   __syncthreads();
   for (int it = warp; it < T * NCH; it += kWarps) {
@@ -345,7 +397,10 @@ __device__ void topk_ranked(const float* __restrict__ lg, int T, int E, int k, S
     const bool take = e < E && ck >= sm.tau[t];
     const unsigned b = __ballot_sync(0xffffffffu, take);
     int base = 0;
-    if (lane == 0 && b) base = atomicAdd(&sm.ncand[t], __popc(b));
+    if (lane == 0 && b) {
+      base = atomicAdd(&sm.ncand[t], __popc(b));
+      atomicOr(&sm.cbits[it - t * NCH], b);  // the candidate experts of all tokens
+    }
     base = __shfl_sync(0xffffffffu, base, 0);
     const int pos = base + __popc(b & ((1u << lane) - 1u));
     if (take) {
@@ -354,6 +409,7 @@ __device__ void topk_ranked(const float* __restrict__ lg, int T, int E, int k, S
     }
   }
   __syncthreads();
+  on_cands();
   {
     const int S = kThreads / T, t = tid / S;
     if (t < T) {
@@ -364,19 +420,15 @@ __device__ void topk_ranked(const float* __restrict__ lg, int T, int E, int k, S
         int r = 0;
 #pragma unroll 4
         for (int j = 0; j < C; ++j) r += cc[j] > me ? 1 : 0;
-        if (r < k) sel[t * k + r] = me;
+        if (r < k) {
+          sm.ids[t * k + r] = int(0xffffffffu - unsigned(me));
+          pr[t * k + r] = expf(float_of_key(unsigned(me >> 32)) - float_of_key(unsigned(sm.top[t] >> 32)));
+        }
       }
     }
   }
   __syncthreads();
   const int n = T * k;
-  for (int i = tid; i < n; i += kThreads) {
-    const int t = i / k;
-    const unsigned long long s = sel[i];
-    sm.ids[i] = int(0xffffffffu - unsigned(s));
-    pr[i] = expf(float_of_key(unsigned(s >> 32)) - float_of_key(unsigned(sel[t * k] >> 32)));
-  }
-  __syncthreads();
   for (int i = tid; i < n; i += kThreads) {
     const float* p = pr + (i / k) * k;
     float den = 0.f;
@@ -421,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     sm.bar_base = ld_relaxed_gpu(a.bar) / gridDim.x * gridDim.x;  // before this CTA's first arrival
     sm.bar_idx = 0;
   }
+  if (tid < 32) sm.cbits[tid] = 0u;
   // this CTA's slice of the shared expert's blob into L2 (its gate/up tasks run in C)
   if (a.has_shared && tid == 0) {
     const size_t slice = ((a.shared_bytes + ncta - 1) / ncta + 15) & ~size_t(15);
@@ -444,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
   uint4 wv0 = make_uint4(0u, 0u, 0u, 0u), wv1 = wv0;
   if (warp < npairs) {
     const uint4* wr = router_row(warp);
-    wv0 = __ldg(wr + lane);
-    wv1 = __ldg(wr + 32 + lane);
+    wv0 = ld_keep16(wr + lane, policy_evict_last());
+    wv1 = ld_keep16(wr + 32 + lane, policy_evict_last());
   }
   // x into shared memory (all loads of a thread in flight together), and the
   // layer's residency and staging rows for the lookups of phase B
@@ -459,6 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
       const int i = tid + j * kThreads;
       if (i < n16) v[j] = src[i];
     }
+    // the router bias of this CTA's rows, with the other loads (the logits add it at the end)
+    const int brow = cta + tid * ncta;
+    const float bv = (tid < nrows && brow < E && a.bias) ? __ldg(a.bias + brow) : 0.f;
     int32_t rv[kEVec], sv[kEVec];
 #pragma unroll
     for (int j = 0; j < kEVec; ++j) {
@@ -479,6 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
         sm.stage[e] = sv[j];
       }
     }
+    if (tid < nrows) sm.bias_r[tid] = bv;
   }
   // the expert kernels accumulate max|h| per row with atomicMax from phase C on
   if (lead) {
@@ -505,8 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
   for (int p = warp; p < npairs; p += kWarps) {
     if (p != warp) {
       const uint4* wr = router_row(p);
-      wv0 = __ldg(wr + lane);
-      wv1 = __ldg(wr + 32 + lane);
+      wv0 = ld_keep16(wr + lane, policy_evict_last());
+      wv1 = ld_keep16(wr + 32 + lane, policy_evict_last());
     }
     const int q = p % QS;
     float pacc[TP];
@@ -550,12 +607,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     float v = 0.f;
     for (int q = 0; q < QS; ++q) v += part[(j * QS + q) * kMaxT + t];
     if (row < E)
-      a.logits[size_t(t) * E + row] = a.bias ? __fadd_rn(v, a.bias[row]) : v;
+      a.logits[size_t(t) * E + row] = a.bias ? __fadd_rn(v, sm.bias_r[j]) : v;
     else
       a.gate_logit[t] = v;
   }
+  grid_arrive(a, sm);
   // x as f16 times the token's power of two (read by every gate/up unit), eight
-  // consecutive columns -- one 16-byte group of the permuted layout -- per item
+  // consecutive columns -- one 16-byte group of the permuted layout -- per item, while the
+  // other CTAs arrive
   for (int i = tid; i < T * H / 8; i += kThreads) {
     const int t = (i * 8) / H, c = i * 8 - t * H;
     const uint4 q = reinterpret_cast<const uint4*>(xs)[i];
@@ -569,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     }
     *reinterpret_cast<uint4*>(x16 + t * XR + perm_col(c)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
-  if (!grid_barrier(a, sm)) return;
+  if (!grid_wait(a, sm)) return;
 
   // ============================================================ B: top-k, groups
   {
@@ -594,11 +653,48 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     }
   }
   __syncthreads();
-  topk_ranked(lg, T, E, k, sm, err, cbest, cand, a.capc, sel, pr);
+  // The candidate experts' gate/up bytes (codes, then scales: two contiguous ranges of each
+  // blob) requested into L2 as soon as the candidates are known, before the ranks and the
+  // grouping: the candidates hold every selection.  The experts' bytes are taken as one
+  // range, expert after expert, of which CTA c requests the c-th share -- a few large
+  // requests per CTA -- from the last warp, which the ranks of up to 8 tokens leave idle.
+  topk_ranked(lg, T, E, k, sm, err, cbest, cand, a.capc, sel, pr, [&]() {
+    if (warp != kWarps - 1) return;
+    const uint32_t gu_c = a.lay.code_off[2] - a.lay.code_off[0], gu_s = a.lay.scale_off[2] - a.lay.scale_off[0];
+    const size_t per = size_t(gu_c) + gu_s;
+    const unsigned word = lane < ((E + 31) >> 5) ? sm.cbits[lane] : 0u;
+    const int cnt = __popc(word);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const size_t V = size_t(__shfl_sync(0xffffffffu, incl, 31)) * per;
+    const size_t share = ((V + ncta - 1) / ncta + 15) & ~size_t(15);
+    const size_t b0 = size_t(cta) * share, b1 = min(V, b0 + share);
+    for (size_t x = b0 / per; b0 < b1 && x * per < b1; ++x) {
+      const unsigned m = __ballot_sync(0xffffffffu, size_t(incl) > x);
+      const int L = __ffs(m) - 1;
+      const int nb = int(x) - __shfl_sync(0xffffffffu, incl - cnt, L);
+      const unsigned w = __shfl_sync(0xffffffffu, word, L);
+      if (lane == 0) {
+        const int e = L * 32 + int(__fns(w, 0, nb + 1));
+        const int slot = sm.resid[e], st = sm.stage[e];
+        const uint8_t* blob = (slot >= 0 && slot < a.nslots) ? a.slots + size_t(slot) * a.blob_bytes
+                              : (st >= 0 && st < a.nstaging) ? a.staging + size_t(st) * a.blob_bytes : nullptr;
+        const size_t s0 = max(b0, x * per) - x * per, s1 = min(b1, (x + 1) * per) - x * per;
+        if (blob && s0 < gu_c) prefetch_bulk_l2(blob + a.lay.code_off[0] + s0, uint32_t(min(s1, size_t(gu_c)) - s0));
+        if (blob && s1 > gu_c) {
+          const size_t c0 = max(s0, size_t(gu_c)) - gu_c;
+          prefetch_bulk_l2(blob + a.lay.scale_off[0] + c0, uint32_t(s1 - gu_c - c0));
+        }
+      }
+    }
+  });
   __syncthreads();
   // groups: the n selections sorted by (expert, position); position t*k + r orders like the
   // token.  n <= 256 < the CTA's threads: one entry per thread.
-  int my_start = 0;
   if (tid < n) {
     const uint32_t kk = sm.key[tid];
     int r = 0;
@@ -607,22 +703,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     sm.srt[r] = kk;
   }
   __syncthreads();
+  // the entries that start a group, as ballots over rounds of 32 that every warp takes
+  // (the same masks in every warp); a start's group is the number of starts before it
+  int G = 0, before = 0;
+  unsigned mine = 0u;
+  for (int r0 = 0; r0 < n; r0 += 32) {
+    const int j = r0 + lane;
+    const bool st = j < n && (j == 0 || (sm.srt[j - 1] >> 16) != (sm.srt[j] >> 16));
+    const unsigned m = __ballot_sync(0xffffffffu, st);
+    if (r0 < warp * 32) before += __popc(m);
+    else if (r0 == warp * 32) mine = m;
+    G += __popc(m);
+  }
   if (tid < n) {
     const uint32_t kk = sm.srt[tid];
     const int pos = int(kk & 0xffffu);
     sm.ent_pos[tid] = pos;
     sm.ent_tok[tid] = pos / k;
-    if (tid == 0 || (sm.srt[tid - 1] >> 16) != (kk >> 16)) {
-      my_start = 1;
-      int g = 0;  // distinct experts before this entry
-      for (int j = 1; j <= tid; ++j) g += (sm.srt[j - 1] >> 16) != (sm.srt[j] >> 16) ? 1 : 0;
+    if ((mine >> lane) & 1u) {
+      const int g = before + __popc(mine & ((1u << lane) - 1u));
       sm.gexp[g] = int(kk >> 16);
       sm.goff[g] = tid;
     }
   }
-  const int G = __syncthreads_count(my_start);
   const int Gt = G + a.has_shared;
   if (tid == 0) sm.goff[G] = n;
+  __syncthreads();
   // lookup of each routed group (the same tables in every CTA: the same result)
   for (int g = tid; g < G; g += kThreads) {
     const int e = sm.gexp[g], e0 = sm.goff[g], e1 = (g + 1 < G) ? sm.goff[g + 1] : n;
@@ -739,19 +845,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
 #pragma unroll
   for (int d = 0; d < kGD; ++d) load(warp + d * kWarps, rr[d]);
   if (tid == kThreads - 32) {
-    // every weight byte of the CTA's later gate/up units and of its down tasks into L2 --
-    // one bulk prefetch per group and region, the rows of consecutive tasks of a group
-    // being contiguous -- so the step's expert bytes stream from HBM at once
-    const int ta0 = t0 + min(t1 - t0, (kGD * kWarps + NCH - 1) / NCH);
-    for (int gi = ta0 / TPG; ta0 < t1 && gi <= (t1 - 1) / TPG; ++gi) {
-      const uint8_t* blob = sm.gblob[gi];
-      if (!blob) continue;
-      const int ta = max(ta0, gi * TPG) - gi * TPG, tb = min(t1, (gi + 1) * TPG) - gi * TPG;
-      for (int m = 0; m < 2; ++m) {
-        prefetch_bulk_l2(blob + a.lay.code_off[m] + size_t(ta) * 8 * H, uint32_t((tb - ta) * 8 * H));
-        prefetch_bulk_l2(blob + a.lay.scale_off[m] + size_t(ta) * H, uint32_t((tb - ta) * H));
-      }
-    }
+    // every weight byte of the CTA's down tasks into L2 -- one bulk prefetch per group and
+    // region, the rows of consecutive tasks of a group being contiguous
     for (int gi = d0 / NRB; d1 > d0 && gi <= (d1 - 1) / NRB; ++gi) {
       const uint8_t* blob = sm.gblob[gi];
       if (!blob) continue;
@@ -836,7 +931,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
     }
     __syncthreads();
   }
-  if (!grid_barrier(a, sm)) return;
+  grid_arrive(a, sm);
 
   // ============================================================ D: down
   // The CTA's tasks [d0, d1) in group order.  The h rows of every group of its range --
@@ -858,17 +953,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
       gi = task >> lNRB;
       rb = task & (NRB - 1);
     };
+    // three units in flight per warp (a unit is half a gate/up unit); the first ones (their
+    // weights in L2 by now, and no other CTA writes them) are requested between this CTA's
+    // arrival at the barrier and its wait, the h rows staged after the wait
+    auto load_d = [&](int u, int lim, UnitRegs<1>& R) {
+      if (u >= lim) return;
+      int gi, rb, ch;
+      unit_of(u, gi, rb, ch);
+      if (sm.gblob[gi]) load_unit<1>(sm.gblob[gi], a.lay, 2, I, rb * 16 + g8, ch, t4, R);
+    };
+    UnitRegs<1> da, db, dc;
+    load_d(warp, min(kUnitsDN, ud), da);
+    load_d(warp + kWarps, min(kUnitsDN, ud), db);
+    load_d(warp + 2 * kWarps, min(kUnitsDN, ud), dc);
+    if (!grid_wait(a, sm)) return;
     for (int q0 = 0; q0 < ud; q0 += kUnitsDN) {
       const int nq = min(kUnitsDN, ud - q0);
-      auto load_d = [&](int u, UnitRegs<1>& R) {
-        if (u >= q0 + nq) return;
-        int gi, rb, ch;
-        unit_of(u, gi, rb, ch);
-        if (sm.gblob[gi]) load_unit<1>(sm.gblob[gi], a.lay, 2, I, rb * 16 + g8, ch, t4, R);
-      };
-      // three units in flight per warp (a unit is half a gate/up unit), requested once the
-      // h rows are staged (their weights are in L2 by then; the rows' loads go first)
-      UnitRegs<1> da, db, dc;
       if (q0 == 0) {
         const int per = I / 4, lper = __ffs(per) - 1;
         constexpr int kB = 4;  // 16 rows of 512 in one batch
@@ -902,9 +1002,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
         }
         __syncthreads();  // the staged rows are complete
       }
-      load_d(q0 + warp, da);
-      load_d(q0 + warp + kWarps, db);
-      load_d(q0 + warp + 2 * kWarps, dc);
+      if (q0 > 0) {
+        load_d(q0 + warp, q0 + nq, da);
+        load_d(q0 + warp + kWarps, q0 + nq, db);
+        load_d(q0 + warp + 2 * kWarps, q0 + nq, dc);
+      }
       auto run_d = [&](int u, const UnitRegs<1>& R) {
         if (u >= q0 + nq) return;
         int gi, rb, ch;
@@ -928,11 +1030,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
       };
       for (int u = q0 + warp; u < q0 + nq; u += 3 * kWarps) {
         run_d(u, da);
-        load_d(u + 3 * kWarps, da);
+        load_d(u + 3 * kWarps, q0 + nq, da);
         run_d(u + kWarps, db);
-        load_d(u + 4 * kWarps, db);
+        load_d(u + 4 * kWarps, q0 + nq, db);
         run_d(u + 2 * kWarps, dc);
-        load_d(u + 5 * kWarps, dc);
+        load_d(u + 5 * kWarps, q0 + nq, dc);
       }
       __syncthreads();
       for (int idx = tid; idx < (nq / NCD) * 32; idx += kThreads) {
