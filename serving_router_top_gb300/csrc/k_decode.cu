@@ -344,7 +344,8 @@ __device__ __forceinline__ unsigned long long rank_key(float x, int e) {
 //      the token's best entry, is its best chunk best).
 // No step is a chain of warp-wide selections, which a decode step cannot afford (nor one
 // warp per token: its chain of dependent shared-memory and shuffle steps was measured
-// slower than the CTA-wide steps and their barriers).  Ids and weights equal the top-k
+// slower than the CTA-wide steps and their barriers); a warp takes its items of steps 1 and
+// 3 four at a time, their loads, reductions and atomics side by side.  Ids and weights equal the top-k
 // kernel's: the same order, and w_r = p_r / sum_j p_j summed in rank order.  NaN logits
 // rank as -inf and record MOE_ENAN.  Leaves key[i] = id << 16 | i for the grouping.  Every
 // thread of the CTA calls this; it holds four __syncthreads and ends without one.
@@ -355,20 +356,31 @@ __device__ void topk_ranked(const float* __restrict__ lg, int T, int E, int k, S
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NCH = (E + 31) >> 5;
   bool nan_seen = false;
-  for (int it = warp; it < T * NCH; it += kWarps) {
-    const int t = it / NCH, e = (it - t * NCH) * 32 + lane;
-    unsigned long long ck = 0ull;
-    if (e < E) {
-      float x = lg[t * E + e];
-      if (x != x) {
-        nan_seen = true;
-        x = -INFINITY;
+  // a warp's items four at a time: every load first, then the reductions
+  for (int it0 = warp; it0 < T * NCH; it0 += 4 * kWarps) {
+    unsigned long long ck[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int it = it0 + q * kWarps, t = it / NCH, e = (it - t * NCH) * 32 + lane;
+      ck[q] = 0ull;
+      if (it < T * NCH && e < E) {
+        float x = lg[t * E + e];
+        if (x != x) {
+          nan_seen = true;
+          x = -INFINITY;
+        }
+        ck[q] = rank_key(x, e);
       }
-      ck = rank_key(x, e);
     }
-    const unsigned hi = __reduce_max_sync(0xffffffffu, unsigned(ck >> 32));
-    const unsigned lo = __reduce_max_sync(0xffffffffu, unsigned(ck >> 32) == hi ? unsigned(ck) : 0u);
-    if (lane == 0) cbest[it] = (static_cast<unsigned long long>(hi) << 32) | lo;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int it = it0 + q * kWarps;
+      if (it < T * NCH) {
+        const unsigned hi = __reduce_max_sync(0xffffffffu, unsigned(ck[q] >> 32));
+        const unsigned lo = __reduce_max_sync(0xffffffffu, unsigned(ck[q] >> 32) == hi ? unsigned(ck[q]) : 0u);
+        if (lane == 0) cbest[it] = (static_cast<unsigned long long>(hi) << 32) | lo;
+      }
+    }
   }
   if (nan_seen) set_error(err, MOE_ENAN);
   if (tid < T) sm.ncand[tid] = 0;
@@ -386,26 +398,44 @@ __device__ void topk_ranked(const float* __restrict__ lg, int T, int E, int k, S
     if (lane < NCH && r == 0) sm.top[warp] = mine;
   }
   __syncthreads();
-  for (int it = warp; it < T * NCH; it += kWarps) {
-    const int t = it / NCH, e = (it - t * NCH) * 32 + lane;
-    unsigned long long ck = 0ull;
-    if (e < E) {
-      float x = lg[t * E + e];
-      if (x != x) x = -INFINITY;
-      ck = rank_key(x, e);
+  // four items at a time again: the loads, the ballots, the four atomics (independent),
+  // then the stores
+  for (int it0 = warp; it0 < T * NCH; it0 += 4 * kWarps) {
+    unsigned long long ck[4];
+    unsigned b[4];
+    int base[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int it = it0 + q * kWarps, t = it / NCH, e = (it - t * NCH) * 32 + lane;
+      ck[q] = 0ull;
+      bool take = false;
+      if (it < T * NCH && e < E) {
+        float x = lg[t * E + e];
+        if (x != x) x = -INFINITY;
+        ck[q] = rank_key(x, e);
+        take = ck[q] >= sm.tau[t];
+      }
+      b[q] = __ballot_sync(0xffffffffu, take);
     }
-    const bool take = e < E && ck >= sm.tau[t];
-    const unsigned b = __ballot_sync(0xffffffffu, take);
-    int base = 0;
-    if (lane == 0 && b) {
-      base = atomicAdd(&sm.ncand[t], __popc(b));
-      atomicOr(&sm.cbits[it - t * NCH], b);  // the candidate experts of all tokens
+    if (lane == 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int it = it0 + q * kWarps, t = it / NCH;
+        base[q] = 0;
+        if (b[q]) {
+          base[q] = atomicAdd(&sm.ncand[t], __popc(b[q]));
+          atomicOr(&sm.cbits[it - t * NCH], b[q]);  // the candidate experts of all tokens
+        }
+      }
     }
-    base = __shfl_sync(0xffffffffu, base, 0);
-    const int pos = base + __popc(b & ((1u << lane) - 1u));
-    if (take) {
-      if (pos < capc) cand[t * capc + pos] = ck;
-      else set_error(err, MOE_ERANGE);  // unreachable: at most min(E, 32 k) entries reach tau
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int it = it0 + q * kWarps, t = it / NCH;
+      const int pos = __shfl_sync(0xffffffffu, base[q], 0) + __popc(b[q] & ((1u << lane) - 1u));
+      if ((b[q] >> lane) & 1u) {
+        if (pos < capc) cand[t * capc + pos] = ck[q];
+        else set_error(err, MOE_ERANGE);  // unreachable: at most min(E, 32 k) entries reach tau
+      }
     }
   }
   __syncthreads();
@@ -762,7 +792,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const Args a) {
       a.grp_src[g] = src;
       a.grp_blob[g] = blob;
       atomicAdd(&sm.cnt[src == MOE_SRC_RESIDENT ? 0 : src == MOE_SRC_STAGED ? 1 : src == MOE_SRC_SKIPPED ? 3 : 2], 1);
-      if (a.heat_row) a.heat_row[e] = __fadd_rn(a.heat_row[e], float(e1 - e0));  // as the heat-update kernel
+      // as the heat-update kernel: one rounded add per expert (each is in one group), here a
+      // reduction that no thread waits for
+      if (a.heat_row) atomicAdd(a.heat_row + e, float(e1 - e0));
     }
   }
   if (a.has_shared && tid == 0) {
